@@ -1,0 +1,10 @@
+"""The oracle: a slow, plain fp64 CPU implementation of the PTPC-FP8 MoE layer.
+
+TEST INFRASTRUCTURE ONLY. It is what the CUDA path is checked against and it
+shares no code with that path. Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import it.
+"""
+
+from .fp8 import (E4M3_MAX, bf16_bits, bf16_from_bits, bf16_round,  # noqa: F401
+                  e4m3_decode, e4m3_encode)
+from .moe_ref import *  # noqa: F401,F403

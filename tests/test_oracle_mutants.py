@@ -1,0 +1,135 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each mutant replaces one oracle function with a plausibly wrong variant (a
+dropped term, a swapped operand, a wrong tie rule ...) on the CPU; the test
+runs the relevant pins against the mutated oracle and expects an assertion
+failure. This checks that the pins constrain every step of the oracle.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.moe_ref as ref
+from tests import test_oracle_layer as layer_pins
+from tests import test_oracle_route as route_pins
+
+
+def _mut_silu(g):
+    return ref.sigmoid_ref(g)                       # dropped the g factor
+
+
+def _mut_expert_ffn_swap(xq, sx, wgu, sgu, wd, sd):
+    I = wgu.shape[0] // 2
+    gu = ref.ptpc_matmul_ref(xq, sx, wgu, sgu)
+    h = ref.silu_ref(gu[:, I:]) * gu[:, :I]         # gate and up swapped
+    hq, sh = ref.quant_rows_ref(h.astype(np.float32))
+    return {"y": ref.ptpc_matmul_ref(hq, sh, wd, sd)}
+
+
+def _mut_expert_ffn_no_requant(xq, sx, wgu, sgu, wd, sd):
+    I = wgu.shape[0] // 2
+    gu = ref.ptpc_matmul_ref(xq, sx, wgu, sgu)
+    h = ref.silu_ref(gu[:, :I]) * gu[:, I:]
+    wdq = ref.dequant_rows_ref(wd, sd)
+    return {"y": h @ wdq.T}                         # h never quantised
+
+
+def _mut_ptpc_one_scale(a, sa, w, sw):
+    acc = ref.e4m3_decode(a) @ ref.e4m3_decode(w).T
+    return acc * np.asarray(sa, np.float64)[:, None]   # weight scale dropped
+
+
+def _mut_route_tie_high(logits, k, renormalize=True):
+    lg = np.asarray(logits, np.float32)
+    E = lg.shape[1]
+    rev = lg[:, ::-1]
+    order = (E - 1) - np.argsort(-rev, axis=1, kind="stable")  # ties -> higher
+    ids = order[:, :k].astype(np.int32)
+    ch = np.take_along_axis(lg, ids.astype(np.int64), 1).astype(np.float64)
+    p = np.exp(ch - ch[:, :1])
+    return ids, p / p.sum(1, keepdims=True)
+
+
+def _mut_route_no_renorm(logits, k, renormalize=True):
+    ids, _ = _orig_route(logits, k, renormalize)
+    lg = np.asarray(logits, np.float64)
+    p = np.exp(lg - lg.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    return ids, np.take_along_axis(p, ids.astype(np.int64), 1)
+
+
+def _mut_permute_unstable(ids, E):
+    counts, offsets, s2f, f2s = _orig_permute(ids, E)
+    s2f = s2f.copy()
+    for e in range(E):
+        s2f[offsets[e]:offsets[e + 1]] = s2f[offsets[e]:offsets[e + 1]][::-1]
+    f2s = np.empty_like(s2f)
+    f2s[s2f] = np.arange(s2f.size, dtype=s2f.dtype)
+    return counts, offsets, s2f, f2s
+
+
+def _mut_quant_wrong_max(v):
+    v32 = np.asarray(v, np.float32)
+    amax = np.abs(v32).max(1)
+    s = (np.maximum(amax, ref.QUANT_EPS) / np.float32(240)).astype(np.float32)
+    return ref.e4m3_encode((v32 / s[:, None]).astype(np.float32)), s
+
+
+def _mut_sigmoid_gate(z):
+    return np.ones_like(np.asarray(z, np.float64))       # shared gate ignored
+
+
+_orig_route = ref.route_ref
+_orig_permute = ref.permute_ref
+
+
+def _layer_pins():
+    for params in [(25, 128, 6, 3, 128, True, "normal"),
+                   (33, 256, 8, 2, 128, False, "weights")]:
+        layer_pins.test_layer_matches_dense_evaluation(*params)
+
+
+def _route_pins():
+    rng = np.random.default_rng(7)
+    for case in route_pins._cases():
+        route_pins.test_golden_cases(case)
+    route_pins.test_selection_properties_with_ties(rng, 6, 3)
+    route_pins.test_all_equal_logits()
+
+
+def _permute_pins():
+    rng = np.random.default_rng(7)
+    route_pins.test_permute_invariants(rng, 37, 8, 2)
+
+
+def _quant_pins():
+    rng = np.random.default_rng(7)
+    layer_pins.test_quant_matches_torch_quantiser(rng)
+
+
+MUTANTS = {
+    "silu_drops_g": (ref, "silu_ref", _mut_silu, _layer_pins),
+    "gate_up_swapped": (ref, "expert_ffn_ref", _mut_expert_ffn_swap, _layer_pins),
+    "no_requant": (ref, "expert_ffn_ref", _mut_expert_ffn_no_requant, _layer_pins),
+    "weight_scale_dropped": (ref, "ptpc_matmul_ref", _mut_ptpc_one_scale,
+                             _layer_pins),
+    "ties_to_higher_index": (ref, "route_ref", _mut_route_tie_high, _route_pins),
+    "no_renormalisation": (ref, "route_ref", _mut_route_no_renorm, _route_pins),
+    "unstable_permutation": (ref, "permute_ref", _mut_permute_unstable,
+                             _permute_pins),
+    "quant_wrong_fp8_max": (ref, "quant_rows_ref", _mut_quant_wrong_max,
+                            _quant_pins),
+    "shared_gate_ignored": (ref, "sigmoid_ref", _mut_sigmoid_gate, _layer_pins),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(monkeypatch, name):
+    module, attr, fn, pins = MUTANTS[name]
+    monkeypatch.setattr(module, attr, fn)
+    # the pin modules imported some oracle functions by name
+    for pin_mod in (layer_pins, route_pins):
+        if hasattr(pin_mod, attr):
+            monkeypatch.setattr(pin_mod, attr, fn)
+    with pytest.raises(AssertionError):
+        pins()
