@@ -28,8 +28,8 @@ _MIN_NORMAL_EXP = -6       # smallest normal exponent of e4m3
 _SUBNORMAL_QUANTUM = 2.0 ** -9
 
 
-def e4m3_decode(codes):
-    """Map e4m3 byte codes to their values (fp64). NaN codes give NaN."""
+def _decode_formula(codes):
+    """Value of each e4m3 code from its bit fields (fp64)."""
     c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
     sign = np.where(c & 0x80, -1.0, 1.0)
     exp_field = (c >> 3) & 0xF
@@ -41,13 +41,36 @@ def e4m3_decode(codes):
     return sign * val
 
 
+_DECODE_TABLE = _decode_formula(np.arange(256))
+
+
+def e4m3_decode(codes):
+    """Map e4m3 byte codes to their values (fp64). NaN codes give NaN.
+
+    A lookup in the 256-entry table of the bit-field formula above."""
+    return _DECODE_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+_CHUNK = 1 << 16
+
+
 def e4m3_encode(values):
     """Round fp32 values to e4m3 codes: nearest, ties to even, saturating.
 
     `values` is converted to fp32 first (the quantiser's inputs are fp32 on
-    both sides of the parity check), then handled exactly in fp64.
+    both sides of the parity check), then handled exactly in fp64, in chunks
+    that stay in cache.
     """
-    v = np.asarray(values, dtype=np.float32).astype(np.float64)
+    v32 = np.asarray(values, dtype=np.float32)
+    flat = v32.reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint8)
+    for i in range(0, flat.size, _CHUNK):
+        out[i:i + _CHUNK] = _encode_chunk(flat[i:i + _CHUNK])
+    return out.reshape(v32.shape)
+
+
+def _encode_chunk(v32):
+    v = v32.astype(np.float64)
     sign_bit = np.signbit(v).astype(np.uint8) << 7
     a = np.abs(v)
     nan = np.isnan(a)
