@@ -1,0 +1,288 @@
+"""Thin ctypes binding of libmoe_ptpc.so (declared in include/moe_ptpc.h).
+
+Argument marshalling only: every function here checks torch tensors' device,
+dtype and contiguity, allocates outputs with torch when the caller passes
+none, and forwards raw device pointers plus the current CUDA stream to the C
+entry point of the same name. All arithmetic runs in the library's kernels.
+The library is loaded on first use; if it is missing this raises instead of
+falling back to anything else.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_DTYPE_BF16 = 0
+MOE_DTYPE_F32 = 1
+MOE_GEMM_GATEUP_SWIGLU = 0
+MOE_GEMM_DOWN = 1
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("shared", ctypes.c_int32),
+                ("renormalize", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_version": (_I, []),
+    "moe_router_logits": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_route": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
+    "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quant_ptpc": (_I, [_P, _I, _I64, _I, _P, _I, _I64, _P, _P, _P]),
+    "moe_shared_gate": (_I, [_P, _P, _I, _I, _P, _P]),
+    "moe_grouped_gemm": (_I, [_I, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _I,
+                              _I, _P]),
+    "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_forward_workspace_size": (_SZ, [ctypes.POINTER(moe_dims)]),
+    "moe_forward": (_I, [ctypes.POINTER(moe_dims), _P, _P, _P, _P, _P, _P, _P,
+                         _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_profiled": (_I, [ctypes.POINTER(moe_dims), _P, _P, _P, _P, _P,
+                                  _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                  ctypes.POINTER(ctypes.c_void_p), _I, _P]),
+    "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+}
+
+MOE_FORWARD_EVENTS = 9
+
+_lib = None
+
+
+def load_library(path=None):
+    """Load (once) and return the ctypes handle of the library."""
+    global _lib
+    if _lib is None:
+        path = path or _build.library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "expert_layer_ptpc_gb300.build.build() (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_names():
+    return sorted(_SIGNATURES)
+
+
+def status_string(status):
+    return load_library().moe_status_string(status).decode()
+
+
+def _check(fn, status):
+    if status != 0:
+        raise MoeError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+def moe_router_logits(x, w_r, logits=None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(w_r, torch.bfloat16, "w_r")
+    T, D = x.shape
+    E = w_r.shape[0]
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _check("moe_router_logits", load_library().moe_router_logits(
+        _ptr(x), _ptr(w_r), T, E, D, _ptr(logits), _stream(stream)))
+    return logits
+
+
+def moe_route(logits, k, renormalize=True, ids=None, weights=None, stream=None):
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check("moe_route", load_library().moe_route(
+        _ptr(logits), T, E, k, int(bool(renormalize)), _ptr(ids), _ptr(weights),
+        _stream(stream)))
+    return ids, weights
+
+
+def moe_permute(ids, E, stream=None):
+    _need(ids, torch.int32, "topk_ids")
+    T, k = ids.shape
+    dev = ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    s2f = torch.empty(T * k, dtype=torch.int32, device=dev)
+    f2s = torch.empty(T * k, dtype=torch.int32, device=dev)
+    lib = load_library()
+    nws = lib.moe_permute_workspace_size(T, E, k)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+    _check("moe_permute", lib.moe_permute(
+        _ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(s2f), _ptr(f2s),
+        _ptr(ws), nws, _stream(stream)))
+    return counts, offsets, s2f, f2s
+
+
+def moe_quant_ptpc(inp, dst_rows=None, copies=1, extra_row_base=-1,
+                   out_rows=None, out_q=None, out_scale=None, stream=None):
+    """Per-row e4m3 quantisation of a [rows, cols] bf16 or fp32 tensor.
+    Returns (codes uint8 [out_rows, cols], scales fp32 [out_rows])."""
+    if inp.dtype == torch.bfloat16:
+        dt = MOE_DTYPE_BF16
+    elif inp.dtype == torch.float32:
+        dt = MOE_DTYPE_F32
+    else:
+        raise ValueError("input must be bf16 or fp32")
+    _need(inp, inp.dtype, "input")
+    rows, cols = inp.shape
+    if dst_rows is not None:
+        _need(dst_rows, torch.int32, "dst_rows")
+    if out_rows is None:
+        out_rows = rows if dst_rows is None else rows * copies
+        if extra_row_base >= 0:
+            out_rows = max(out_rows, extra_row_base + rows)
+    if out_q is None:
+        out_q = torch.empty((out_rows, cols), dtype=torch.uint8, device=inp.device)
+    if out_scale is None:
+        out_scale = torch.empty(out_rows, dtype=torch.float32, device=inp.device)
+    _check("moe_quant_ptpc", load_library().moe_quant_ptpc(
+        _ptr(inp), dt, rows, cols, _ptr(dst_rows), copies, extra_row_base,
+        _ptr(out_q), _ptr(out_scale), _stream(stream)))
+    return out_q, out_scale
+
+
+def moe_shared_gate(x, w_g, gate=None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(w_g, torch.bfloat16, "w_g")
+    T, D = x.shape
+    if gate is None:
+        gate = torch.empty(T, dtype=torch.float32, device=x.device)
+    _check("moe_shared_gate", load_library().moe_shared_gate(
+        _ptr(x), _ptr(w_g), T, D, _ptr(gate), _stream(stream)))
+    return gate
+
+
+def moe_grouped_gemm(kind, A, a_scale, W, w_scale, group_offsets, out=None,
+                     rows_hint=0, stream=None):
+    """kind MOE_GEMM_GATEUP_SWIGLU: W [G, 2N, K] -> out [rows, N] fp32;
+    kind MOE_GEMM_DOWN: W [G, N, K] -> out [rows, N] fp32."""
+    _need(A, torch.uint8, "A")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(W, torch.uint8, "W")
+    _need(w_scale, torch.float32, "w_scale")
+    _need(group_offsets, torch.int32, "group_offsets")
+    a_rows, K = A.shape
+    G = W.shape[0]
+    N = W.shape[1] // 2 if kind == MOE_GEMM_GATEUP_SWIGLU else W.shape[1]
+    if W.shape[2] != K or group_offsets.numel() != G + 1:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((a_rows, N), dtype=torch.float32, device=A.device)
+    _check("moe_grouped_gemm", load_library().moe_grouped_gemm(
+        kind, _ptr(A), _ptr(a_scale), a_rows, _ptr(W), _ptr(w_scale),
+        _ptr(group_offsets), G, N, K, _ptr(out), MOE_DTYPE_F32, rows_hint,
+        _stream(stream)))
+    return out
+
+
+def moe_combine(y, flat_to_sorted, topk_w, y_shared=None, shared_gate=None,
+                out=None, stream=None):
+    _need(y, torch.float32, "y")
+    _need(flat_to_sorted, torch.int32, "flat_to_sorted")
+    _need(topk_w, torch.float32, "topk_w")
+    T, k = topk_w.shape
+    D = y.shape[1]
+    if out is None:
+        out = torch.empty((T, D), dtype=torch.bfloat16, device=y.device)
+    _check("moe_combine", load_library().moe_combine(
+        _ptr(y), _ptr(flat_to_sorted), _ptr(topk_w), T, k, D, _ptr(y_shared),
+        _ptr(shared_gate), _ptr(out), _stream(stream)))
+    return out
+
+
+def make_dims(T, D, E, k, I, shared, renormalize=True):
+    return moe_dims(T, D, E, k, I, int(bool(shared)), int(bool(renormalize)))
+
+
+def moe_forward_workspace_size(dims):
+    return load_library().moe_forward_workspace_size(ctypes.byref(dims))
+
+
+def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,
+                router_w=None, shared_gate_w=None, out=None, ws=None,
+                topk_ids=None, topk_w=None, stream=None, events=None):
+    """The whole layer; returns out [T, D] bf16. `events`: optional list of
+    MOE_FORWARD_EVENTS torch.cuda.Event(enable_timing=True), recorded at the
+    step boundaries (moe_forward_profiled)."""
+    _need(x, torch.bfloat16, "x")
+    for t, n in ((w_gu, "w_gu"), (w_d, "w_d")):
+        _need(t, torch.uint8, n)
+    for t, n in ((s_gu, "s_gu"), (s_d, "s_d")):
+        _need(t, torch.float32, n)
+    if router_logits is not None:
+        _need(router_logits, torch.float32, "router_logits")
+    if router_w is not None:
+        _need(router_w, torch.bfloat16, "router_w")
+    if shared_gate_w is not None:
+        _need(shared_gate_w, torch.bfloat16, "shared_gate_w")
+    lib = load_library()
+    if out is None:
+        out = torch.empty((dims.T, dims.D), dtype=torch.bfloat16, device=x.device)
+    need = lib.moe_forward_workspace_size(ctypes.byref(dims))
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    args = (ctypes.byref(dims), _ptr(x), _ptr(router_logits), _ptr(router_w),
+            _ptr(w_gu), _ptr(s_gu), _ptr(w_d), _ptr(s_d), _ptr(shared_gate_w),
+            _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel())
+    if events is None:
+        _check("moe_forward", lib.moe_forward(*args, _stream(stream)))
+    else:
+        if len(events) != MOE_FORWARD_EVENTS:
+            raise ValueError(f"need {MOE_FORWARD_EVENTS} events")
+        handles = (ctypes.c_void_p * MOE_FORWARD_EVENTS)(
+            *[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check("moe_forward_profiled", lib.moe_forward_profiled(
+            *args, handles, MOE_FORWARD_EVENTS, _stream(stream)))
+    return out
+
+
+def moe_device_status(stream=None):
+    """Synchronise the stream and return (status, error bits)."""
+    detail = ctypes.c_uint(0)
+    st = load_library().moe_device_status(_stream(stream), ctypes.byref(detail))
+    return st, detail.value

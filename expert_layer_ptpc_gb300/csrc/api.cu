@@ -1,0 +1,358 @@
+// C ABI of the PTPC-FP8 MoE layer: argument checks, workspace layout and the
+// chaining of the kernels on the caller's stream. Declared in moe_ptpc.h.
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/moe_ptpc.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// Set by kernels whose bounded wait ran out; read and cleared by
+// moe_device_status().
+__device__ unsigned g_error_word;
+
+unsigned* device_error_word() {
+  static std::mutex mu;
+  static unsigned* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess)
+      addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+namespace {
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline int cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Byte offsets of the intermediates inside the moe_forward workspace.
+struct ForwardLayout {
+  size_t ids, w, logits, counts, offsets, s2f, f2s, perm, xq, sx, gate, h, hq,
+      sh, y, total;
+};
+
+ForwardLayout forward_layout(const moe_dims& d) {
+  const int64_t R = (int64_t)d.T * d.k;
+  const int64_t rows = R + (d.shared ? d.T : 0);
+  const int64_t G = (int64_t)d.E + (d.shared ? 1 : 0);
+  ForwardLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.ids = take(R * 4);
+  L.w = take(R * 4);
+  L.logits = take((size_t)d.T * d.E * 4);
+  L.counts = take(G * 4);
+  L.offsets = take((G + 1) * 4);
+  L.s2f = take(R * 4);
+  L.f2s = take(R * 4);
+  L.perm = take(permute_ws_bytes(R, d.E));
+  L.xq = take(rows * d.D);
+  L.sx = take(rows * 4);
+  L.gate = take((size_t)d.T * 4);
+  L.h = take(rows * d.I * 4);
+  L.hq = take(rows * d.I);
+  L.sh = take(rows * 4);
+  L.y = take(rows * d.D * 4);
+  L.total = off;
+  return L;
+}
+
+int check_dims(const moe_dims* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->D <= 0 || d->E <= 0 || d->I <= 0 || d->k <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->shared != 0 && d->shared != 1) return MOE_ERR_INVALID_ARG;
+  if (d->k > d->E || d->k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+  if (d->E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (d->D % 128 != 0 || d->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)d->T * (d->k + 1) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_router_logits(const uint16_t* x, const uint16_t* w_r, int T, int E,
+                      int D, float* logits, moe_stream_t stream) {
+  if (T < 0 || E <= 0 || D <= 0 || D % 2 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_r || !logits || !aligned16(x) || !aligned16(w_r))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_logits(x, w_r, T, E, D, logits, stream));
+}
+
+int moe_route(const float* logits, int T, int E, int k, int renormalize,
+              int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  if (T < 0 || E <= 0 || k < 1 || k > E || k > kMaxTopK)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_route(logits, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w, stream));
+}
+
+size_t moe_permute_workspace_size(int T, int E, int k) {
+  if (T < 0 || E <= 0 || k <= 0) return 0;
+  return permute_ws_bytes((int64_t)T * k, E);
+}
+
+int moe_permute(const int32_t* topk_ids, int T, int E, int k,
+                int32_t* expert_counts, int32_t* expert_offsets,
+                int32_t* sorted_to_flat, int32_t* flat_to_sorted, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || E <= 0 || k < 1 || k > E || k > kMaxTopK)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !sorted_to_flat || !flat_to_sorted))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = permute_ws_bytes((int64_t)T * k, E);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_permute(topk_ids, (int64_t)T * k, E, expert_counts,
+                                    expert_offsets, sorted_to_flat,
+                                    flat_to_sorted, -1, ws, stream));
+}
+
+int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
+                   const int32_t* dst_rows, int copies, int64_t extra_row_base,
+                   uint8_t* out_q, float* out_scale, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || copies < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (in_dtype != MOE_DTYPE_BF16 && in_dtype != MOE_DTYPE_F32)
+    return MOE_ERR_INVALID_ARG;
+  if (dst_rows == nullptr && copies != 1) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!in || !out_q || !out_scale || !aligned16(in) || !aligned16(out_q))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quant(in, in_dtype, rows, cols, dst_rows, copies,
+                                  extra_row_base, out_q, out_scale, nullptr,
+                                  nullptr, stream));
+}
+
+int moe_shared_gate(const uint16_t* x, const uint16_t* w_g, int T, int D,
+                    float* gate, moe_stream_t stream) {
+  if (T < 0 || D <= 0 || D % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_g || !gate || !aligned16(x) || !aligned16(w_g))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_shared_gate(x, w_g, T, D, gate, stream));
+}
+
+int moe_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
+                     int64_t a_rows, const uint8_t* W, const float* w_scale,
+                     const int32_t* group_offsets, int groups, int N, int K,
+                     void* out, int out_dtype, int rows_hint,
+                     moe_stream_t stream) {
+  if (kind != MOE_GEMM_GATEUP_SWIGLU && kind != MOE_GEMM_DOWN)
+    return MOE_ERR_INVALID_ARG;
+  if (a_rows < 0 || groups < 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (out_dtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
+  if (groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  if (a_rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (a_rows == 0 || groups == 0) return MOE_OK;
+  if (!A || !a_scale || !W || !w_scale || !group_offsets || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  return launch_grouped_gemm(kind, A, a_scale, a_rows, W, w_scale, group_offsets,
+                             groups, N, K, static_cast<float*>(out), rows_hint,
+                             stream);
+}
+
+int moe_combine(const float* y, const int32_t* flat_to_sorted,
+                const float* topk_w, int T, int k, int D, const float* y_shared,
+                const float* shared_gate, uint16_t* out, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || D <= 0 || D % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((y_shared == nullptr) != (shared_gate == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y || !flat_to_sorted || !topk_w || !out || !aligned16(y) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (y_shared != nullptr && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(y, flat_to_sorted, topk_w, T, k, D, y_shared,
+                                    shared_gate, out, stream));
+}
+
+size_t moe_forward_workspace_size(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return forward_layout(*dims).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+int forward_impl(const moe_dims* dims, const uint16_t* x,
+                 const float* router_logits, const uint16_t* router_w,
+                 const uint8_t* w_gu, const float* s_gu, const uint8_t* w_d,
+                 const float* s_d, const uint16_t* shared_gate_w, uint16_t* out,
+                 int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                 size_t ws_bytes, cudaEvent_t const* ev, cudaStream_t stream) {
+  auto mark = [&](int i) {
+    if (ev != nullptr) cudaEventRecord(ev[i], stream);
+  };
+  int st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims d = *dims;
+  if (d.T == 0) return MOE_OK;   // empty batch: nothing to read or write
+  if ((router_logits == nullptr) == (router_w == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (d.shared && shared_gate_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!d.shared && shared_gate_w != nullptr) return MOE_ERR_INVALID_ARG;
+  if (!x || !w_gu || !s_gu || !w_d || !s_d || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gu) || !aligned16(w_d) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (router_w != nullptr && !aligned16(router_w)) return MOE_ERR_INVALID_ARG;
+  if (shared_gate_w != nullptr && !aligned16(shared_gate_w)) return MOE_ERR_INVALID_ARG;
+  const ForwardLayout L = forward_layout(d);
+  if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+  const int64_t R = (int64_t)d.T * d.k;
+  const int64_t rows = R + (d.shared ? d.T : 0);
+  const int G = d.E + (d.shared ? 1 : 0);
+  int32_t* ids = topk_ids_out ? topk_ids_out : static_cast<int32_t*>(at(L.ids));
+  float* tw = topk_w_out ? topk_w_out : static_cast<float*>(at(L.w));
+  auto* counts = static_cast<int32_t*>(at(L.counts));
+  auto* offsets = static_cast<int32_t*>(at(L.offsets));
+  auto* s2f = static_cast<int32_t*>(at(L.s2f));
+  auto* f2s = static_cast<int32_t*>(at(L.f2s));
+  auto* xq = static_cast<uint8_t*>(at(L.xq));
+  auto* sx = static_cast<float*>(at(L.sx));
+  auto* gate = static_cast<float*>(at(L.gate));
+  auto* h = static_cast<float*>(at(L.h));
+  auto* hq = static_cast<uint8_t*>(at(L.hq));
+  auto* sh = static_cast<float*>(at(L.sh));
+  auto* y = static_cast<float*>(at(L.y));
+
+  mark(0);
+  const float* logits = router_logits;
+  if (router_w != nullptr) {
+    auto* lg = static_cast<float*>(at(L.logits));
+    st = cuda_status(launch_router_logits(x, router_w, d.T, d.E, d.D, lg, stream));
+    if (st != MOE_OK) return st;
+    logits = lg;
+  }
+  mark(1);
+  st = cuda_status(launch_route(logits, d.T, d.E, d.k, d.renormalize ? 1 : 0, ids,
+                                tw, stream));
+  if (st != MOE_OK) return st;
+  mark(2);
+  st = cuda_status(launch_permute(ids, R, d.E, counts, offsets, s2f, f2s,
+                                  d.shared ? d.T : -1, at(L.perm), stream));
+  if (st != MOE_OK) return st;
+  mark(3);
+  // x -> FP8 codes written straight into each token's k expert rows (and its
+  // shared-expert row R + t), plus the shared-expert gate.
+  st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
+                                d.shared ? R : -1, xq, sx,
+                                d.shared ? shared_gate_w : nullptr,
+                                d.shared ? gate : nullptr, stream));
+  if (st != MOE_OK) return st;
+  mark(4);
+  const int hint = (int)std::max<int64_t>(1, R / d.E);
+  st = launch_grouped_gemm(MOE_GEMM_GATEUP_SWIGLU, xq, sx, rows, w_gu, s_gu,
+                           offsets, G, d.I, d.D, h, hint, stream);
+  if (st != MOE_OK) return st;
+  mark(5);
+  st = cuda_status(launch_quant(h, MOE_DTYPE_F32, rows, d.I, nullptr, 1, -1, hq,
+                                sh, nullptr, nullptr, stream));
+  if (st != MOE_OK) return st;
+  mark(6);
+  st = launch_grouped_gemm(MOE_GEMM_DOWN, hq, sh, rows, w_d, s_d, offsets, G,
+                           d.D, d.I, y, hint, stream);
+  if (st != MOE_OK) return st;
+  mark(7);
+  st = cuda_status(launch_combine(y, f2s, tw, d.T, d.k, d.D,
+                                  d.shared ? y + R * d.D : nullptr,
+                                  d.shared ? gate : nullptr, out, stream));
+  if (st != MOE_OK) return st;
+  mark(8);
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward(const moe_dims* dims, const uint16_t* x,
+                const float* router_logits, const uint16_t* router_w,
+                const uint8_t* w_gu, const float* s_gu, const uint8_t* w_d,
+                const float* s_d, const uint16_t* shared_gate_w, uint16_t* out,
+                int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+  return forward_impl(dims, x, router_logits, router_w, w_gu, s_gu, w_d, s_d,
+                      shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
+                      nullptr, stream);
+}
+
+int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
+                         const float* router_logits, const uint16_t* router_w,
+                         const uint8_t* w_gu, const float* s_gu,
+                         const uint8_t* w_d, const float* s_d,
+                         const uint16_t* shared_gate_w, uint16_t* out,
+                         int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                         size_t ws_bytes, void* const* events, int n_events,
+                         moe_stream_t stream) {
+  if (events == nullptr || n_events != MOE_FORWARD_EVENTS) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_events; ++i)
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  return forward_impl(dims, x, router_logits, router_w, w_gu, s_gu, w_d, s_d,
+                      shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
+                      reinterpret_cast<cudaEvent_t const*>(events), stream);
+}
+
+int moe_device_status(moe_stream_t stream, unsigned* detail) {
+  if (detail) *detail = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (word != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (detail) *detail = word;
+  return word != 0 ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Unpermute and top-k-weighted combine back to bf16.
+//
+// "Optimizing Qwen 3.5 397B MoE on Ironwood TPU7x", SparseCore unpermute
+// paragraph: the expert outputs are gathered back per token by the routing
+// map and reduced locally, without materialising padded intermediates.
+//
+//   out[t] = bf16_rne( sum_{j<k} w[t, j] * y[flat_to_sorted[t k + j]]
+//                      + gate[t] * y_shared[t] )
+// summed in fp32, slot order j = 0..k-1, shared term last.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kVec = 8;   // elements per thread per step (2 x float4 in, 16 B out)
+
+__global__ void __launch_bounds__(512) combine_kernel(
+    const float* __restrict__ y, const int32_t* __restrict__ f2s,
+    const float* __restrict__ topk_w, int k, int D,
+    const float* __restrict__ y_shared, const float* __restrict__ gate,
+    __nv_bfloat16* __restrict__ out) {
+  const int t = blockIdx.x;
+  __shared__ int32_t rows[kMaxTopK];
+  __shared__ float wts[kMaxTopK];
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = f2s[(int64_t)t * k + threadIdx.x];
+    wts[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const float g = y_shared != nullptr ? gate[t] : 0.f;
+  for (int c = threadIdx.x * kVec; c < D; c += blockDim.x * kVec) {
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const float* src = y + (int64_t)rows[j] * D + c;
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 b = *reinterpret_cast<const float4*>(src + 4);
+      const float w = wts[j];
+      acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+      acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+      acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
+      acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+    }
+    if (y_shared != nullptr) {
+      const float* src = y_shared + (int64_t)t * D + c;
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 b = *reinterpret_cast<const float4*>(src + 4);
+      acc[0] = fmaf(g, a.x, acc[0]); acc[1] = fmaf(g, a.y, acc[1]);
+      acc[2] = fmaf(g, a.z, acc[2]); acc[3] = fmaf(g, a.w, acc[3]);
+      acc[4] = fmaf(g, b.x, acc[4]); acc[5] = fmaf(g, b.y, acc[5]);
+      acc[6] = fmaf(g, b.z, acc[6]); acc[7] = fmaf(g, b.w, acc[7]);
+    }
+    uint4 packed;
+    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    *reinterpret_cast<uint4*>(out + (int64_t)t * D + c) = packed;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y, const int32_t* f2s,
+                           const float* topk_w, int T, int k, int D,
+                           const float* y_shared, const float* shared_gate,
+                           uint16_t* out, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  int threads = D / kVec;
+  if (threads > 512) threads = 512;
+  threads = ((threads + 31) / 32) * 32;
+  combine_kernel<<<T, threads, 0, stream>>>(
+      y, f2s, topk_w, k, D, y_shared, shared_gate,
+      reinterpret_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

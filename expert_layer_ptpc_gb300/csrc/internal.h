@@ -1,0 +1,59 @@
+// Internal launchers behind the C ABI. Each validates nothing (api.cu does)
+// and enqueues its kernels on `stream`.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxGroups = kMaxExperts + 1;
+
+// Address of the device error word of the current device.
+unsigned* device_error_word();
+
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_r, int T,
+                                 int E, int D, float* logits,
+                                 cudaStream_t stream);
+
+cudaError_t launch_route(const float* logits, int T, int E, int k,
+                         int renormalize, int32_t* ids, float* w,
+                         cudaStream_t stream);
+
+// Scratch bytes of the permutation for R = T * k flat entries.
+size_t permute_ws_bytes(int64_t R, int E);
+
+// Histogram, scan and stable scatter. `extra_group_rows` >= 0 appends one more
+// group (index E) of that many rows after the routed ones: counts[E] and
+// offsets[E + 1] are written too (the shared expert's rows R .. R + T - 1).
+cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
+                           int32_t* counts, int32_t* offsets, int32_t* s2f,
+                           int32_t* f2s, int extra_group_rows, void* ws,
+                           cudaStream_t stream);
+
+// Per-row e4m3 quantisation with scatter; `gate_w` non-null also computes
+// gate_out[r] = sigmoid(in[r] . gate_w) (bf16 input only).
+cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
+                         const int32_t* dst_rows, int copies,
+                         int64_t extra_row_base, uint8_t* out_q,
+                         float* out_scale, const uint16_t* gate_w,
+                         float* gate_out, cudaStream_t stream);
+
+cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
+                               int D, float* gate, cudaStream_t stream);
+
+// Returns a moe_status.
+int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
+                        int64_t a_rows, const uint8_t* W, const float* w_scale,
+                        const int32_t* offsets, int groups, int N, int K,
+                        float* out, int rows_hint, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* y, const int32_t* f2s,
+                           const float* topk_w, int T, int k, int D,
+                           const float* y_shared, const float* shared_gate,
+                           uint16_t* out, cudaStream_t stream);
+
+}  // namespace moe

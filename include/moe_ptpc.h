@@ -1,0 +1,254 @@
+/*
+ * moe_ptpc.h - C ABI of the GB300 (sm_103a) PTPC-FP8 Mixture-of-Experts layer.
+ *
+ * The layer ("Optimizing Qwen 3.5 397B MoE on Ironwood TPU7x", the MoE
+ * paragraph of the model description, and its SparseCore / GMM V2 paragraphs;
+ * "Ultimate Latency Optimization of Qwen3 and Qwen3-VL on AMD MI300X Series",
+ * sections 2.1.1, 2.1.4 and 2.1.5):
+ *
+ *   logits -> softmax top-k routing -> histogram + prefix sum + permutation
+ *   into expert-contiguous rows -> per-token FP8 e4m3 quantisation ->
+ *   grouped gate/up GEMM with fused SwiGLU -> per-token requantisation ->
+ *   grouped down GEMM -> top-k-weighted unpermute-combine to bf16.
+ *
+ * PTPC ("per-token activation, per-channel weight", section 2.1.1 and Figure 3
+ * of the MI300X page): every activation row carries one fp32 scale, every
+ * weight output channel one fp32 scale, and a GEMM output element is
+ *   out[r, n] = s_a[r] * s_w[n] * sum_k qa[r, k] * qw[n, k].
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers owned by the caller unless a parameter says
+ *    otherwise; nothing here allocates device memory, and every call is
+ *    asynchronous on `stream` (NULL = the legacy default stream).
+ *  - Matrices are row-major with the reduction dimension contiguous.
+ *  - bf16 values are passed as uint16_t bit patterns; FP8 values as uint8_t
+ *    e4m3 codes (OCP "E4M3": bias 7, max 448, no infinities).
+ *  - The return value is a status (moe_status) for argument and launch
+ *    errors, known before the kernels run. Errors found by a running kernel
+ *    (a bounded wait that expired) are reported by moe_device_status().
+ *  - Device pointers must be 16-byte aligned. D and I must be multiples of
+ *    128; 1 <= k <= min(E, 32); E <= 1024.
+ *  - NaN or infinite inputs are outside the contract.
+ */
+#ifndef MOE_PTPC_H
+#define MOE_PTPC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* A CUDA stream (cudaStream_t). */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer  */
+  MOE_ERR_UNSUPPORTED = -2, /* valid but outside the supported shapes      */
+  MOE_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed        */
+  MOE_ERR_WORKSPACE = -4,   /* workspace missing or too small              */
+  MOE_ERR_TIMEOUT = -5      /* a kernel's bounded wait expired             */
+} moe_status;
+
+typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
+
+typedef enum moe_gemm_kind {
+  MOE_GEMM_GATEUP_SWIGLU = 0, /* h = silu(x Wg^T) * (x Wu^T), fp32 out      */
+  MOE_GEMM_DOWN = 1           /* y = h Wd^T, fp32 out                        */
+} moe_gemm_kind;
+
+/* Dimensions of one layer call. */
+typedef struct moe_dims {
+  int32_t T;           /* tokens                                             */
+  int32_t D;           /* hidden size                                        */
+  int32_t E;           /* routed experts                                     */
+  int32_t k;           /* experts per token                                  */
+  int32_t I;           /* expert intermediate size                           */
+  int32_t shared;      /* 1: one always-on shared expert of size I, else 0   */
+  int32_t renormalize; /* 1: top-k weights renormalised to sum to 1          */
+} moe_dims;
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MOE_API int moe_version(void);
+
+/*
+ * moe_router_logits - router gate projection ("Optimizing Qwen 3.5 397B MoE
+ * on Ironwood TPU7x", MoE paragraph: the router gate projects each token).
+ *   logits[t, e] = sum_d x[t, d] * w_r[e, d], accumulated in fp64 and rounded
+ *   once to fp32, so the fp32 logits are the exactly rounded dot products.
+ *   x      [T, D] bf16;  w_r [E, D] bf16;  logits [T, E] fp32 (written).
+ * Errors: MOE_ERR_INVALID_ARG for null pointers or non-positive sizes.
+ */
+MOE_API int moe_router_logits(const uint16_t* x, const uint16_t* w_r, int T,
+                              int E, int D, float* logits, moe_stream_t stream);
+
+/*
+ * moe_route - softmax top-k routing (same paragraph; the [tokens, k] id and
+ * weight arrays of the TPU page's expert-parallel routing paragraph).
+ *   Per token: the k largest fp32 logits, ties to the lower expert index, in
+ *   descending order; topk_w[t, j] = softmax probability of the chosen expert,
+ *   renormalised over the k chosen when `renormalize` (a softmax over the k
+ *   chosen logits), else the plain softmax over all E. fp32 arithmetic.
+ *   logits [T, E] fp32;  topk_ids [T, k] int32 and topk_w [T, k] fp32 (written).
+ * Errors: MOE_ERR_INVALID_ARG (null, T < 0, k outside 1..min(E, 32)),
+ *         MOE_ERR_UNSUPPORTED (E > 1024).  T == 0 is a no-op.
+ */
+MOE_API int moe_route(const float* logits, int T, int E, int k, int renormalize,
+                      int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/*
+ * moe_permute - expert histogram, prefix sum and stable permutation (TPU
+ * page, SparseCore permute paragraph: rows gathered into expert-contiguous
+ * order with no padding).
+ *   With flat index f = t * k + j and R = T * k:
+ *   expert_counts[e]  = #{f : topk_ids[f] == e}                 [E]
+ *   expert_offsets    = exclusive prefix sum of counts          [E + 1]
+ *   sorted_to_flat[s] = flat index stored at sorted row s        [R]
+ *   flat_to_sorted[f] = sorted row of flat index f               [R]
+ *   Rows of one expert keep ascending f (a stable counting sort), so every
+ *   output is unique and deterministic.
+ *   ws: device scratch of at least moe_permute_workspace_size(T, E, k) bytes.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (E > 1024),
+ *         MOE_ERR_WORKSPACE.  Ids outside [0, E) are outside the contract.
+ */
+MOE_API size_t moe_permute_workspace_size(int T, int E, int k);
+MOE_API int moe_permute(const int32_t* topk_ids, int T, int E, int k,
+                        int32_t* expert_counts, int32_t* expert_offsets,
+                        int32_t* sorted_to_flat, int32_t* flat_to_sorted,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_quant_ptpc - per-row FP8 e4m3 quantisation with optional scatter
+ * (MI300X page, section 2.1.1: per-token activation and per-channel weight
+ * scales; section 2.1.5: per-token quantisation fused into the producer).
+ *   For each row r < rows of `in` [rows, cols] (bf16 or fp32):
+ *     s_r = fp32(max(amax_r, 1e-12) / 448),  q = e4m3_rne_sat(fp32(v / s_r)),
+ *   both divisions IEEE fp32. A weight matrix W[N, K] quantised with this
+ *   call gets one scale per output channel.
+ *   Destinations: if dst_rows is NULL, row r goes to output row r (copies must
+ *   be 1); else to rows dst_rows[r * copies + c] for c < copies. If
+ *   extra_row_base >= 0 it is also written to row extra_row_base + r.
+ *   out_q [*, cols] uint8 and out_scale [*] fp32 are indexed by output row.
+ * Errors: MOE_ERR_INVALID_ARG (null, cols not a positive multiple of 16,
+ *         bad dtype, copies < 1).
+ */
+MOE_API int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
+                           const int32_t* dst_rows, int copies,
+                           int64_t extra_row_base, uint8_t* out_q,
+                           float* out_scale, moe_stream_t stream);
+
+/*
+ * moe_shared_gate - shared-expert gate sigmoid(x[t] . w_g), fp32 (the TPU
+ * page's shared expert runs on every token; its gate is a sigmoid).
+ *   x [T, D] bf16;  w_g [D] bf16;  gate [T] fp32 (written).
+ */
+MOE_API int moe_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
+                            int D, float* gate, moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm - PTPC FP8 grouped GEMM on the tcgen05 tensor cores (TPU
+ * page, GMM V2 paragraph: gate and up packed in one tile with SwiGLU fused,
+ * ragged per-expert row slices with no padding).
+ *   Group g owns activation rows [group_offsets[g], group_offsets[g + 1]) of
+ *   A [a_rows, K] (e4m3, row scales a_scale [a_rows]); group_offsets is a
+ *   DEVICE array of groups + 1 non-decreasing entries <= a_rows.
+ *   MOE_GEMM_GATEUP_SWIGLU: W [groups, 2N, K] (rows 0..N-1 gate, N..2N-1 up),
+ *     w_scale [groups, 2N]; out [a_rows, N] fp32:
+ *       g = s_a s_wg (qa . qwg),  u = s_a s_wu (qa . qwu),  h = g sigmoid(g) u.
+ *   MOE_GEMM_DOWN: W [groups, N, K], w_scale [groups, N]; out [a_rows, N] fp32:
+ *       y = s_a s_w (qa . qw).
+ *   Rows outside every group are not written. Zero-row groups read nothing.
+ *   rows_hint: expected rows per non-empty group (<= 0: a_rows / groups); it
+ *   only selects the token-tile width.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (N or K not multiples of
+ *         128, out_dtype not MOE_DTYPE_F32, groups > 1025), MOE_ERR_CUDA.
+ */
+MOE_API int moe_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
+                             int64_t a_rows, const uint8_t* W,
+                             const float* w_scale, const int32_t* group_offsets,
+                             int groups, int N, int K, void* out, int out_dtype,
+                             int rows_hint, moe_stream_t stream);
+
+/*
+ * moe_combine - unpermute and top-k-weighted reduction back to bf16 (TPU
+ * page, SparseCore unpermute paragraph: indirect gather plus local reduce).
+ *   out[t, :] = bf16_rne( sum_{j<k} topk_w[t, j] * y[flat_to_sorted[t k + j], :]
+ *                         + shared_gate[t] * y_shared[t, :] )
+ *   summed in fp32 in slot order j = 0..k-1, the shared term last.
+ *   y [*, D] fp32; flat_to_sorted [T * k]; topk_w [T, k] fp32;
+ *   y_shared [T, D] fp32 and shared_gate [T] fp32, both NULL when there is no
+ *   shared expert; out [T, D] bf16 (written).
+ */
+MOE_API int moe_combine(const float* y, const int32_t* flat_to_sorted,
+                        const float* topk_w, int T, int k, int D,
+                        const float* y_shared, const float* shared_gate,
+                        uint16_t* out, moe_stream_t stream);
+
+/*
+ * moe_forward - the whole layer, every step above chained on `stream`.
+ *   x [T, D] bf16. Router input: exactly one of router_logits [T, E] fp32 and
+ *   router_w [E, D] bf16 (then the logits are computed by moe_router_logits).
+ *   Weights, pre-quantised per output channel with moe_quant_ptpc:
+ *     w_gu [G, 2I, D] e4m3, s_gu [G, 2I];  w_d [G, D, I] e4m3, s_d [G, D],
+ *   where G = E + dims->shared and group E is the shared expert.
+ *   shared_gate_w [D] bf16 when dims->shared, else NULL.
+ *   out [T, D] bf16 (written). topk_ids_out [T, k] / topk_w_out [T, k]:
+ *   optional, receive the routing when non-NULL.
+ *   ws: device workspace of moe_forward_workspace_size(dims) bytes; it holds
+ *   the routing, permutation, quantised activations and GEMM intermediates.
+ * Errors: those of the steps; MOE_ERR_WORKSPACE if ws_bytes is too small.
+ */
+MOE_API size_t moe_forward_workspace_size(const moe_dims* dims);
+MOE_API int moe_forward(const moe_dims* dims, const uint16_t* x,
+                        const float* router_logits, const uint16_t* router_w,
+                        const uint8_t* w_gu, const float* s_gu,
+                        const uint8_t* w_d, const float* s_d,
+                        const uint16_t* shared_gate_w, uint16_t* out,
+                        int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                        size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_forward_profiled - moe_forward with timing marks: identical work and
+ *   arguments, plus `events`, an array of MOE_FORWARD_EVENTS cudaEvent_t
+ *   created by the caller, recorded on `stream` at the step boundaries:
+ *   [0] start, [1] after the router projection (no-op without router_w),
+ *   [2] after routing, [3] after the permutation, [4] after the x
+ *   quantisation, [5] after the gate/up GEMM, [6] after the requantisation,
+ *   [7] after the down GEMM, [8] after the combine.
+ * Errors: those of moe_forward; MOE_ERR_INVALID_ARG if n_events differs.
+ */
+#define MOE_FORWARD_EVENTS 9
+MOE_API int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
+                                 const float* router_logits,
+                                 const uint16_t* router_w, const uint8_t* w_gu,
+                                 const float* s_gu, const uint8_t* w_d,
+                                 const float* s_d,
+                                 const uint16_t* shared_gate_w, uint16_t* out,
+                                 int32_t* topk_ids_out, float* topk_w_out,
+                                 void* ws, size_t ws_bytes, void* const* events,
+                                 int n_events, moe_stream_t stream);
+
+/*
+ * moe_device_status - synchronise `stream`, then read and clear the device
+ * error word that kernels set when a bounded wait expires. Returns MOE_OK,
+ * MOE_ERR_TIMEOUT, or MOE_ERR_CUDA if the stream reported a CUDA error.
+ * `detail` (nullable) receives the raw error bits.
+ */
+MOE_API int moe_device_status(moe_stream_t stream, unsigned* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_PTPC_H */

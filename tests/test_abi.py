@@ -1,0 +1,74 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry point
+include/moe_ptpc.h declares; host-side argument checks answer without
+touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from expert_layer_ptpc_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
+                      "moe_ptpc.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for n in ["moe_route", "moe_permute", "moe_quant_ptpc", "moe_grouped_gemm",
+              "moe_combine", "moe_forward"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_the_header(lib):
+    assert binding.exported_names() == _declared()
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    assert "workspace" in binding.status_string(-4)
+    assert lib.moe_version() >= 100
+
+
+def test_argument_errors_need_no_gpu(lib):
+    # invalid k, E too large, misaligned / null pointers: rejected on the host
+    assert lib.moe_route(None, 4, 8, 0, 1, None, None, None) == -1
+    assert lib.moe_route(None, 4, 2048, 2, 1, None, None, None) == -2
+    assert lib.moe_route(None, 0, 8, 2, 1, None, None, None) == 0   # empty
+    assert lib.moe_quant_ptpc(None, 0, 4, 100, None, 1, -1, None, None,
+                              None) == -1                          # cols % 16
+    assert lib.moe_grouped_gemm(0, None, None, 8, None, None, None, 2, 100,
+                                256, None, 1, 0, None) == -2       # N % 128
+    d = binding.make_dims(16, 4096, 128, 8, 1536, False)
+    need = lib.moe_forward_workspace_size(ctypes.byref(d))
+    assert need > 16 * 8 * 4
+    bad = binding.make_dims(16, 4000, 128, 8, 1536, False)
+    assert lib.moe_forward_workspace_size(ctypes.byref(bad)) == 0
+    assert lib.moe_forward(ctypes.byref(bad), *([None] * 12), 0, None) == -2
+    # workspace too small is reported before any launch
+    fake = ctypes.c_void_p(0x1000)
+    rc = lib.moe_forward(ctypes.byref(d), fake, fake, None, fake, fake, fake,
+                         fake, None, fake, None, None, fake, 16, None)
+    assert rc == -4
+
+
+def test_permute_workspace_size(lib):
+    assert lib.moe_permute_workspace_size(16, 128, 8) == 0          # one block
+    assert lib.moe_permute_workspace_size(8192, 128, 8) == 8 * 128 * 4

@@ -1,0 +1,179 @@
+"""End-to-end parity of moe_forward (through the C ABI) against the oracle.
+
+Small layers are checked on every token. The five workloads run at their full
+sizes, in the launch configuration the benchmark uses; there the oracle
+evaluates a seeded sample of tokens (every output row depends only on its own
+token once the routing is fixed) while the routing and the permutation are
+compared bit for bit on all tokens. The GPU-quantised weights of every expert
+the sample touches are compared byte for byte with the oracle's.
+
+Accuracy contract on bf16 outputs: max|gpu - oracle| <= 2e-2 * rms(oracle) and
+sum|gpu - oracle| / sum|oracle| <= 5e-3."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_layer_ptpc_gb300 import synthetic as syn
+from tests.gpu_helpers import (U32, ensure_library, layer_tolerance_ok,
+                               quantize_experts, require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    require_gpu()
+    ensure_library()
+
+
+class _Run:
+    """A layer on the GPU plus the oracle's view of the same inputs."""
+
+    def __init__(self, cfg, seed=0):
+        from expert_layer_ptpc_gb300.layer import MoELayer
+        self.cfg = cfg
+        self.seed = seed
+        self.layer = MoELayer.synthetic(cfg, "cuda", seed)
+        self.qcache = {}
+
+    def inputs(self, cfg):
+        x = syn.gen_x(cfg, "cuda", self.seed)
+        logits = (None if cfg.router == "weights"
+                  else syn.gen_logits(cfg, "cuda", self.seed))
+        return x, logits
+
+    def expert_weights(self, es):
+        missing = [e for e in es if e not in self.qcache]
+        raw = []
+        for e in missing:
+            gu, d = syn.gen_expert_weights(self.cfg, e, "cuda", self.seed)
+            raw.append((gu.cpu().numpy(), d.cpu().numpy()))
+        for e, q in zip(missing, quantize_experts(raw)):
+            self.qcache[e] = q
+            # the GPU's own quantisation of this expert, byte for byte
+            L = self.layer
+            assert np.array_equal(L.w_gu[e].cpu().numpy(), q[0]), e
+            assert np.array_equal(L.s_gu[e].cpu().numpy().view(np.uint32),
+                                  q[1].view(np.uint32)), e
+            assert np.array_equal(L.w_d[e].cpu().numpy(), q[2]), e
+            assert np.array_equal(L.s_d[e].cpu().numpy().view(np.uint32),
+                                  q[3].view(np.uint32)), e
+        return {e: self.qcache[e] for e in es}
+
+    def check(self, cfg, n_sample=None):
+        from expert_layer_ptpc_gb300 import binding
+        T, k, E = cfg.T, cfg.k, cfg.E
+        x, logits = self.inputs(cfg)
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        out = self.layer.forward(x, logits, topk_ids=ids, topk_w=tw)
+        st, bits = binding.moe_device_status()
+        assert st == 0, f"device status {st} bits {bits:#x}"
+
+        xn = x.float().cpu().numpy()
+        if logits is None:
+            ln = oracle.router_logits_ref(
+                xn, self.layer.router_w.float().cpu().numpy())
+        else:
+            ln = logits.cpu().numpy()
+        rid, rw = oracle.route_ref(ln, k, cfg.renormalize)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=64 * U32, atol=0)
+        # permutation of the same ids, full size, bit-exact
+        counts, offs, s2f, f2s = binding.moe_permute(ids, E)
+        rc, ro, rs, rf = oracle.permute_ref(rid, E)
+        assert np.array_equal(counts.cpu().numpy(), rc)
+        assert np.array_equal(offs.cpu().numpy(), ro)
+        assert np.array_equal(s2f.cpu().numpy(), rs)
+        assert np.array_equal(f2s.cpu().numpy(), rf)
+
+        if n_sample is None or n_sample >= T:
+            tokens = np.arange(T)
+        else:
+            rng = np.random.default_rng(T + 17)
+            tokens = np.sort(rng.choice(T, n_sample, replace=False))
+            tokens[0] = 0
+            tokens[-1] = T - 1            # first and last token always
+        touched = sorted(set(int(e) for e in rid[tokens].ravel()))
+        if cfg.shared:
+            touched.append(E)
+        qmap = self.expert_weights(touched)
+        wg = (self.layer.shared_gate_w.float().cpu().numpy()
+              if cfg.shared else None)
+        r = oracle.moe_forward_ref(
+            xn, k, lambda e: qmap[e], E, logits=ln, w_g=wg,
+            renormalize=cfg.renormalize, tokens=tokens)
+        got = out.float().cpu().numpy()[tokens]
+        ok, max_rel, l1 = layer_tolerance_ok(got, r["out64"])
+        assert ok, f"{cfg.name}: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
+        return max_rel, l1
+
+
+# ---------------------------------------------------------------------------
+# small layers, every token
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [
+    syn.LayerConfig("s1", 300, 512, 16, 4, 256, True, "normal"),
+    syn.LayerConfig("s2", 97, 256, 8, 8, 128, False, "normal"),
+    syn.LayerConfig("s3", 50, 384, 32, 3, 384, False, "normal", False),
+    syn.LayerConfig("s4", 1, 256, 64, 6, 128, True, "normal"),
+    syn.LayerConfig("s5", 129, 256, 1, 1, 256, False, "normal"),
+    syn.LayerConfig("s6", 40, 256, 12, 2, 128, True, "weights"),
+], ids=lambda c: c.name)
+def test_small_layer_all_tokens(cfg):
+    _Run(cfg).check(cfg)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size
+# ---------------------------------------------------------------------------
+def test_tiny_layer():
+    cfg = syn.CONFIGS["tiny"]
+    _Run(cfg).check(cfg)
+
+
+def test_decode_layer():
+    cfg = syn.CONFIGS["decode"]
+    _Run(cfg).check(cfg)
+
+
+def test_prefill_layer():
+    cfg = syn.CONFIGS["prefill"]
+    _Run(cfg).check(cfg, n_sample=6)
+
+
+def test_skewed_layer():
+    cfg = syn.CONFIGS["skewed"]
+    _Run(cfg).check(cfg, n_sample=24)
+
+
+@pytest.fixture(scope="module")
+def sweep_run():
+    return _Run(syn.CONFIGS["sweep"])
+
+
+@pytest.mark.parametrize("T", syn.SWEEP_T)
+def test_sweep_layer(sweep_run, T):
+    cfg = syn.sweep_config(T)
+    sweep_run.check(cfg, n_sample=4)
+
+
+def test_forward_is_deterministic():
+    cfg = syn.LayerConfig("det", 2000, 512, 32, 4, 256, True, "normal")
+    run = _Run(cfg)
+    x, logits = run.inputs(cfg)
+    a = run.layer.forward(x, logits).clone()
+    b = run.layer.forward(x, logits).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_empty_batch_is_noop():
+    cfg = syn.LayerConfig("empty", 0, 256, 8, 2, 128, False, "normal")
+    run = _Run(syn.LayerConfig("empty", 4, 256, 8, 2, 128, False, "normal"))
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((0, 8), dtype=torch.float32, device="cuda")
+    out = run.layer.forward(x, lg)
+    assert out.shape == (0, 256)
+    assert cfg.T == 0

@@ -1,0 +1,268 @@
+"""Per-entry-point parity of the CUDA path against the oracle, through the C
+ABI, on seeded inputs small enough for the full oracle: several tiles, ragged
+tails, empty experts and the degenerate cases of each step.
+
+Bars: routing ids, counts, offsets, the permutation, FP8 codes and scales are
+bit-exact; floating-point outputs stay within bounds derived from fp32
+arithmetic (stated at each check)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_helpers import U32, ensure_library, gemm_bound, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    require_gpu()
+    ensure_library()
+
+
+def B():
+    from expert_layer_ptpc_gb300 import binding
+    return binding
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# ---------------------------------------------------------------------------
+# router projection
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,E,D", [(64, 8, 256), (5, 3, 128), (33, 64, 4096)])
+def test_router_logits_exact(T, E, D):
+    g = torch.Generator().manual_seed(T * 1000 + E)
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16)
+    w = (torch.randn(E, D, generator=g) * 0.02).to(torch.bfloat16)
+    got = B().moe_router_logits(x.cuda(), w.cuda()).cpu().numpy()
+    ref = oracle.router_logits_ref(x.float().numpy(), w.float().numpy())
+    # fp64 sums of exact products, one rounding: equal except for a double
+    # rounding at an fp32 midpoint, which would differ by one ulp
+    diff = np.abs(got.view(np.int32).astype(np.int64) - ref.view(np.int32))
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.999
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,E,k,renorm,ties", [
+    (64, 8, 2, True, False), (100, 128, 8, True, False),
+    (37, 512, 10, True, False), (16, 1024, 32, True, False),
+    (50, 64, 6, False, False), (200, 16, 5, True, True),
+    (31, 32, 32, True, True), (7, 1, 1, True, False), (9, 40, 1, False, True),
+])
+def test_route(T, E, k, renorm, ties):
+    rng = np.random.default_rng(T + E + k)
+    if ties:
+        logits = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    else:
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+    ids, w = B().moe_route(cuda(logits), k, renormalize=renorm)
+    rid, rw = oracle.route_ref(logits, k, renormalize=renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    # fp32 exp and sum over <= 32 terms: a few ulps relative
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=64 * U32, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# permutation
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,E,k,skew", [
+    (64, 8, 2, False), (1, 512, 10, False), (16, 128, 8, False),
+    (3000, 64, 6, True), (8192, 128, 8, False), (4096, 256, 8, True),
+    (20000, 1024, 4, True), (5, 7, 7, False),
+])
+def test_permute(T, E, k, skew):
+    rng = np.random.default_rng(T * 7 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    if skew:   # many experts empty
+        logits[:, : E // 2] -= 20.0
+    ids, _ = oracle.route_ref(logits, k)
+    counts, offsets, s2f, f2s = B().moe_permute(cuda(ids), E)
+    rc, ro, rs, rf = oracle.permute_ref(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(s2f.cpu().numpy(), rs)
+    assert np.array_equal(f2s.cpu().numpy(), rf)
+
+
+# ---------------------------------------------------------------------------
+# quantisation
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,rows,cols", [
+    ("bf16", 64, 256), ("bf16", 33, 4096), ("f32", 130, 1536),
+    ("f32", 7, 128), ("bf16", 5, 16), ("f32", 3, 8192),
+])
+def test_quant_exact(dtype, rows, cols):
+    rng = np.random.default_rng(rows * cols)
+    v = (rng.standard_normal((rows, cols)) *
+         np.exp(rng.uniform(-10, 10, size=(rows, 1)))).astype(np.float32)
+    v[0] = 0.0                                   # zero row
+    if rows > 2:
+        v[1, :] = 1e-30                          # scale from the 1e-12 floor
+        v[2, ::3] = 0.0
+    t = torch.from_numpy(v)
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+        v = t.float().numpy()
+    q, s = B().moe_quant_ptpc(t.cuda())
+    rq, rs = oracle.quant_rows_ref(v)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_scatter_with_extra_rows():
+    rng = np.random.default_rng(3)
+    T, D, k = 40, 512, 3
+    x = torch.from_numpy(rng.standard_normal((T, D)).astype(np.float32)).to(
+        torch.bfloat16)
+    perm = rng.permutation(T * k).astype(np.int32)
+    R = T * k
+    q, s = B().moe_quant_ptpc(x.cuda(), dst_rows=cuda(perm), copies=k,
+                              extra_row_base=R, out_rows=R + T)
+    rq, rs = oracle.quant_rows_ref(x.float().numpy())
+    q = q.cpu().numpy()
+    s = s.cpu().numpy()
+    for f in range(R):
+        assert np.array_equal(q[perm[f]], rq[f // k])
+        assert s[perm[f]] == rs[f // k]
+    assert np.array_equal(q[R:], rq)
+    assert np.array_equal(s[R:], rs)
+
+
+def test_shared_gate():
+    rng = np.random.default_rng(4)
+    x = torch.from_numpy(rng.standard_normal((70, 2048)).astype(np.float32)).to(
+        torch.bfloat16)
+    wg = (torch.from_numpy(rng.standard_normal(2048).astype(np.float32)) *
+          0.02).to(torch.bfloat16)
+    got = B().moe_shared_gate(x.cuda(), wg.cuda()).cpu().numpy()
+    ref = oracle.shared_gate_ref(x.float().numpy(), wg.float().numpy())
+    # fp32 dot of 2048 exact products (relative to sum|x w|) then expf
+    absdot = np.abs(x.float().numpy()) @ np.abs(wg.float().numpy())
+    bound = (2048 * U32) * absdot * ref * (1 - ref) + 8 * U32
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+# ---------------------------------------------------------------------------
+# grouped GEMMs
+# ---------------------------------------------------------------------------
+def _grouped_case(G, counts, N, K, gateup, seed):
+    rng = np.random.default_rng(seed)
+    rows = int(sum(counts))
+    a = rng.standard_normal((rows, K)).astype(np.float32)
+    aq, sa = oracle.quant_rows_ref(a)
+    wn = 2 * N if gateup else N
+    w = (rng.standard_normal((G, wn, K)) / np.sqrt(K)).astype(np.float32)
+    wq = np.empty((G, wn, K), np.uint8)
+    sw = np.empty((G, wn), np.float32)
+    for g in range(G):
+        wq[g], sw[g] = oracle.quant_rows_ref(w[g])
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return aq, sa, wq, sw, offs
+
+
+def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
+    G = wq.shape[0]
+    rows = aq.shape[0]
+    out = np.zeros((rows, N))
+    bound = np.zeros((rows, N))
+    adec = oracle.e4m3_decode(aq)
+    for g in range(G):
+        r0, r1 = offs[g], offs[g + 1]
+        if r1 == r0:
+            continue
+        full = oracle.ptpc_matmul_ref(aq[r0:r1], sa[r0:r1], wq[g], sw[g])
+        absacc = (np.abs(adec[r0:r1]) @ np.abs(oracle.e4m3_decode(wq[g])).T) * \
+            sa[r0:r1, None].astype(np.float64) * sw[g][None, :].astype(np.float64)
+        K = aq.shape[1]
+        if gateup:
+            gg, uu = full[:, :N], full[:, N:]
+            eg = gemm_bound(absacc[:, :N], K)
+            eu = gemm_bound(absacc[:, N:], K)
+            sig = oracle.sigmoid_ref(gg)
+            silu = gg * sig
+            dsilu = np.abs(sig * (1 + gg * (1 - sig)))
+            out[r0:r1] = silu * uu
+            # first-order propagation plus the fp32 evaluation of silu * u
+            bound[r0:r1] = dsilu * np.abs(uu) * eg + np.abs(silu) * eu + \
+                16 * U32 * np.abs(silu * uu) + 1e-30
+        else:
+            out[r0:r1] = full
+            bound[r0:r1] = gemm_bound(absacc, K) + 1e-30
+    return out, bound
+
+
+@pytest.mark.parametrize("gateup", [True, False])
+@pytest.mark.parametrize("G,counts,N,K,hint", [
+    (4, [3, 0, 17, 1], 128, 256, 0),                 # BN 16, ragged, empty
+    (8, [40, 33, 0, 0, 64, 1, 90, 7], 256, 512, 0),  # BN 32
+    (3, [200, 129, 64], 128, 1024, 0),               # BN 128 / 64
+    (5, [300, 0, 257, 511, 2], 384, 384, 0),         # BN 128 / 256, tails
+    (2, [1000, 24], 128, 4096, 0),                   # long K
+    (6, [5, 9, 0, 300, 2, 3], 256, 256, 16),         # hint forces BN 16
+])
+def test_grouped_gemm(gateup, G, counts, N, K, hint):
+    aq, sa, wq, sw, offs = _grouped_case(G, counts, N, K, gateup,
+                                         seed=G * 100 + N + K)
+    kind = 0 if gateup else 1
+    out = B().moe_grouped_gemm(kind, cuda(aq), cuda(sa), cuda(wq), cuda(sw),
+                               cuda(offs), rows_hint=hint)
+    st, bits = B().moe_device_status()
+    assert st == 0, bits
+    got = out.cpu().numpy().astype(np.float64)
+    ref, bound = _ref_grouped(aq, sa, wq, sw, offs, N, gateup)
+    err = np.abs(got - ref)
+    bad = err > bound
+    assert not bad.any(), (np.argwhere(bad)[:5], err[bad][:5], bound[bad][:5])
+
+
+def test_grouped_gemm_leaves_other_rows_alone():
+    # rows before the first group and after the last are not written
+    aq, sa, wq, sw, offs = _grouped_case(3, [10, 0, 20], 128, 256, False, 9)
+    offs = offs + 5
+    aq = np.concatenate([np.zeros((5, 256), np.uint8), aq,
+                         np.zeros((7, 256), np.uint8)])
+    sa = np.concatenate([np.ones(5, np.float32), sa, np.ones(7, np.float32)])
+    out = torch.full((42, 128), 7.0, device="cuda")
+    B().moe_grouped_gemm(1, cuda(aq), cuda(sa), cuda(wq), cuda(sw), cuda(offs),
+                         out=out)
+    o = out.cpu().numpy()
+    assert np.all(o[:5] == 7.0) and np.all(o[35:] == 7.0)
+
+
+# ---------------------------------------------------------------------------
+# combine
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,k,D,shared", [(64, 2, 256, False), (17, 8, 4096, True),
+                                          (5, 10, 1024, True), (1, 1, 128, False)])
+def test_combine(T, k, D, shared):
+    rng = np.random.default_rng(T * k + D)
+    R = T * k
+    y = rng.standard_normal((R + (T if shared else 0), D)).astype(np.float32)
+    f2s = rng.permutation(R).astype(np.int32)
+    w = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    gate = rng.uniform(0, 1, T).astype(np.float32) if shared else None
+    ys = y[R:] if shared else None
+    out = B().moe_combine(cuda(y), cuda(f2s), cuda(w),
+                          y_shared=cuda(ys) if shared else None,
+                          shared_gate=cuda(gate) if shared else None)
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = np.zeros((T, D))
+    absref = np.zeros((T, D))
+    for t in range(T):
+        for j in range(k):
+            term = w[t, j].astype(np.float64) * y[f2s[t * k + j]]
+            ref[t] += term
+            absref[t] += np.abs(term)
+        if shared:
+            ref[t] += gate[t].astype(np.float64) * ys[t]
+            absref[t] += np.abs(gate[t].astype(np.float64) * ys[t])
+    # fp32 sum of k+1 products, then one bf16 rounding (half a bf16 ulp)
+    bound = (k + 2) * U32 * absref + 2.0 ** -8 * np.abs(ref) * (1 + 1e-6)
+    assert np.all(np.abs(got - ref) <= bound + 1e-30)
