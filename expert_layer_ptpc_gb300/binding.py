@@ -46,6 +46,7 @@ _SIGNATURES = {
     "moe_route": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_ptpc": (_I, [_P, _I, _I64, _I, _P, _I, _I64, _P, _P, _P]),
     "moe_shared_gate": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_grouped_gemm": (_I, [_I, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _I,
@@ -155,6 +156,21 @@ def moe_permute(ids, E, stream=None):
     _check("moe_permute", lib.moe_permute(
         _ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(s2f), _ptr(f2s),
         _ptr(ws), nws, _stream(stream)))
+    return counts, offsets, s2f, f2s
+
+
+def moe_permute_noalloc(ids, E, counts, offsets, s2f, f2s, stream=None):
+    """moe_permute without a workspace: the library's fixed scratch array is
+    used (see include/moe_ptpc.h for its limit and sharing rules). All output
+    tensors are supplied by the caller; nothing is allocated."""
+    _need(ids, torch.int32, "topk_ids")
+    for t, n in ((counts, "expert_counts"), (offsets, "expert_offsets"),
+                 (s2f, "sorted_to_flat"), (f2s, "flat_to_sorted")):
+        _need(t, torch.int32, n)
+    T, k = ids.shape
+    _check("moe_permute_noalloc", load_library().moe_permute_noalloc(
+        _ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(s2f), _ptr(f2s),
+        _stream(stream)))
     return counts, offsets, s2f, f2s
 
 

@@ -129,6 +129,29 @@ MOE_API int moe_permute(const int32_t* topk_ids, int T, int E, int k,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_permute_noalloc - the same permutation as moe_permute, for callers that
+ * cannot allocate device memory. The pages have no counterpart of this entry
+ * point; it exists for hosts that embed the layer in a framework which has
+ * already reserved the device memory in its own arena, or serving loops that
+ * may not call cudaMalloc/cudaFree (both synchronise the device).
+ *   Inputs, outputs, results and errors are those of moe_permute; there is no
+ *   workspace argument. Scratch: a fixed 1 MiB device array inside the
+ *   library (held on every GPU that loads the library until the process
+ *   exits), enough for T * k <= 8192 * floor(262144 / E) flat entries (for
+ *   E = 128: 16,777,216; for E = 1024: 2,097,152). Larger calls return
+ *   MOE_ERR_UNSUPPORTED before launching anything.
+ *   The first call on each device (with that device current) looks up the
+ *   array's device address; make it before any stream capture on the device.
+ *   All calls share the array and it keeps the last call's contents (nothing
+ *   in it needs to start at zero): calls whose kernels overlap on the GPU race
+ *   on it, so the caller must serialise them. Allocates nothing.
+ */
+MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int T, int E, int k,
+                                int32_t* expert_counts, int32_t* expert_offsets,
+                                int32_t* sorted_to_flat,
+                                int32_t* flat_to_sorted, moe_stream_t stream);
+
+/*
  * moe_quant_ptpc - per-row FP8 e4m3 quantisation with optional scatter
  * (MI300X page, section 2.1.1: per-token activation and per-channel weight
  * scales; section 2.1.5: per-token quantisation fused into the producer).
