@@ -114,7 +114,7 @@ int moe_router_logits(const uint16_t* x, const uint16_t* w_r, int T, int E,
   if (T == 0) return MOE_OK;
   if (!x || !w_r || !logits || !aligned16(x) || !aligned16(w_r))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_router_logits(x, w_r, T, E, D, logits, stream));
+  return cuda_status(launch_router_logits(x, w_r, T, E, D, logits, stream, false));
 }
 
 int moe_route(const float* logits, int T, int E, int k, int renormalize,
@@ -125,7 +125,8 @@ int moe_route(const float* logits, int T, int E, int k, int renormalize,
   if (T == 0) return MOE_OK;
   if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   return cuda_status(
-      launch_route(logits, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w, stream));
+      launch_route(logits, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w, stream,
+                   false));
 }
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
@@ -148,7 +149,7 @@ int moe_permute(const int32_t* topk_ids, int T, int E, int k,
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_permute(topk_ids, (int64_t)T * k, E, expert_counts,
                                     expert_offsets, sorted_to_flat,
-                                    flat_to_sorted, -1, ws, stream));
+                                    flat_to_sorted, -1, ws, stream, false));
 }
 
 int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
@@ -156,6 +157,7 @@ int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
                    uint8_t* out_q, float* out_scale, moe_stream_t stream) {
   if (rows < 0 || cols <= 0 || cols % 16 != 0 || copies < 1)
     return MOE_ERR_INVALID_ARG;
+  if (cols > kMaxQuantCols || copies > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (in_dtype != MOE_DTYPE_BF16 && in_dtype != MOE_DTYPE_F32)
     return MOE_ERR_INVALID_ARG;
   if (dst_rows == nullptr && copies != 1) return MOE_ERR_INVALID_ARG;
@@ -164,12 +166,12 @@ int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_quant(in, in_dtype, rows, cols, dst_rows, copies,
                                   extra_row_base, out_q, out_scale, nullptr,
-                                  nullptr, stream));
+                                  nullptr, stream, false));
 }
 
 int moe_shared_gate(const uint16_t* x, const uint16_t* w_g, int T, int D,
                     float* gate, moe_stream_t stream) {
-  if (T < 0 || D <= 0 || D % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || D <= 0 || D % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !w_g || !gate || !aligned16(x) || !aligned16(w_g))
     return MOE_ERR_INVALID_ARG;
@@ -194,7 +196,7 @@ int moe_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   if (!aligned16(A) || !aligned16(W) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   return launch_grouped_gemm(kind, A, a_scale, a_rows, W, w_scale, group_offsets,
                              groups, N, K, static_cast<float*>(out), rows_hint,
-                             stream);
+                             stream, false);
 }
 
 int moe_combine(const float* y, const int32_t* flat_to_sorted,
@@ -208,7 +210,7 @@ int moe_combine(const float* y, const int32_t* flat_to_sorted,
     return MOE_ERR_INVALID_ARG;
   if (y_shared != nullptr && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_combine(y, flat_to_sorted, topk_w, T, k, D, y_shared,
-                                    shared_gate, out, stream));
+                                    shared_gate, out, stream, false));
 }
 
 size_t moe_forward_workspace_size(const moe_dims* dims) {
@@ -267,17 +269,22 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
   const float* logits = router_logits;
   if (router_w != nullptr) {
     auto* lg = static_cast<float*>(at(L.logits));
-    st = cuda_status(launch_router_logits(x, router_w, d.T, d.E, d.D, lg, stream));
+    st = cuda_status(
+        launch_router_logits(x, router_w, d.T, d.E, d.D, lg, stream, false));
     if (st != MOE_OK) return st;
     logits = lg;
   }
   mark(1);
+  // Kernels after the first overlap their launch with the previous kernel's
+  // tail (programmatic dependent launch); each orders itself with pdl_wait().
+  // Event marks between the steps serialise them instead.
+  const bool pdl = ev == nullptr;
   st = cuda_status(launch_route(logits, d.T, d.E, d.k, d.renormalize ? 1 : 0, ids,
-                                tw, stream));
+                                tw, stream, pdl && router_w != nullptr));
   if (st != MOE_OK) return st;
   mark(2);
   st = cuda_status(launch_permute(ids, R, d.E, counts, offsets, s2f, f2s,
-                                  d.shared ? d.T : -1, at(L.perm), stream));
+                                  d.shared ? d.T : -1, at(L.perm), stream, pdl));
   if (st != MOE_OK) return st;
   mark(3);
   // x -> FP8 codes written straight into each token's k expert rows (and its
@@ -285,25 +292,25 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
   st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
                                 d.shared ? R : -1, xq, sx,
                                 d.shared ? shared_gate_w : nullptr,
-                                d.shared ? gate : nullptr, stream));
+                                d.shared ? gate : nullptr, stream, pdl));
   if (st != MOE_OK) return st;
   mark(4);
   const int hint = (int)std::max<int64_t>(1, R / d.E);
   st = launch_grouped_gemm(MOE_GEMM_GATEUP_SWIGLU, xq, sx, rows, w_gu, s_gu,
-                           offsets, G, d.I, d.D, h, hint, stream);
+                           offsets, G, d.I, d.D, h, hint, stream, pdl);
   if (st != MOE_OK) return st;
   mark(5);
   st = cuda_status(launch_quant(h, MOE_DTYPE_F32, rows, d.I, nullptr, 1, -1, hq,
-                                sh, nullptr, nullptr, stream));
+                                sh, nullptr, nullptr, stream, pdl));
   if (st != MOE_OK) return st;
   mark(6);
   st = launch_grouped_gemm(MOE_GEMM_DOWN, hq, sh, rows, w_d, s_d, offsets, G,
-                           d.D, d.I, y, hint, stream);
+                           d.D, d.I, y, hint, stream, pdl);
   if (st != MOE_OK) return st;
   mark(7);
   st = cuda_status(launch_combine(y, f2s, tw, d.T, d.k, d.D,
                                   d.shared ? y + R * d.D : nullptr,
-                                  d.shared ? gate : nullptr, out, stream));
+                                  d.shared ? gate : nullptr, out, stream, pdl));
   if (st != MOE_OK) return st;
   mark(8);
   return MOE_OK;

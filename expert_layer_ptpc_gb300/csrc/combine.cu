@@ -14,9 +14,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kVec = 8;   // elements per thread per step (2 x float4 in, 16 B out)
+constexpr int kVec = 8;        // elements per thread (2 x float4 in, 16 B out)
+constexpr int kThreads = 128;  // a block covers 1024 columns of one token
 
-__global__ void __launch_bounds__(512) combine_kernel(
+__global__ void __launch_bounds__(kThreads) combine_kernel(
     const float* __restrict__ y, const int32_t* __restrict__ f2s,
     const float* __restrict__ topk_w, int k, int D,
     const float* __restrict__ y_shared, const float* __restrict__ gate,
@@ -24,13 +25,16 @@ __global__ void __launch_bounds__(512) combine_kernel(
   const int t = blockIdx.x;
   __shared__ int32_t rows[kMaxTopK];
   __shared__ float wts[kMaxTopK];
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x < k) {
     rows[threadIdx.x] = f2s[(int64_t)t * k + threadIdx.x];
     wts[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
   }
   __syncthreads();
   const float g = y_shared != nullptr ? gate[t] : 0.f;
-  for (int c = threadIdx.x * kVec; c < D; c += blockDim.x * kVec) {
+  const int c = (blockIdx.y * kThreads + threadIdx.x) * kVec;
+  if (c < D) {
     float acc[kVec];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) acc[i] = 0.f;
@@ -66,15 +70,12 @@ __global__ void __launch_bounds__(512) combine_kernel(
 cudaError_t launch_combine(const float* y, const int32_t* f2s,
                            const float* topk_w, int T, int k, int D,
                            const float* y_shared, const float* shared_gate,
-                           uint16_t* out, cudaStream_t stream) {
+                           uint16_t* out, cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
-  int threads = D / kVec;
-  if (threads > 512) threads = 512;
-  threads = ((threads + 31) / 32) * 32;
-  combine_kernel<<<T, threads, 0, stream>>>(
-      y, f2s, topk_w, k, D, y_shared, shared_gate,
-      reinterpret_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  const dim3 grid((unsigned)T, (unsigned)((D / kVec + kThreads - 1) / kThreads));
+  return launch_kernel(pdl, grid, dim3(kThreads), 0, stream, combine_kernel, y,
+                       f2s, topk_w, k, D, y_shared, shared_gate,
+                       reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace moe

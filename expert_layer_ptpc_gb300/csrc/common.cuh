@@ -52,6 +52,25 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Block until every grid this one depends on has completed and its memory is
+// visible. A no-op when the kernel was launched without the programmatic
+// serialization attribute (it then starts after its predecessor anyway).
+// Every kernel of the forward executes it in every thread before touching
+// data produced by the kernel launched just before it.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to be scheduled. Issued only after
+// pdl_wait(), so when kernel N+1 starts, kernel N-1 has completed: N+1 may
+// read N-1's outputs (and anything older) before its own pdl_wait().
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -210,12 +210,40 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
+      // The weights and the tile map (offsets come from the permutation, two
+      // launches back) do not depend on the previous kernel: stream the first
+      // stages' weight tiles before waiting for it, then add the activations.
+      const int first = blockIdx.x;
+      int npre = 0;
+      TileInfo t0{};
+      int w0 = 0;
+      if (first < total_tiles) {
+        t0 = decode_tile(first, prefix, groups, offsets, BN);
+        w0 = GATEUP ? t0.group * 2 * N + t0.ctile * kBM : t0.group * N + t0.ctile * kBM;
+        npre = kblocks < C::kStages ? kblocks : C::kStages;
+        for (int kb = 0; kb < npre; ++kb) {   // fresh ring: stage kb, phase 0
+          mbar_arrive_expect_tx(full_bar(kb), C::kStage);
+          tma_load_2d(stage_a(kb, 0), &tm_w, kb * kBK, w0, full_bar(kb), pol_w);
+          if (GATEUP)
+            tma_load_2d(stage_a(kb, 1), &tm_w, kb * kBK, w0 + N, full_bar(kb), pol_w);
+        }
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      for (int kb = 0; kb < npre; ++kb) {
+        tma_load_2d(stage_b(kb), &tm_a, kb * kBK, t0.row0, full_bar(kb), pol_a);
+#pragma unroll
+        for (int i = 0; i < C::kStages; ++i)
+          if (i == kb) last_phase[i] = 0;
+      }
+      s = npre % C::kStages;
+      ph = npre == C::kStages ? 1u : 0u;
+      for (int tile = first; ok && tile < total_tiles; tile += gridDim.x) {
+        const TileInfo ti = tile == first ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
         const int wrow0 = GATEUP ? ti.group * 2 * N + ti.ctile * kBM
                                  : ti.group * N + ti.ctile * kBM;
         const int wrow1 = wrow0 + N;   // up projection rows (gate/up only)
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = tile == first ? npre : 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                  kErrTimeoutProducer)) {
             ok = false;
@@ -244,9 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
                             kErrTimeoutDrain);
         }
       }
+    } else {
+      pdl_wait();
+      pdl_launch_dependents();
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    pdl_wait();
+    pdl_launch_dependents();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
       int s = 0;
@@ -295,6 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     }
   } else {
     // ---------------- epilogue ----------------
+    pdl_wait();
+    pdl_launch_dependents();
     const int q = warp & 3;               // TMEM lane quarter of this warp
     const int m = q * 32 + lane;          // channel within the tile
     int it = 0;
@@ -392,16 +427,21 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
 }
 
 int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
 }
 
 template <int BN, bool GATEUP>
 int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
         const float* w_scale, const int32_t* offsets, int groups, int N, int K,
-        float* out, cudaStream_t stream) {
+        float* out, cudaStream_t stream, bool pdl) {
   using C = Cfg<BN, GATEUP>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
@@ -414,10 +454,10 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / kBM);
   const int grid = (int)std::min<int64_t>(upper, sm_count());
   if (grid <= 0) return 0;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(
-      tm_w, tm_a, a_scale, w_scale, offsets, groups, N, K, out,
-      device_error_word());
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+  const cudaError_t e = launch_kernel(
+      pdl, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, kern, tm_w, tm_a,
+      a_scale, w_scale, offsets, groups, N, K, out, device_error_word());
+  return e == cudaSuccess ? 0 : -3;
 }
 
 }  // namespace
@@ -425,20 +465,21 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
 int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         int64_t a_rows, const uint8_t* W, const float* w_scale,
                         const int32_t* offsets, int groups, int N, int K,
-                        float* out, int rows_hint, cudaStream_t stream) {
+                        float* out, int rows_hint, cudaStream_t stream,
+                        bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
   if (kind == 0) {
-    if (avg <= 16) return run<16, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-    if (avg <= 32) return run<32, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-    if (avg <= 64) return run<64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-    return run<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
+    if (avg <= 16) return run<16, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 32) return run<32, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 64) return run<64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    return run<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   }
-  if (avg <= 16) return run<16, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-  if (avg <= 32) return run<32, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-  if (avg <= 64) return run<64, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-  if (avg <= 128) return run<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
-  return run<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream);
+  if (avg <= 16) return run<16, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 32) return run<32, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 64) return run<64, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 128) return run<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  return run<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
 }
 
 }  // namespace moe

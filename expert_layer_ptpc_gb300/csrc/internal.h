@@ -8,6 +8,26 @@
 
 namespace moe {
 
+// Launch `kernel`; with `pdl` the launch may overlap the tail of the previous
+// kernel in the stream (programmatic dependent launch), and the kernel
+// orders itself with pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, void (*kernel)(KArgs...),
+                          Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxGroups = kMaxExperts + 1;
@@ -17,11 +37,11 @@ unsigned* device_error_word();
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_r, int T,
                                  int E, int D, float* logits,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, bool pdl);
 
 cudaError_t launch_route(const float* logits, int T, int E, int k,
                          int renormalize, int32_t* ids, float* w,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool pdl);
 
 // Scratch bytes of the permutation for R = T * k flat entries.
 size_t permute_ws_bytes(int64_t R, int E);
@@ -32,7 +52,7 @@ size_t permute_ws_bytes(int64_t R, int E);
 cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
                            int32_t* counts, int32_t* offsets, int32_t* s2f,
                            int32_t* f2s, int extra_group_rows, void* ws,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool pdl);
 
 // Per-row e4m3 quantisation with scatter; `gate_w` non-null also computes
 // gate_out[r] = sigmoid(in[r] . gate_w) (bf16 input only).
@@ -40,7 +60,10 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          const int32_t* dst_rows, int copies,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
-                         float* gate_out, cudaStream_t stream);
+                         float* gate_out, cudaStream_t stream, bool pdl);
+
+// Largest row length launch_quant handles.
+constexpr int kMaxQuantCols = 32768;
 
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
                                int D, float* gate, cudaStream_t stream);
@@ -49,11 +72,12 @@ cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
 int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         int64_t a_rows, const uint8_t* W, const float* w_scale,
                         const int32_t* offsets, int groups, int N, int K,
-                        float* out, int rows_hint, cudaStream_t stream);
+                        float* out, int rows_hint, cudaStream_t stream,
+                        bool pdl);
 
 cudaError_t launch_combine(const float* y, const int32_t* f2s,
                            const float* topk_w, int T, int k, int D,
                            const float* y_shared, const float* shared_gate,
-                           uint16_t* out, cudaStream_t stream);
+                           uint16_t* out, cudaStream_t stream, bool pdl);
 
 }  // namespace moe

@@ -61,17 +61,31 @@ __device__ int block_exclusive_scan(int* vals, int n, int* warp_tot) {
   return total;
 }
 
-// Per-warp expert histograms of one chunk: whist[w * E + e].
-__device__ void chunk_warp_histograms(const int32_t* __restrict__ ids,
-                                      int64_t f0, int64_t R, int E, int* whist) {
-  for (int i = threadIdx.x; i < kWarps * E; i += kThreads) whist[i] = 0;
-  __syncthreads();
+constexpr int kPerLane = kSub / 32;         // entries a lane holds
+
+// Load this warp's sub-chunk: lane holds entries begin + 32 i + lane
+// (i < kPerLane); -1 past the end.
+__device__ __forceinline__ void load_warp_ids(const int32_t* __restrict__ ids,
+                                              int64_t f0, int64_t R,
+                                              int (&e)[kPerLane]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t begin = f0 + (int64_t)warp * kSub;
-  for (int i = lane; i < kSub; i += 32) {
-    const int64_t f = begin + i;
-    if (f < R) atomicAdd(&whist[warp * E + ids[f]], 1);
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int64_t f = begin + 32 * i + lane;
+    e[i] = f < R ? ids[f] : -1;
   }
+}
+
+// Per-warp expert histograms of one chunk: whist[w * E + e].
+__device__ void chunk_warp_histograms(const int (&e)[kPerLane], int E,
+                                      int* whist) {
+  for (int i = threadIdx.x; i < kWarps * E; i += kThreads) whist[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i)
+    if (e[i] >= 0) atomicAdd(&whist[warp * E + e[i]], 1);
   __syncthreads();
 }
 
@@ -89,26 +103,28 @@ __device__ void warp_bases(const int* base, int E, int* whist) {
   __syncthreads();
 }
 
-// Stable scatter of one chunk given per-warp starting rows.
-__device__ void chunk_scatter(const int32_t* __restrict__ ids, int64_t f0,
-                              int64_t R, int E, int* whist,
-                              int32_t* __restrict__ s2f,
+// Stable scatter of one chunk given per-warp starting rows. 32 consecutive
+// entries at a time: lanes with the same expert are ranked by lane order.
+__device__ void chunk_scatter(const int (&e)[kPerLane], int64_t f0, int64_t R,
+                              int E, int* whist, int32_t* __restrict__ s2f,
                               int32_t* __restrict__ f2s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* base = whist + warp * E;
   const int64_t begin = f0 + (int64_t)warp * kSub;
-  for (int i = 0; i < kSub; i += 32) {
-    const int64_t f = begin + i + lane;
-    const bool valid = f < R;
-    const int e = valid ? ids[f] : -1 - lane;   // distinct sentinels
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    if (begin + 32 * i >= R) break;               // warp-uniform
+    const int64_t f = begin + 32 * i + lane;
+    const bool valid = e[i] >= 0;
+    const int key = valid ? e[i] : -1 - lane;     // distinct sentinels
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
     int pos = 0;
-    if (valid) pos = base[e] + __popc(peers & lanemask_lt());
+    if (valid) pos = base[key] + __popc(peers & lanemask_lt());
     __syncwarp();
     if (valid) {
       s2f[pos] = (int32_t)f;
       f2s[f] = pos;
-      if (lane == __ffs(peers) - 1) base[e] += __popc(peers);
+      if (lane == __ffs(peers) - 1) base[key] += __popc(peers);
     }
     __syncwarp();
   }
@@ -131,7 +147,11 @@ __global__ void __launch_bounds__(kThreads) permute_small_kernel(
   int* whist = smem;                       // kWarps * E
   int* scan = whist + kWarps * E;          // E + 1
   int* warp_tot = scan + E + 1;            // kWarps + 1
-  chunk_warp_histograms(ids, 0, R, E, whist);
+  pdl_wait();
+  pdl_launch_dependents();
+  int mine[kPerLane];
+  load_warp_ids(ids, 0, R, mine);
+  chunk_warp_histograms(mine, E, whist);
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int c = 0;
     for (int w = 0; w < kWarps; ++w) c += whist[w * E + e];
@@ -144,13 +164,15 @@ __global__ void __launch_bounds__(kThreads) permute_small_kernel(
   if (threadIdx.x == 0) offsets[E] = total;
   write_extra_group(E, total, extra, counts, offsets);
   warp_bases(scan, E, whist);
-  chunk_scatter(ids, 0, R, E, whist, s2f, f2s);
+  chunk_scatter(mine, 0, R, E, whist, s2f, f2s);
 }
 
 // R > kChunk, pass 1: per-chunk expert counts -> hist[c * E + e].
 __global__ void __launch_bounds__(kThreads) permute_hist_kernel(
     const int32_t* __restrict__ ids, int64_t R, int E, int* __restrict__ hist) {
   extern __shared__ int smem[];
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t f0 = (int64_t)blockIdx.x * kChunk;
   for (int i = threadIdx.x; i < E; i += kThreads) smem[i] = 0;
   __syncthreads();
@@ -171,6 +193,8 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
   extern __shared__ int smem[];
   int* scan = smem;              // E + 1
   int* warp_tot = scan + E + 1;  // kWarps + 1
+  pdl_wait();
+  pdl_launch_dependents();
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int c = 0;
     for (int ch = 0; ch < nchunks; ++ch) c += hist[(int64_t)ch * E + e];
@@ -200,12 +224,16 @@ __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
   extern __shared__ int smem[];
   int* whist = smem;                  // kWarps * E
   int* base = whist + kWarps * E;     // E
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t f0 = (int64_t)blockIdx.x * kChunk;
   for (int e = threadIdx.x; e < E; e += kThreads)
     base[e] = hist[(int64_t)blockIdx.x * E + e];
-  chunk_warp_histograms(ids, f0, R, E, whist);
+  int mine[kPerLane];
+  load_warp_ids(ids, f0, R, mine);
+  chunk_warp_histograms(mine, E, whist);
   warp_bases(base, E, whist);
-  chunk_scatter(ids, f0, R, E, whist, s2f, f2s);
+  chunk_scatter(mine, f0, R, E, whist, s2f, f2s);
 }
 
 }  // namespace
@@ -219,32 +247,36 @@ size_t permute_ws_bytes(int64_t R, int E) {
 cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
                            int32_t* counts, int32_t* offsets, int32_t* s2f,
                            int32_t* f2s, int extra_group_rows, void* ws,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool pdl) {
   if (R <= kChunk) {
     const size_t smem = (size_t)(kWarps * E + E + 1 + kWarps + 1) * sizeof(int);
     cudaError_t err = cudaFuncSetAttribute(
         permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
         (int)smem);
     if (err != cudaSuccess) return err;
-    permute_small_kernel<<<1, kThreads, smem, stream>>>(
-        ids, (int)R, E, counts, offsets, s2f, f2s, extra_group_rows);
-    return cudaGetLastError();
+    return launch_kernel(pdl, dim3(1), dim3(kThreads), smem, stream,
+                         permute_small_kernel, ids, (int)R, E, counts, offsets,
+                         s2f, f2s, extra_group_rows);
   }
   const int nchunks = (int)((R + kChunk - 1) / kChunk);
   int* hist = static_cast<int*>(ws);
-  permute_hist_kernel<<<nchunks, kThreads, E * sizeof(int), stream>>>(ids, R, E,
-                                                                      hist);
-  const size_t smem_scan = (size_t)(E + 1 + kWarps + 1) * sizeof(int);
-  permute_scan_kernel<<<1, kThreads, smem_scan, stream>>>(
-      nchunks, E, hist, counts, offsets, extra_group_rows);
-  const size_t smem_sc = (size_t)(kWarps * E + E) * sizeof(int);
-  cudaError_t err = cudaFuncSetAttribute(
-      permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)smem_sc);
+  cudaError_t err = launch_kernel(pdl, dim3(nchunks), dim3(kThreads),
+                                  E * sizeof(int), stream, permute_hist_kernel,
+                                  ids, R, E, hist);
   if (err != cudaSuccess) return err;
-  permute_scatter_kernel<<<nchunks, kThreads, smem_sc, stream>>>(ids, R, E, hist,
-                                                                 s2f, f2s);
-  return cudaGetLastError();
+  const size_t smem_scan = (size_t)(E + 1 + kWarps + 1) * sizeof(int);
+  err = launch_kernel(pdl, dim3(1), dim3(kThreads), smem_scan, stream,
+                      permute_scan_kernel, nchunks, E, hist, counts, offsets,
+                      extra_group_rows);
+  if (err != cudaSuccess) return err;
+  const size_t smem_sc = (size_t)(kWarps * E + E) * sizeof(int);
+  err = cudaFuncSetAttribute(permute_scatter_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_sc);
+  if (err != cudaSuccess) return err;
+  return launch_kernel(pdl, dim3(nchunks), dim3(kThreads), smem_sc, stream,
+                       permute_scatter_kernel, ids, R, E, (const int*)hist, s2f,
+                       f2s);
 }
 
 }  // namespace moe

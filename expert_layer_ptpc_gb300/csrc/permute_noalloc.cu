@@ -87,6 +87,6 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_ids, int T, int E, int k,
   if (scratch == nullptr) return MOE_ERR_CUDA;
   err = launch_permute(topk_ids, R, E, expert_counts, expert_offsets,
                        sorted_to_flat, flat_to_sorted, -1, scratch,
-                       static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream), false);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

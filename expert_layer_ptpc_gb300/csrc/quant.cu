@@ -11,6 +11,8 @@
 //
 // Both divisions are IEEE round-to-nearest (__fdiv_rn), so codes and scales
 // are the exactly rounded values of that definition.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,87 +20,114 @@ namespace moe {
 
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
-constexpr int kUnit = 8;   // elements per lane per step
+constexpr int kVec = 16;        // elements per thread per unit (16 bytes of codes)
+constexpr int kMaxThreads = 512;
+constexpr int kWarpsPerBlock = 8;   // shared-gate kernel
 
-__device__ __forceinline__ void load_unit(const __nv_bfloat16* p, float (&v)[kUnit]) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&v)[kVec]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __low2float(h[i]);
-    v[2 * i + 1] = __high2float(h[i]);
+  for (int h = 0; h < 2; ++h) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(p + 8 * h);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * h + 2 * i] = __low2float(b[i]);
+      v[8 * h + 2 * i + 1] = __high2float(b[i]);
+    }
   }
 }
 
-__device__ __forceinline__ void load_unit(const float* p, float (&v)[kUnit]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[kVec]) {
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const float4 a = *reinterpret_cast<const float4*>(p + 4 * h);
+    v[4 * h] = a.x; v[4 * h + 1] = a.y; v[4 * h + 2] = a.z; v[4 * h + 3] = a.w;
+  }
 }
 
-template <typename InT>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_kernel(
+// One block per row; each thread holds UNITS vectors of kVec elements, so the
+// row is read from memory once. The row maximum (and the gate's dot product)
+// is reduced over the block, the scale is formed once, and every thread
+// writes its 16-byte code vectors to each destination row.
+template <typename InT, int UNITS>
+__global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
     const InT* __restrict__ in, int64_t rows, int cols,
     const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
     uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
     const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out) {
-  const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;
-  if (r >= rows) return;
-  const int lane = (int)lane_id();
+  __shared__ float red_max[kMaxThreads / 32];
+  __shared__ float red_dot[kMaxThreads / 32];
+  __shared__ int64_t dst[kMaxTopK + 1];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int nunits = cols / kVec;
   const InT* row = in + r * cols;
 
-  // pass 1: row amax (and the shared-expert gate's dot product)
+  float v[UNITS][kVec];
   float amax = 0.f, dot = 0.f;
-  for (int c = lane * kUnit; c < cols; c += 32 * kUnit) {
-    float v[kUnit];
-    load_unit(row + c, v);
 #pragma unroll
-    for (int i = 0; i < kUnit; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    if (gate_w != nullptr) {
-      float w[kUnit];
-      load_unit(gate_w + c, w);
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = tid + i * blockDim.x;
+    if (u < nunits) {
+      load_vec(row + u * kVec, v[i]);
 #pragma unroll
-      for (int i = 0; i < kUnit; ++i) dot = fmaf(v[i], w[i], dot);
+      for (int j = 0; j < kVec; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+      if (gate_w != nullptr) {
+        float g[kVec];
+        load_vec(gate_w + u * kVec, g);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) dot = fmaf(v[i][j], g[j], dot);
+      }
     }
   }
   amax = warp_max(amax);
-  const float s = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
-
-  // destinations of this row
-  const int ndst = (dst_rows != nullptr ? copies : 1) + (extra_row_base >= 0 ? 1 : 0);
+  dot = warp_sum(dot);
   if (lane == 0) {
-    for (int d = 0; d < ndst; ++d) {
-      const int64_t o = d < (dst_rows != nullptr ? copies : 1)
-                            ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + d] : r)
-                            : extra_row_base + r;
-      out_scale[o] = s;
+    red_max[warp] = amax;
+    red_dot[warp] = dot;
+  }
+  // destination rows of this row
+  const int nmain = dst_rows != nullptr ? copies : 1;
+  const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
+  if (tid < ndst) {
+    dst[tid] = tid < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + tid] : r)
+                           : extra_row_base + r;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float a = lane < nwarps ? red_max[lane] : 0.f;
+    float d = lane < nwarps ? red_dot[lane] : 0.f;
+    a = warp_max(a);
+    d = warp_sum(d);
+    if (lane == 0) {
+      red_max[0] = a;
+      red_dot[0] = d;
     }
-    if (gate_w != nullptr) gate_out[r] = 0.f;  // placeholder, set below
   }
-  if (gate_w != nullptr) {
-    dot = warp_sum(dot);
-    if (lane == 0) gate_out[r] = 1.0f / (1.0f + expf(-dot));
-  }
+  __syncthreads();
+  const float s = __fdiv_rn(fmaxf(red_max[0], 1e-12f), 448.0f);
+  if (tid < ndst) out_scale[dst[tid]] = s;
+  if (gate_w != nullptr && tid == 0) gate_out[r] = 1.0f / (1.0f + expf(-red_dot[0]));
 
-  // pass 2: quantise and store to every destination
-  for (int c = lane * kUnit; c < cols; c += 32 * kUnit) {
-    float v[kUnit];
-    load_unit(row + c, v);
-    uint32_t packed[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i], s), __fdiv_rn(v[4 * i + 1], s));
-      const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i + 2], s), __fdiv_rn(v[4 * i + 3], s));
-      packed[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-    }
-    const uint2 q = make_uint2(packed[0], packed[1]);
-    for (int d = 0; d < ndst; ++d) {
-      const int64_t o = d < (dst_rows != nullptr ? copies : 1)
-                            ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + d] : r)
-                            : extra_row_base + r;
-      *reinterpret_cast<uint2*>(out_q + o * cols + c) = q;
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = tid + i * blockDim.x;
+    if (u < nunits) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[i][4 * q], s),
+                                            __fdiv_rn(v[i][4 * q + 1], s));
+        const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[i][4 * q + 2], s),
+                                            __fdiv_rn(v[i][4 * q + 3], s));
+        w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int d = 0; d < ndst; ++d)
+        *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
     }
   }
 }
@@ -106,18 +135,40 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_kernel(
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) shared_gate_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
     int T, int D, float* __restrict__ gate) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;
   if (t >= T) return;
   float dot = 0.f;
-  for (int c = (int)lane_id() * kUnit; c < D; c += 32 * kUnit) {
-    float v[kUnit], g[kUnit];
-    load_unit(x + (int64_t)t * D + c, v);
-    load_unit(w + c, g);
+  for (int c = (int)lane_id() * kVec; c < D; c += 32 * kVec) {
+    float v[kVec], g[kVec];
+    load_vec(x + (int64_t)t * D + c, v);
+    load_vec(w + c, g);
 #pragma unroll
-    for (int i = 0; i < kUnit; ++i) dot = fmaf(v[i], g[i], dot);
+    for (int i = 0; i < kVec; ++i) dot = fmaf(v[i], g[i], dot);
   }
   dot = warp_sum(dot);
   if (lane_id() == 0) gate[t] = 1.0f / (1.0f + expf(-dot));
+}
+
+template <typename InT>
+cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
+                        const int32_t* dst_rows, int copies,
+                        int64_t extra_row_base, uint8_t* out_q,
+                        float* out_scale, const __nv_bfloat16* gate_w,
+                        float* gate_out, cudaStream_t stream, bool pdl) {
+  const int nunits = cols / kVec;
+  int threads = std::min(kMaxThreads, ((nunits + 31) / 32) * 32);
+  const int units = (nunits + threads - 1) / threads;
+  const dim3 grid((unsigned)rows), block(threads);
+  auto go = [&](auto kern) {
+    return launch_kernel(pdl, grid, block, 0, stream, kern, in, rows, cols,
+                         dst_rows, copies, extra_row_base, out_q, out_scale,
+                         gate_w, gate_out);
+  };
+  if (units <= 1) return go(quant_rows_kernel<InT, 1>);
+  if (units <= 2) return go(quant_rows_kernel<InT, 2>);
+  return go(quant_rows_kernel<InT, 4>);
 }
 
 }  // namespace
@@ -126,30 +177,26 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          const int32_t* dst_rows, int copies,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
-                         float* gate_out, cudaStream_t stream) {
+                         float* gate_out, cudaStream_t stream, bool pdl) {
   if (rows == 0) return cudaSuccess;
-  const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  const auto* gw = reinterpret_cast<const __nv_bfloat16*>(gate_w);
-  if (in_dtype == 0) {
-    quant_rows_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(in), rows, cols, dst_rows, copies,
-        extra_row_base, out_q, out_scale, gw, gate_out);
-  } else {
-    quant_rows_kernel<float><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(
-        static_cast<const float*>(in), rows, cols, dst_rows, copies,
-        extra_row_base, out_q, out_scale, nullptr, nullptr);
-  }
-  return cudaGetLastError();
+  if (in_dtype == 0)
+    return launch_rows(static_cast<const __nv_bfloat16*>(in), rows, cols,
+                       dst_rows, copies, extra_row_base, out_q, out_scale,
+                       reinterpret_cast<const __nv_bfloat16*>(gate_w), gate_out,
+                       stream, pdl);
+  return launch_rows(static_cast<const float*>(in), rows, cols, dst_rows, copies,
+                     extra_row_base, out_q, out_scale,
+                     (const __nv_bfloat16*)nullptr, (float*)nullptr, stream, pdl);
 }
 
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
                                int D, float* gate, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  shared_gate_kernel<<<blocks, kWarpsPerBlock * 32, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x),
-      reinterpret_cast<const __nv_bfloat16*>(w_g), T, D, gate);
-  return cudaGetLastError();
+  return launch_kernel(false, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream,
+                       shared_gate_kernel,
+                       reinterpret_cast<const __nv_bfloat16*>(x),
+                       reinterpret_cast<const __nv_bfloat16*>(w_g), T, D, gate);
 }
 
 }  // namespace moe

@@ -17,6 +17,8 @@ namespace moe {
 __global__ void router_logits_kernel(const __nv_bfloat16* __restrict__ x,
                                      const __nv_bfloat16* __restrict__ w, int T,
                                      int E, int D, float* __restrict__ logits) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t pair = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (pair >= (int64_t)T * E) return;
   const int t = (int)(pair / E), e = (int)(pair % E);
@@ -35,15 +37,16 @@ __global__ void router_logits_kernel(const __nv_bfloat16* __restrict__ x,
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_r, int T,
                                  int E, int D, float* logits,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool pdl) {
   const int64_t pairs = (int64_t)T * E;
   if (pairs == 0) return cudaSuccess;
   const int warps = 8;
   const int64_t blocks = (pairs + warps - 1) / warps;
-  router_logits_kernel<<<(unsigned)blocks, warps * 32, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x),
-      reinterpret_cast<const __nv_bfloat16*>(w_r), T, E, D, logits);
-  return cudaGetLastError();
+  return launch_kernel(pdl, dim3((unsigned)blocks), dim3(warps * 32), 0, stream,
+                       router_logits_kernel,
+                       reinterpret_cast<const __nv_bfloat16*>(x),
+                       reinterpret_cast<const __nv_bfloat16*>(w_r), T, E, D,
+                       logits);
 }
 
 // ---------------------------------------------------------------------------
@@ -57,6 +60,8 @@ template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ ids, float* __restrict__ weights) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
   const int lane = (int)lane_id();
@@ -123,22 +128,21 @@ __global__ void __launch_bounds__(256) route_kernel(
 
 cudaError_t launch_route(const float* logits, int T, int E, int k,
                          int renormalize, int32_t* ids, float* w,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int warps = 8;
-  const unsigned blocks = (unsigned)((T + warps - 1) / warps);
+  const dim3 grid((unsigned)((T + warps - 1) / warps)), block(warps * 32);
   const int npl = (E + 31) / 32;
-#define MOE_ROUTE(N)                                                        \
-  route_kernel<N><<<blocks, warps * 32, 0, stream>>>(logits, T, E, k,       \
-                                                     renormalize, ids, w)
-  if (npl <= 1) MOE_ROUTE(1);
-  else if (npl <= 2) MOE_ROUTE(2);
-  else if (npl <= 4) MOE_ROUTE(4);
-  else if (npl <= 8) MOE_ROUTE(8);
-  else if (npl <= 16) MOE_ROUTE(16);
-  else MOE_ROUTE(32);
-#undef MOE_ROUTE
-  return cudaGetLastError();
+  auto go = [&](auto kern) {
+    return launch_kernel(pdl, grid, block, 0, stream, kern, logits, T, E, k,
+                         renormalize, ids, w);
+  };
+  if (npl <= 1) return go(route_kernel<1>);
+  if (npl <= 2) return go(route_kernel<2>);
+  if (npl <= 4) return go(route_kernel<4>);
+  if (npl <= 8) return go(route_kernel<8>);
+  if (npl <= 16) return go(route_kernel<16>);
+  return go(route_kernel<32>);
 }
 
 }  // namespace moe

@@ -164,7 +164,8 @@ MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int T, int E, int k,
  *   extra_row_base >= 0 it is also written to row extra_row_base + r.
  *   out_q [*, cols] uint8 and out_scale [*] fp32 are indexed by output row.
  * Errors: MOE_ERR_INVALID_ARG (null, cols not a positive multiple of 16,
- *         bad dtype, copies < 1).
+ *         bad dtype, copies < 1), MOE_ERR_UNSUPPORTED (cols > 32768 or
+ *         copies > 32).
  */
 MOE_API int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
                            const int32_t* dst_rows, int copies,
@@ -174,7 +175,7 @@ MOE_API int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
 /*
  * moe_shared_gate - shared-expert gate sigmoid(x[t] . w_g), fp32 (the TPU
  * page's shared expert runs on every token; its gate is a sigmoid).
- *   x [T, D] bf16;  w_g [D] bf16;  gate [T] fp32 (written).
+ *   x [T, D] bf16 (D a multiple of 16);  w_g [D] bf16;  gate [T] fp32.
  */
 MOE_API int moe_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
                             int D, float* gate, moe_stream_t stream);
