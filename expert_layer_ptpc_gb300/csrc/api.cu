@@ -166,7 +166,7 @@ int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_quant(in, in_dtype, rows, cols, dst_rows, copies,
                                   extra_row_base, out_q, out_scale, nullptr,
-                                  nullptr, stream, false));
+                                  nullptr, stream, false, false));
 }
 
 int moe_shared_gate(const uint16_t* x, const uint16_t* w_g, int T, int D,
@@ -292,7 +292,8 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
   st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
                                 d.shared ? R : -1, xq, sx,
                                 d.shared ? shared_gate_w : nullptr,
-                                d.shared ? gate : nullptr, stream, pdl));
+                                d.shared ? gate : nullptr, stream, pdl,
+                                false));
   if (st != MOE_OK) return st;
   mark(4);
   const int hint = (int)std::max<int64_t>(1, R / d.E);
@@ -301,7 +302,8 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
   if (st != MOE_OK) return st;
   mark(5);
   st = cuda_status(launch_quant(h, MOE_DTYPE_F32, rows, d.I, nullptr, 1, -1, hq,
-                                sh, nullptr, nullptr, stream, pdl));
+                                sh, nullptr, nullptr, stream, pdl,
+                                /*release_early=*/true));
   if (st != MOE_OK) return st;
   mark(6);
   st = launch_grouped_gemm(MOE_GEMM_DOWN, hq, sh, rows, w_d, s_d, offsets, G,

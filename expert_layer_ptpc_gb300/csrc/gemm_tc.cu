@@ -51,18 +51,26 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int BN, bool GATEUP>
+template <int BN, int BMW, bool GATEUP>
 struct Cfg {
-  static constexpr int kNumA = GATEUP ? 2 : 1;
-  static constexpr int kATile = kBM * kBK;
+  // BMW = output channels per tile. 128: the MMA's 128 rows are 128 channels
+  // (gate/up: a second MMA for the up rows). 64: for small token tiles, a
+  // tile is 64 channels so twice as many tiles spread over the SMs; gate/up
+  // packs 64 gate and the matching 64 up rows into one 128-row operand.
+  static constexpr bool kPacked = BMW == 64;
+  static constexpr int kNumA = (GATEUP && !kPacked) ? 2 : 1;  // MMAs per K step
+  static constexpr int kATile = kBM * kBK;                     // one 128-row operand
   static constexpr int kBTile = BN * kBK;
   static constexpr int kStage = kNumA * kATile + kBTile;
+  static constexpr int kTxBytes = (GATEUP ? 2 : 1) * BMW * kBK + kBTile;
   static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
-  static constexpr int kAccCols = kNumA * BN;               // one buffer
+  static constexpr int kAccCols = kNumA * BN;                  // one buffer
   static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
-  static constexpr int kNumBars = 2 * kStages + 5;
-  static constexpr int kSmemBytes =
-      1024 + kStages * kStage + kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kXBytes = (GATEUP && kPacked) ? 64 * 16 * 4 : 0;
+  static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes +
+                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+  static_assert(BMW == 64 || BMW == 128, "tile width");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kStages >= 2, "pipeline depth");
 };
@@ -74,12 +82,13 @@ struct TileInfo {
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* prefix,
                                                 int groups, const int32_t* offsets,
                                                 int bn) {
-  int lo = 0, hi = groups - 1;   // largest g with prefix[g] <= tile
+  // the largest g with prefix[g] <= tile; empty groups share their
+  // successor's prefix value, so this is the non-empty group owning the tile
+  int lo = 0, hi = groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (prefix[mid] <= tile) lo = mid; else hi = mid - 1;
   }
-  // skip empty groups that share the same prefix value
   const int g = lo;
   const int start = offsets[g], end = offsets[g + 1];
   const int tt = (end - start + bn - 1) / bn;
@@ -116,25 +125,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int BN, bool GATEUP>
+template <int BN, int BMW, bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a, const float* __restrict__ a_scale,
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
     unsigned* __restrict__ err) {
-  using C = Cfg<BN, GATEUP>;
+  using C = Cfg<BN, BMW, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
+                                               C::kXBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
   __shared__ int warp_tot[kThreads / 32 + 1];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_ctiles = N / kBM;
+  const int n_ctiles = N / BMW;
   const int kblocks = K / kBK;
 
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
@@ -142,6 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   auto accf_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
   auto acce_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * C::kStages + 4);
+  const uint32_t xfull_bar = smem_u32(bars + 2 * C::kStages + 5);
+  const uint32_t xempty_bar = smem_u32(bars + 2 * C::kStages + 6);
   auto stage_a = [&](int s, int which) {
     return smem_u32(smem + s * C::kStage + which * C::kATile);
   };
@@ -160,6 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       mbar_init(acce_bar(b), 128);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(xfull_bar, 64);
+    mbar_init(xempty_bar, 64);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -199,6 +214,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   const uint32_t tmem_base = *tmem_holder;
   const int total_tiles = prefix[groups];
 
+  // first weight row of a tile (gate rows for gate/up)
+  auto weight_row = [&](const TileInfo& ti) {
+    return GATEUP ? ti.group * 2 * N + ti.ctile * BMW : ti.group * N + ti.ctile * BMW;
+  };
+  // the weight loads of one stage
+  auto load_weights = [&](int s, int kb, int wrow, uint64_t pol) {
+    if (GATEUP) {
+      if (C::kPacked) {   // 64 gate rows, then the matching 64 up rows
+        tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow, full_bar(s), pol);
+        tma_load_2d(stage_a(s, 0) + 64 * kBK, &tm_w, kb * kBK, wrow + N,
+                    full_bar(s), pol);
+      } else {
+        tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow, full_bar(s), pol);
+        tma_load_2d(stage_a(s, 1), &tm_w, kb * kBK, wrow + N, full_bar(s), pol);
+      }
+    } else {
+      tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow, full_bar(s), pol);
+    }
+  };
+
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -216,16 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       const int first = blockIdx.x;
       int npre = 0;
       TileInfo t0{};
-      int w0 = 0;
       if (first < total_tiles) {
         t0 = decode_tile(first, prefix, groups, offsets, BN);
-        w0 = GATEUP ? t0.group * 2 * N + t0.ctile * kBM : t0.group * N + t0.ctile * kBM;
         npre = kblocks < C::kStages ? kblocks : C::kStages;
         for (int kb = 0; kb < npre; ++kb) {   // fresh ring: stage kb, phase 0
-          mbar_arrive_expect_tx(full_bar(kb), C::kStage);
-          tma_load_2d(stage_a(kb, 0), &tm_w, kb * kBK, w0, full_bar(kb), pol_w);
-          if (GATEUP)
-            tma_load_2d(stage_a(kb, 1), &tm_w, kb * kBK, w0 + N, full_bar(kb), pol_w);
+          mbar_arrive_expect_tx(full_bar(kb), C::kTxBytes);
+          load_weights(kb, kb, weight_row(t0), pol_w);
         }
       }
       pdl_wait();
@@ -239,20 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       s = npre % C::kStages;
       ph = npre == C::kStages ? 1u : 0u;
       for (int tile = first; ok && tile < total_tiles; tile += gridDim.x) {
-        const TileInfo ti = tile == first ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
-        const int wrow0 = GATEUP ? ti.group * 2 * N + ti.ctile * kBM
-                                 : ti.group * N + ti.ctile * kBM;
-        const int wrow1 = wrow0 + N;   // up projection rows (gate/up only)
+        const TileInfo ti =
+            tile == first ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
+        const int wrow = weight_row(ti);
         for (int kb = tile == first ? npre : 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                  kErrTimeoutProducer)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), C::kStage);
-          tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow0, full_bar(s), pol_w);
-          if (GATEUP)
-            tma_load_2d(stage_a(s, 1), &tm_w, kb * kBK, wrow1, full_bar(s), pol_w);
+          mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
+          load_weights(s, kb, wrow, pol_w);
           tma_load_2d(stage_b(s), &tm_a, kb * kBK, ti.row0, full_bar(s), pol_a);
 #pragma unroll
           for (int i = 0; i < C::kStages; ++i)
@@ -308,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             const uint32_t acc = (kb | kk) != 0;
             const uint64_t bdesc = smem_desc_k_sw128(b + kk * 32);
             mma_f8f6f4(d0, smem_desc_k_sw128(a0 + kk * 32), bdesc, idesc, acc);
-            if (GATEUP) {
+            if (C::kNumA == 2) {
               const uint32_t a1 = stage_a(s, 1);
               mma_f8f6f4(d1, smem_desc_k_sw128(a1 + kk * 32), bdesc, idesc, acc);
             }
@@ -331,20 +359,64 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     pdl_wait();
     pdl_launch_dependents();
     const int q = warp & 3;               // TMEM lane quarter of this warp
-    const int m = q * 32 + lane;          // channel within the tile
+    const int m = q * 32 + lane;          // accumulator row (lane) of this thread
     int it = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+    uint32_t xc = 0;                      // gate/up exchanges so far (packed)
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++it) {
       const int ab = it & 1;
       const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
       if (!warp_wait(accf_bar(ab), acc_ph, abort_flag, err, kErrTimeoutEpilogue))
         break;
       tc_fence_after_sync();
       const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
-      const int ch = ti.ctile * kBM + m;
       const int nvalid = min(BN, ti.row_end - ti.row0);
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
-      if (GATEUP) {
+      if (GATEUP && C::kPacked) {
+        // lanes 0-63: gate of channels ctile*64 + m; lanes 64-127: up of the
+        // same channels. Up values pass to the gate threads through xbuf.
+        const bool is_gate = q < 2;
+        const int ch = ti.ctile * 64 + (is_gate ? m : m - 64);
+        const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
+        const float swu = w_scale[(int64_t)ti.group * 2 * N + N + ch];
+        for (int n0 = 0; ok && n0 < nvalid; n0 += 16, ++xc) {
+          float a[16];
+          tmem_ld_x16(taddr + n0, a);
+          tmem_ld_wait();
+          if (!is_gate) {
+            if (!warp_wait(xempty_bar, (xc & 1u) ^ 1u, abort_flag, err,
+                           kErrTimeoutEpilogue)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xbuf[j * 64 + (m - 64)] = a[j];
+            mbar_arrive(xfull_bar);
+          } else {
+            if (!warp_wait(xfull_bar, xc & 1u, abort_flag, err,
+                           kErrTimeoutEpilogue)) {
+              ok = false;
+              break;
+            }
+            float u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = xbuf[j * 64 + m];
+            mbar_arrive(xempty_bar);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (n0 + j < nvalid) {
+                const int row = ti.row0 + n0 + j;
+                const float sx = a_scale[row];
+                const float g = a[j] * sx * swg;
+                const float uu = u[j] * sx * swu;
+                out[(int64_t)row * N + ch] = g / (1.0f + expf(-g)) * uu;
+              }
+            }
+          }
+        }
+      } else if (GATEUP) {
+        const int ch = ti.ctile * kBM + m;
         const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
         const float swu = w_scale[(int64_t)ti.group * 2 * N + N + ch];
         for (int n0 = 0; n0 < nvalid; n0 += 16) {
@@ -359,12 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
               const float sx = a_scale[row];
               const float g = ag[j] * sx * swg;
               const float u = au[j] * sx * swu;
-              const float h = g / (1.0f + expf(-g)) * u;
-              out[(int64_t)row * N + ch] = h;
+              out[(int64_t)row * N + ch] = g / (1.0f + expf(-g)) * u;
             }
           }
         }
-      } else {
+      } else if (m < BMW) {   // down projection (packed: lanes 0-63 only)
+        const int ch = ti.ctile * BMW + m;
         const float sw = w_scale[(int64_t)ti.group * N + ch];
         for (int n0 = 0; n0 < nvalid; n0 += 16) {
           float acc[16];
@@ -438,20 +510,20 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int BN, bool GATEUP>
+template <int BN, int BMW, bool GATEUP>
 int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
         const float* w_scale, const int32_t* offsets, int groups, int N, int K,
         float* out, cudaStream_t stream, bool pdl) {
-  using C = Cfg<BN, GATEUP>;
+  using C = Cfg<BN, BMW, GATEUP>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
-  if (!make_tmap(&tm_w, W, w_rows, K, kBM)) return -3;
+  if (!make_tmap(&tm_w, W, w_rows, K, BMW)) return -3;
   if (!make_tmap(&tm_a, A, a_rows, K, BN)) return -3;
-  auto kern = grouped_gemm_kernel<BN, GATEUP>;
+  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
-  const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / kBM);
+  const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / BMW);
   const int grid = (int)std::min<int64_t>(upper, sm_count());
   if (grid <= 0) return 0;
   const cudaError_t e = launch_kernel(
@@ -470,16 +542,16 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
   if (kind == 0) {
-    if (avg <= 16) return run<16, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-    if (avg <= 32) return run<32, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-    if (avg <= 64) return run<64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-    return run<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 16) return run<16, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 32) return run<32, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 64) return run<64, 128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    return run<128, 128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   }
-  if (avg <= 16) return run<16, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-  if (avg <= 32) return run<32, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-  if (avg <= 64) return run<64, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-  if (avg <= 128) return run<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
-  return run<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 16) return run<16, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 32) return run<32, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 64) return run<64, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  if (avg <= 128) return run<128, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  return run<256, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
 }
 
 }  // namespace moe

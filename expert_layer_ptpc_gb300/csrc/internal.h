@@ -55,12 +55,15 @@ cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
                            cudaStream_t stream, bool pdl);
 
 // Per-row e4m3 quantisation with scatter; `gate_w` non-null also computes
-// gate_out[r] = sigmoid(in[r] . gate_w) (bf16 input only).
+// gate_out[r] = sigmoid(in[r] . gate_w) (bf16 input only). `release_early`
+// lets the next kernel launch before this one's dependency wait (see
+// quant.cu for when that is safe).
 cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          const int32_t* dst_rows, int copies,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
-                         float* gate_out, cudaStream_t stream, bool pdl);
+                         float* gate_out, cudaStream_t stream, bool pdl,
+                         bool release_early);
 
 // Largest row length launch_quant handles.
 constexpr int kMaxQuantCols = 32768;

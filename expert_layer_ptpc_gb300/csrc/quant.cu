@@ -54,12 +54,17 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
     const InT* __restrict__ in, int64_t rows, int cols,
     const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
     uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
-    const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out) {
+    const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out,
+    int release_early) {
   __shared__ float red_max[kMaxThreads / 32];
   __shared__ float red_dot[kMaxThreads / 32];
   __shared__ int64_t dst[kMaxTopK + 1];
+  // release_early: the next kernel may start before this one waits. Only
+  // for a successor whose pre-wait part reads nothing this kernel's
+  // predecessor produces (the down GEMM reads the tile map and weights).
+  if (release_early) pdl_launch_dependents();
   pdl_wait();
-  pdl_launch_dependents();
+  if (!release_early) pdl_launch_dependents();
   const int64_t r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
@@ -156,7 +161,8 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
                         const int32_t* dst_rows, int copies,
                         int64_t extra_row_base, uint8_t* out_q,
                         float* out_scale, const __nv_bfloat16* gate_w,
-                        float* gate_out, cudaStream_t stream, bool pdl) {
+                        float* gate_out, cudaStream_t stream, bool pdl,
+                        bool release_early) {
   const int nunits = cols / kVec;
   int threads = std::min(kMaxThreads, ((nunits + 31) / 32) * 32);
   const int units = (nunits + threads - 1) / threads;
@@ -164,7 +170,7 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
   auto go = [&](auto kern) {
     return launch_kernel(pdl, grid, block, 0, stream, kern, in, rows, cols,
                          dst_rows, copies, extra_row_base, out_q, out_scale,
-                         gate_w, gate_out);
+                         gate_w, gate_out, release_early ? 1 : 0);
   };
   if (units <= 1) return go(quant_rows_kernel<InT, 1>);
   if (units <= 2) return go(quant_rows_kernel<InT, 2>);
@@ -177,16 +183,18 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          const int32_t* dst_rows, int copies,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
-                         float* gate_out, cudaStream_t stream, bool pdl) {
+                         float* gate_out, cudaStream_t stream, bool pdl,
+                         bool release_early) {
   if (rows == 0) return cudaSuccess;
   if (in_dtype == 0)
     return launch_rows(static_cast<const __nv_bfloat16*>(in), rows, cols,
                        dst_rows, copies, extra_row_base, out_q, out_scale,
                        reinterpret_cast<const __nv_bfloat16*>(gate_w), gate_out,
-                       stream, pdl);
+                       stream, pdl, release_early);
   return launch_rows(static_cast<const float*>(in), rows, cols, dst_rows, copies,
                      extra_row_base, out_q, out_scale,
-                     (const __nv_bfloat16*)nullptr, (float*)nullptr, stream, pdl);
+                     (const __nv_bfloat16*)nullptr, (float*)nullptr, stream, pdl,
+                     release_early);
 }
 
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
