@@ -135,6 +135,23 @@ class ClockSampler:
                 "window": window}
 
 
+def max_over_ranks(x, device):
+    """The largest value of x over all ranks (a replica run is as slow as its
+    slowest rank); x itself when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_tokens_per_s(T, world, max_ms):
+    """Whole-job throughput of `world` replicas that each process T tokens per
+    step, the step taking max_ms on the slowest rank."""
+    return world * T / (max_ms * 1e-3)
+
+
 def physical_gpu(local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     parts = [p for p in vis.split(",") if p.strip()]
@@ -427,10 +444,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     phase_ms = [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(nev - 1)]
     profiled_ms = sum(e[0].elapsed_time(e[nev - 1]) for e in evs) / len(evs)
     mean_ms = sum(step_ms) / len(step_ms)
-    t = torch.tensor([mean_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(mean_ms, dev)
 
     # e2e: the same forward through the public API from pinned host buffers,
     # copies in and out inside the timed region
@@ -461,10 +475,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         e_ms.append((a, b))
     torch.cuda.synchronize()
     e2e_mean = sum(a.elapsed_time(b) for a, b in e_ms) / len(e_ms)
-    t2 = torch.tensor([e2e_mean], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-    e2e_max = float(t2.item())
+    e2e_max = max_over_ranks(e2e_mean, dev)
     h2d = x.numel() * 2 + (logits.numel() * 4 if logits is not None else 0)
     d2h = out.numel() * 2
 
@@ -506,7 +517,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "achieved_fp8_tflops": F / (max_ms * 1e-3) / 1e12,
         "t_roof_ms": t_roof * 1e3, "frac": t_roof / (max_ms * 1e-3)}
     clocks = sampler.summary(t_wall0, t_wall1)
-    tokens_per_s = world * cfg.T / (max_ms * 1e-3)
+    tokens_per_s = replica_tokens_per_s(cfg.T, world, max_ms)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -523,7 +534,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         "layer_roofline": layer_roofline,
         "kernel_ms": kernel_ms, "dominant_kernel": dominant,
         "profiled_ms_per_step": profiled_ms,
-        "e2e": {"value": world * cfg.T / (e2e_max * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": replica_tokens_per_s(cfg.T, world, e2e_max),
+                "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_max},
         "gpu_launches": kernel_launches_per_step(cfg) * args.steps,

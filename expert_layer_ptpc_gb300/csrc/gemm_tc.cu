@@ -65,7 +65,10 @@ struct Cfg {
   static constexpr int kTxBytes = (GATEUP ? 2 : 1) * BMW * kBK + kBTile;
   static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
   static constexpr int kAccCols = kNumA * BN;                  // one buffer
-  static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+  // two accumulator buffers (epilogue of one tile overlaps the next tile's
+  // MMAs) when they fit in the 512 TMEM columns, else one
+  static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;
+  static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols);
   static constexpr int kNumBars = 2 * kStages + 7;
   static constexpr int kXBytes = (GATEUP && kPacked) ? 64 * 16 * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes +
@@ -237,7 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
+      // small token tiles read each weight tile once: stream it past L2;
+      // wider tiles share a weight tile between neighbouring token tiles
+      const uint64_t pol_w =
+          BN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
       const uint64_t pol_a = l2_policy_evict_last();
       int last_phase[C::kStages];
 #pragma unroll
@@ -316,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles;
            tile += gridDim.x, ++it) {
-        const int ab = it & 1;
-        const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+        const int ab = it % C::kAccBufs;
+        const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
         if (!mbar_wait_bounded(acce_bar(ab), acc_ph ^ 1, abort_flag, err,
                                kErrTimeoutMma)) break;
         tc_fence_after_sync();
@@ -364,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     uint32_t xc = 0;                      // gate/up exchanges so far (packed)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++it) {
-      const int ab = it & 1;
-      const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+      const int ab = it % C::kAccBufs;
+      const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
       if (!warp_wait(accf_bar(ab), acc_ph, abort_flag, err, kErrTimeoutEpilogue))
         break;
       tc_fence_after_sync();

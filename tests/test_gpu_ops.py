@@ -205,6 +205,7 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
     (3, [200, 129, 64], 128, 1024, 0),               # BN 128 / 64
     (5, [300, 0, 257, 511, 2], 384, 384, 0),         # BN 128 / 256, tails
     (2, [1000, 24], 128, 4096, 0),                   # long K
+    (2, [600, 301], 256, 512, 0),                    # BN 256 (wide tiles)
     (6, [5, 9, 0, 300, 2, 3], 256, 256, 16),         # hint forces BN 16
 ])
 def test_grouped_gemm(gateup, G, counts, N, K, hint):
