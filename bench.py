@@ -152,6 +152,25 @@ def replica_tokens_per_s(T, world, max_ms):
     return world * T / (max_ms * 1e-3)
 
 
+def captured_traffic(algorithmic_bytes, bn_decode):
+    """DRAM traffic of the gate/up launch from the committed ncu record
+    (profiles/traffic_gateup_decode.json), scaled to this launch by its
+    algorithmic bytes; None when the record is missing, was taken on another
+    tile shape, or the kernel sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_gateup_decode.json")
+    if not bn_decode or not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != rec["sources_sha256"]:
+        return None
+    return rec["traffic_per_algorithmic_byte"] * algorithmic_bytes
+
+
 def physical_gpu(local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     parts = [p for p in vis.split(",") if p.strip()]
@@ -506,9 +525,17 @@ def run_ours(args, cfg, rank, world, local_rank):
         gemm_roofline = {"bound": "hbm", "achieved": ach, "peak": hbm,
                          "unit": "GB/s", "frac": ach / hbm,
                          "peak_source": peak_src}
+    # decode-sized token tiles (<= 16 rows per expert on average) run the
+    # instantiation the traffic record was captured on
+    decode_tiles = cfg.rows / max(1, cfg.groups) <= 16
+    traffic = captured_traffic(gu_bytes, decode_tiles)
     gemm_roofline.update({
         "kernel": "gate/up grouped GEMM (tcgen05, SwiGLU epilogue)",
-        "traffic": None, "algorithmic_bytes_per_launch": gu_bytes,
+        "traffic": traffic,
+        "traffic_source": ("ncu capture scaled by algorithmic bytes "
+                           "(profiles/traffic_gateup_decode.json)"
+                           if traffic is not None else None),
+        "algorithmic_bytes_per_launch": gu_bytes,
         "flops_per_launch": gu_flops, "ms_per_launch": gemm_ms})
     t_roof = max(F / (fp8_peak * 1e12), B / (hbm * 1e9))
     layer_roofline = {

@@ -1,0 +1,620 @@
+// PTPC FP8 grouped GEMMs on a pair of SMs (tcgen05 cta_group::2).
+//
+// Same computation as gemm_tc.cu ("Optimizing Qwen 3.5 397B MoE on Ironwood
+// TPU7x", GMM V2 paragraph; "Ultimate Latency Optimization of Qwen3 and
+// Qwen3-VL on AMD MI300X Series", section 2.1.1), for wide token tiles where
+// the tensor cores, not HBM, set the pace. Two CTAs of a cluster run one MMA
+// of M = 256 rows: each CTA holds 128 weight rows and half of the BN token
+// rows in its shared memory, and receives its 128 accumulator rows (x BN
+// token columns) in its own TMEM. Each SM therefore loads half of the token
+// tile that a single-CTA 128-row MMA of the same width would need, which
+// halves the shared-memory traffic per multiply-add on the B side.
+//
+// Tile = 256 MMA rows x BN tokens of one expert:
+//   gate/up: 128 channels; each CTA packs 64 gate rows and the matching 64
+//            up rows (its channels ctile*128 + rank*64 + [0, 64)), so SwiGLU
+//            partners meet in one CTA (exchanged through shared memory);
+//   down:    256 output channels, 128 per CTA.
+//
+// Roles per CTA (11 warps), both CTAs of the pair:
+//   warp 0      TMEM allocation (both CTAs); the MMA issuer (leader)
+//   warps 1-4   epilogue on this CTA's TMEM rows
+//   warps 5-10  TMA producers, one box each: this CTA's two 64-row weight
+//               boxes and its 32-row token boxes, into its own ring of
+//               stages; both CTAs' copies complete on the leader's stage
+//               barrier, which expects both halves
+// The leader's commits are multicast to both CTAs (stage free, accumulator
+// ready); both CTAs' epilogues release an accumulator buffer by arriving on
+// the leader's barrier. All waits are bounded (common.cuh).
+#include <algorithm>
+
+#include "gemm_common.cuh"
+
+namespace moe {
+namespace {
+
+using namespace gemm;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+      "r"(ncols)
+      : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+               "r"(ncols)
+               : "memory");
+}
+// D (+)= A * B^T over the CTA pair (M = 256), issued by one leader thread.
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc,
+                                         uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at this offset in every CTA of `mask` when the
+// leader's MMAs issued so far complete.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar)
+      : "memory");
+}
+
+// 2D tiled load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void* tmap,
+                                                 int32_t x, int32_t y, uint32_t bar,
+                                                 uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(cache_policy)
+      : "memory");
+}
+
+// Bounded waits on barriers that other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                     volatile int* abort_flag,
+                                                     unsigned* err, unsigned code) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((spin & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag,
+                                                  unsigned* err, unsigned code) {
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    const bool ok = mbar_try_wait_cluster(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((spin & 63u) == 63u) {
+      int bail = 0;
+      if (lane_id() == 0) {
+        if (*abort_flag) {
+          bail = 1;
+        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicOr(err, code);
+          bail = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, bail, 0)) return false;
+    }
+  }
+}
+
+template <int BN, bool GATEUP>
+struct PairCfg {
+  static constexpr int kHalfB = BN / 2;                  // token rows per CTA
+  // TMA boxes of one stage (per CTA): two 64-row weight boxes, then 32-row
+  // token boxes; one producer warp per box
+  static constexpr int kTBoxRows = 32;
+  static constexpr int kTBoxes = kHalfB / kTBoxRows;
+  static constexpr int kBoxes = 2 + kTBoxes;
+  static_assert(kBoxes <= kMaxBoxes, "one producer warp per box");
+  static constexpr int kATile = 128 * kBK;               // this CTA's 128 MMA rows
+  static constexpr int kBTile = kHalfB * kBK;
+  static constexpr int kStage = kATile + kBTile;
+  static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
+  static constexpr int kAccBufs = 2 * BN <= 512 ? 2 : 1;
+  static constexpr int kTmemCols = pow2_at_least(kAccBufs * BN);
+  static constexpr int kChunk = 32;                      // epilogue columns per pass
+  static constexpr int kXBytes = GATEUP ? 64 * kChunk * 4 : 0;
+  static constexpr int kTileCh = GATEUP ? 128 : 256;     // channels per tile
+  static constexpr int kNumBars = 2 * kStages + 7;
+  // Reserved after the stages: one more token half-tile, so that any operand
+  // read starting at a stage stays inside this CTA's allocation.
+  static constexpr int kPadBytes = kBTile;
+  static constexpr int kSmemBytes = 1024 + kStages * kStage + kPadBytes + kXBytes +
+                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
+  static_assert(kStages >= 3, "pipeline depth");
+};
+
+template <int BN, bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
+    const __grid_constant__ CUtensorMap tm_w,
+    const __grid_constant__ CUtensorMap tm_a, const float* __restrict__ a_scale,
+    const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
+    int groups, int N, int K, float* __restrict__ out,
+    unsigned* __restrict__ err) {
+  using C = PairCfg<BN, GATEUP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kPadBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
+                                               C::kPadBytes + C::kXBytes);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
+  __shared__ int warp_tot[kThreads / 32 + 1];
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_rank();        // 0: the leader issues the MMAs
+  const int first_tile = (int)cluster_index();
+  const int tile_step = (int)cluster_count();
+  const int n_ctiles = N / C::kTileCh;
+  const int kblocks = K / kBK;
+
+  // full (leader's is the one used): both halves of a stage landed;
+  // empty: stage free in this CTA (the leader's multicast commit)
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  auto accf_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
+  auto acce_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * C::kStages + 4);
+  const uint32_t xfull_bar = smem_u32(bars + 2 * C::kStages + 5);
+  const uint32_t xempty_bar = smem_u32(bars + 2 * C::kStages + 6);
+  auto stage_a = [&](int s) { return smem_u32(smem + s * C::kStage); };
+  auto stage_b = [&](int s) { return smem_u32(smem + s * C::kStage + C::kATile); };
+
+  // ---------------- set-up ----------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), C::kBoxes);   // the leader's producer warps
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 8);     // one per epilogue warp of both CTAs (leader)
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(xfull_bar, 4);       // one per epilogue warp
+    mbar_init(xempty_bar, 4);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_a);
+  }
+  if (warp == kMmaWarp) tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
+
+  {   // tile prefix: prefix[g] = sum_{g' < g} ceil(rows_g' / BN) * n_ctiles
+    const int per = (groups + kThreads - 1) / kThreads;
+    const int g0 = threadIdx.x * per;
+    int local = 0;
+    for (int g = g0; g < g0 + per && g < groups; ++g)
+      local += ((offsets[g + 1] - offsets[g] + BN - 1) / BN) * n_ctiles;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - local;
+    for (int g = g0; g < g0 + per && g < groups; ++g) {
+      prefix[g] = run;
+      run += ((offsets[g + 1] - offsets[g] + BN - 1) / BN) * n_ctiles;
+    }
+    if (threadIdx.x == kThreads - 1) prefix[groups] = base + incl;
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total_tiles = prefix[groups];
+
+  // this CTA's first weight row of a tile (gate rows for gate/up)
+  auto weight_row = [&](const TileInfo& ti) {
+    return GATEUP ? ti.group * 2 * N + ti.ctile * 128 + (int)rank * 64
+                  : ti.group * N + ti.ctile * 256 + (int)rank * 128;
+  };
+  // Both CTAs' copies of stage s complete on the leader's full[s]: the
+  // leader's own with a plain TMA, the peer's with the pair form.
+  auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y, int s,
+                  uint64_t pol) {
+    if (rank == 0) tma_load_2d(dst, tm, x, y, full_bar(s), pol);
+    else tma_load_2d_pair(dst, tm, x, y, map_to_rank(full_bar(s), 0), pol);
+  };
+
+  const int box = producer_box(warp);
+  if (box >= 0) {
+    // ---------------- TMA producers (both CTAs): box `box` of every stage ----------------
+    const bool weight_box = box < 2;
+    if (lane == 0 && box < C::kBoxes) {
+      const uint64_t pol = weight_box ? l2_policy_evict_normal() : l2_policy_evict_last();
+      // bytes of this box in one CTA; the leader expects both CTAs' bytes
+      const uint32_t bytes = weight_box ? 64u * kBK : (uint32_t)(C::kTBoxRows * kBK);
+      auto issue = [&](int s, int kb, const TileInfo& ti) {
+        const int x = kb * kBK;
+        if (box == 0)        // gate rows, or the first half of the down rows
+          load(stage_a(s), &tm_w, x, weight_row(ti), s, pol);
+        else if (box == 1)   // up rows, or the second half of the down rows
+          load(stage_a(s) + 64 * kBK, &tm_w, x, weight_row(ti) + (GATEUP ? N : 64), s,
+               pol);
+        else {               // 32 rows of this CTA's half of the token tile
+          const int t = box - 2;
+          load(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
+               ti.row0 + (int)rank * C::kHalfB + t * C::kTBoxRows, s, pol);
+        }
+      };
+      auto expect = [&](int s) {
+        if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+      };
+      int last_phase[C::kStages];
+#pragma unroll
+      for (int i = 0; i < C::kStages; ++i) last_phase[i] = -1;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      // weights and the tile map do not depend on the previous kernel
+      int npre = 0;
+      TileInfo t0{};
+      if (weight_box && first_tile < total_tiles) {
+        t0 = decode_tile(first_tile, prefix, groups, offsets, BN);
+        npre = kblocks < C::kStages ? kblocks : C::kStages;
+        for (int kb = 0; kb < npre; ++kb) {
+          expect(kb);
+          issue(kb, kb, t0);
+#pragma unroll
+          for (int i = 0; i < C::kStages; ++i)
+            if (i == kb) last_phase[i] = 0;
+        }
+        s = npre % C::kStages;
+        ph = npre == C::kStages ? 1u : 0u;
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step) {
+        const TileInfo ti = (tile == first_tile && npre > 0)
+                                ? t0
+                                : decode_tile(tile, prefix, groups, offsets, BN);
+        for (int kb = tile == first_tile ? npre : 0; kb < kblocks; ++kb) {
+          if (!wait_cluster_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
+                                    kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          expect(s);
+          issue(s, kb, ti);
+#pragma unroll
+          for (int i = 0; i < C::kStages; ++i)
+            if (i == s) last_phase[i] = (int)ph;
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // drain: this CTA's copies have landed before its memory is released.
+      // The leader sees them (both halves) on its full barriers; the peer
+      // sees a stage consumed, hence landed, when the leader frees it.
+#pragma unroll
+      for (int i = 0; i < C::kStages; ++i) {
+        if (last_phase[i] >= 0) {
+          volatile int no_abort = 0;
+          if (rank == 0)
+            mbar_wait_bounded(full_bar(i), (uint32_t)last_phase[i], &no_abort, err,
+                              kErrTimeoutDrain);
+          else
+            wait_cluster_bounded(empty_bar(i), (uint32_t)last_phase[i], &no_abort,
+                                 err, kErrTimeoutDrain);
+        }
+      }
+    } else {
+      pdl_wait();
+      pdl_launch_dependents();
+    }
+  } else if (warp == kMmaWarp) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (leader) ----------------
+      constexpr uint32_t idesc = idesc_e4m3_f32(256, BN);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step, ++it) {
+        const int ab = it % C::kAccBufs;
+        const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
+        if (!wait_cluster_bounded(acce_bar(ab), acc_ph ^ 1, abort_flag, err,
+                                  kErrTimeoutMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_cluster_bounded(full_bar(s), ph, abort_flag, err, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a = stage_a(s), b = stage_b(s);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_pair(d, smem_desc_k_sw128(a + kk * 32), smem_desc_k_sw128(b + kk * 32),
+                     idesc, (kb | kk) != 0);
+          mma_commit_pair_mc(empty_bar(s), 0x3);   // stage free in both CTAs
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (ok) mma_commit_pair_mc(accf_bar(ab), 0x3);   // accumulators ready
+      }
+      mma_commit_pair(drain_bar);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(drain_bar, 0, &no_abort, err, kErrTimeoutDrain);
+    }
+  } else {
+    // ---------------- epilogue (both CTAs) ----------------
+    pdl_wait();
+    pdl_launch_dependents();
+    const int q = warp & 3;               // TMEM lane quarter of this warp
+    const int m = q * 32 + lane;          // accumulator row of this thread
+    int it = 0;
+    uint32_t xc = 0;
+    bool ok = true;
+    for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step, ++it) {
+      const int ab = it % C::kAccBufs;
+      const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
+      if (!warp_wait_cluster(accf_bar(ab), acc_ph, abort_flag, err,
+                             kErrTimeoutEpilogue))
+        break;
+      tc_fence_after_sync();
+      const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
+      const int nvalid = min(BN, ti.row_end - ti.row0);
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN);
+      if (GATEUP) {
+        // lanes 0-63 hold gate, 64-127 up, of channels ctile*128 + rank*64 +
+        // [0, 64). Per 32-column chunk the gate threads hand their columns
+        // 16-31 to the up threads and receive up columns 0-15, so every
+        // thread finishes 16 outputs.
+        const bool is_gate = q < 2;
+        const int pm = is_gate ? m : m - 64;          // channel within the CTA
+        const int ch = ti.ctile * 128 + (int)rank * 64 + pm;
+        const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
+        const float swu = w_scale[(int64_t)ti.group * 2 * N + N + ch];
+        float* xg = xbuf;              // gate values of columns 16-31 [16][64]
+        float* xu = xbuf + 16 * 64;    // up values of columns 0-15    [16][64]
+        for (int n0 = 0; ok && n0 < nvalid; n0 += C::kChunk, ++xc) {
+          float a[C::kChunk];
+          tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&a[0]));
+          tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&a[16]));
+          tmem_ld_wait();
+          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+          if (!warp_wait(xempty_bar, (xc & 1u) ^ 1u, abort_flag, err,
+                         kErrTimeoutEpilogue)) {
+            ok = false;
+            break;
+          }
+          if (is_gate) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xg[j * 64 + pm] = a[16 + j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xu[j * 64 + pm] = a[j];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xfull_bar);
+          if (!warp_wait(xfull_bar, xc & 1u, abort_flag, err, kErrTimeoutEpilogue)) {
+            ok = false;
+            break;
+          }
+          float g[16], u[16];
+          const int c0 = is_gate ? 0 : 16;           // this thread's columns
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            g[j] = is_gate ? a[j] : xg[j * 64 + pm];
+            u[j] = is_gate ? xu[j * 64 + pm] : a[16 + j];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xempty_bar);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float sx = __shfl_sync(0xffffffffu, sx_l, c0 + j);
+            if (n0 + c0 + j < nvalid) {
+              const float gg = g[j] * sx * swg;
+              const float uu = u[j] * sx * swu;
+              out[(int64_t)(ti.row0 + n0 + c0 + j) * N + ch] =
+                  gg / (1.0f + expf(-gg)) * uu;
+            }
+          }
+        }
+      } else {
+        const int ch = ti.ctile * 256 + (int)rank * 128 + m;
+        const float sw = w_scale[(int64_t)ti.group * N + ch];
+        for (int n0 = 0; n0 < nvalid; n0 += 32) {
+          float acc[32];
+          tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
+          tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
+          tmem_ld_wait();
+          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float sx = __shfl_sync(0xffffffffu, sx_l, j);
+            if (n0 + j < nvalid)
+              out[(int64_t)(ti.row0 + n0 + j) * N + ch] = acc[j] * sx * sw;
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(acce_bar(ab));
+        else mbar_arrive_cluster(map_to_rank(acce_bar(ab), 0));
+      }
+    }
+  }
+
+  // ---------------- tear-down ----------------
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();   // the leader's MMAs (which use both CTAs) are complete
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, bool GATEUP>
+int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
+             const uint8_t* W, const float* w_scale, const int32_t* offsets,
+             int groups, int N, int K, float* out, cudaStream_t stream, bool pdl) {
+  using C = PairCfg<BN, GATEUP>;
+  CUtensorMap tm_w, tm_a;
+  const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
+  if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
+  if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
+  auto kern = grouped_gemm_pair_kernel<BN, GATEUP>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return -3;
+  const int64_t upper =
+      ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / C::kTileCh);
+  // Persistent clusters: launch no more than can be resident at once (the
+  // SM pairs a cluster needs are fewer than half the SMs on some parts).
+  static int resident[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (resident[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+      n = sm_count() / 2;
+    resident[dev] = n;
+  }
+  const int clusters = (int)std::min<int64_t>(upper, resident[dev]);
+  if (clusters <= 0) return 0;
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.numAttrs = pdl ? 2 : 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, a_scale, w_scale, offsets, groups,
+                         N, K, out, device_error_word());
+  return e == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace
+
+bool grouped_gemm_pair_supported(int kind, int N) {
+  return N % (kind == 0 ? 128 : 256) == 0;
+}
+
+int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
+                             int64_t a_rows, const uint8_t* W,
+                             const float* w_scale, const int32_t* offsets,
+                             int groups, int N, int K, float* out, int bn,
+                             cudaStream_t stream, bool pdl) {
+  if (kind == 0) {
+    if (bn <= 128)
+      return run_pair<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
+                                 K, out, stream, pdl);
+    return run_pair<256, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
+                               out, stream, pdl);
+  }
+  if (bn <= 128)
+    return run_pair<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
+                                K, out, stream, pdl);
+  return run_pair<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
+                              out, stream, pdl);
+}
+
+}  // namespace moe

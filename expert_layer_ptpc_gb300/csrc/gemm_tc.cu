@@ -18,38 +18,30 @@
 // For gate/up, two accumulators (gate, up) share one B tile, so a thread
 // holds gate and up of the same channel and token and applies SwiGLU alone.
 //
-// CTA = 6 warps, persistent over a static tile sequence:
-//   warp 0      TMA producer (one lane): weight and activation tiles into a
-//               STAGES-deep ring of shared-memory stages (128-byte swizzle)
-//   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma
+// CTA = 11 warps, persistent over a static tile sequence:
+//   warp 0      TMEM allocator and MMA issuer (one lane): tcgen05.mma
 //               kind::f8f6f4, M=128, N=BN, K=32 per instruction, into one of
 //               two accumulator buffers
-//   warps 2-5   epilogue: tcgen05.ld of its 32 TMEM lanes, PTPC dequant,
+//   warps 1-4   epilogue: tcgen05.ld of its 32 TMEM lanes, PTPC dequant,
 //               SwiGLU, fp32 stores (coalesced: a warp writes 32 channels)
+//   warps 5-10  TMA producers, one lane each: the 64-row weight boxes and the
+//               token boxes of a stage (one box per warp), into a STAGES-
+//               deep ring of shared-memory stages (128-byte swizzle)
 // Every wait is bounded (common.cuh): a wait that runs out raises the device
 // error word, the CTA's roles stop, in-flight copies and MMAs are drained and
 // the TMEM is freed before the kernel returns.
-#include <cudaTypedefs.h>
-
+#include <cstdlib>
 #include <mutex>
 
-#include "common.cuh"
-#include "internal.h"
+#include "gemm_common.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kBM = 128;   // output channels per tile (MMA M)
-constexpr int kBK = 128;   // K bytes per stage = one 128-byte swizzle row
-constexpr int kStageBudget = 200 * 1024;
+using namespace gemm;
 
-constexpr int pow2_at_least(int v) {
-  int p = 32;
-  while (p < v) p <<= 1;
-  return p;
-}
+constexpr int kBM = 128;   // output channels per tile (MMA M)
 
 template <int BN, int BMW, bool GATEUP>
 struct Cfg {
@@ -62,7 +54,14 @@ struct Cfg {
   static constexpr int kATile = kBM * kBK;                     // one 128-row operand
   static constexpr int kBTile = BN * kBK;
   static constexpr int kStage = kNumA * kATile + kBTile;
-  static constexpr int kTxBytes = (GATEUP ? 2 : 1) * BMW * kBK + kBTile;
+  // TMA boxes of one stage: 64-row weight boxes (gate/up: two per 128-row
+  // tile, or one gate + one up when packed; down: two), then token boxes of
+  // up to 64 rows. One producer warp per box.
+  static constexpr int kWBoxes = GATEUP ? (kPacked ? 2 : 4) : BMW / 64;
+  static constexpr int kTBoxRows = BN < 64 ? BN : 64;
+  static constexpr int kTBoxes = BN / kTBoxRows;
+  static constexpr int kBoxes = kWBoxes + kTBoxes;
+  static_assert(kBoxes <= kMaxBoxes, "one producer warp per box");
   static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
   static constexpr int kAccCols = kNumA * BN;                  // one buffer
   // two accumulator buffers (epilogue of one tile overlaps the next tile's
@@ -77,56 +76,6 @@ struct Cfg {
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kStages >= 2, "pipeline depth");
 };
-
-struct TileInfo {
-  int group, ctile, row0, row_end;
-};
-
-__device__ __forceinline__ TileInfo decode_tile(int tile, const int* prefix,
-                                                int groups, const int32_t* offsets,
-                                                int bn) {
-  // the largest g with prefix[g] <= tile; empty groups share their
-  // successor's prefix value, so this is the non-empty group owning the tile
-  int lo = 0, hi = groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= tile) lo = mid; else hi = mid - 1;
-  }
-  const int g = lo;
-  const int start = offsets[g], end = offsets[g + 1];
-  const int tt = (end - start + bn - 1) / bn;
-  const int local = tile - prefix[g];
-  TileInfo t;
-  t.group = g;
-  t.ctile = local / tt;
-  t.row0 = start + (local % tt) * bn;
-  t.row_end = end;
-  return t;
-}
-
-// Warp-uniform bounded wait (all lanes return the same answer).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag,
-                                          unsigned* err, unsigned code) {
-  const unsigned long long t0 = global_timer_ns();
-  for (uint32_t spin = 0;; ++spin) {
-    const bool ok = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    if ((spin & 63u) == 63u) {
-      int bail = 0;
-      if (lane_id() == 0) {
-        if (*abort_flag) {
-          bail = 1;
-        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-          *abort_flag = 1;
-          atomicOr(err, code);
-          bail = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, bail, 0)) return false;
-    }
-  }
-}
 
 template <int BN, int BMW, bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
@@ -168,12 +117,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   // ---------------- set-up ----------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), C::kBoxes);   // one arrival per box
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 128);
+      mbar_init(acce_bar(b), 4);     // one per epilogue warp
     }
     mbar_init(drain_bar, 1);
     mbar_init(xfull_bar, 64);
@@ -185,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_a);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
 
   // tile prefix: prefix[g] = sum_{g' < g} ceil(rows_g' / BN) * n_ctiles
   {
@@ -221,73 +170,80 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   auto weight_row = [&](const TileInfo& ti) {
     return GATEUP ? ti.group * 2 * N + ti.ctile * BMW : ti.group * N + ti.ctile * BMW;
   };
-  // the weight loads of one stage
-  auto load_weights = [&](int s, int kb, int wrow, uint64_t pol) {
-    if (GATEUP) {
-      if (C::kPacked) {   // 64 gate rows, then the matching 64 up rows
-        tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow, full_bar(s), pol);
-        tma_load_2d(stage_a(s, 0) + 64 * kBK, &tm_w, kb * kBK, wrow + N,
-                    full_bar(s), pol);
-      } else {
-        tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow, full_bar(s), pol);
-        tma_load_2d(stage_a(s, 1), &tm_w, kb * kBK, wrow + N, full_bar(s), pol);
-      }
-    } else {
-      tma_load_2d(stage_a(s, 0), &tm_w, kb * kBK, wrow, full_bar(s), pol);
-    }
-  };
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
+  const int box = producer_box(warp);
+  if (box >= 0) {
+    // ---------------- TMA producers: box `box` of every stage ----------------
+    const bool weight_box = box < C::kWBoxes;
+    if (lane == 0 && box < C::kBoxes) {
       // small token tiles read each weight tile once: stream it past L2;
       // wider tiles share a weight tile between neighbouring token tiles
-      const uint64_t pol_w =
-          BN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
-      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol = !weight_box ? l2_policy_evict_last()
+                           : BN <= 32  ? l2_policy_evict_first()
+                                       : l2_policy_evict_normal();
+      const uint32_t bytes =
+          weight_box ? 64u * kBK : (uint32_t)(C::kTBoxRows * kBK);
+      auto issue = [&](int s, int kb, const TileInfo& ti) {
+        const int x = kb * kBK;
+        if (weight_box) {
+          const int wrow = weight_row(ti);
+          int row, off;   // weight row of the box and its offset in the stage
+          if (GATEUP && !C::kPacked) {   // boxes 0,1: gate halves; 2,3: up halves
+            row = wrow + (box >= 2 ? N : 0) + (box & 1) * 64;
+            off = (box >= 2 ? C::kATile : 0) + (box & 1) * 64 * kBK;
+          } else if (GATEUP) {           // packed: 64 gate rows, 64 up rows
+            row = wrow + (box == 1 ? N : 0);
+            off = box * 64 * kBK;
+          } else {                       // down: the two halves of the tile
+            row = wrow + box * 64;
+            off = box * 64 * kBK;
+          }
+          tma_load_2d(stage_a(s, 0) + off, &tm_w, x, row, full_bar(s), pol);
+        } else {
+          const int t = box - C::kWBoxes;
+          tma_load_2d(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
+                      ti.row0 + t * C::kTBoxRows, full_bar(s), pol);
+        }
+      };
       int last_phase[C::kStages];
 #pragma unroll
-      for (int s = 0; s < C::kStages; ++s) last_phase[s] = -1;
+      for (int i = 0; i < C::kStages; ++i) last_phase[i] = -1;
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       // The weights and the tile map (offsets come from the permutation, two
-      // launches back) do not depend on the previous kernel: stream the first
-      // stages' weight tiles before waiting for it, then add the activations.
+      // launches back) do not depend on the previous kernel: the weight
+      // producers fill the first stages before waiting for it.
       const int first = blockIdx.x;
       int npre = 0;
       TileInfo t0{};
-      if (first < total_tiles) {
+      if (weight_box && first < total_tiles) {
         t0 = decode_tile(first, prefix, groups, offsets, BN);
         npre = kblocks < C::kStages ? kblocks : C::kStages;
         for (int kb = 0; kb < npre; ++kb) {   // fresh ring: stage kb, phase 0
-          mbar_arrive_expect_tx(full_bar(kb), C::kTxBytes);
-          load_weights(kb, kb, weight_row(t0), pol_w);
+          mbar_arrive_expect_tx(full_bar(kb), bytes);
+          issue(kb, kb, t0);
+#pragma unroll
+          for (int i = 0; i < C::kStages; ++i)
+            if (i == kb) last_phase[i] = 0;
         }
+        s = npre % C::kStages;
+        ph = npre == C::kStages ? 1u : 0u;
       }
       pdl_wait();
       pdl_launch_dependents();
-      for (int kb = 0; kb < npre; ++kb) {
-        tma_load_2d(stage_b(kb), &tm_a, kb * kBK, t0.row0, full_bar(kb), pol_a);
-#pragma unroll
-        for (int i = 0; i < C::kStages; ++i)
-          if (i == kb) last_phase[i] = 0;
-      }
-      s = npre % C::kStages;
-      ph = npre == C::kStages ? 1u : 0u;
       for (int tile = first; ok && tile < total_tiles; tile += gridDim.x) {
-        const TileInfo ti =
-            tile == first ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
-        const int wrow = weight_row(ti);
+        const TileInfo ti = (tile == first && npre > 0)
+                                ? t0
+                                : decode_tile(tile, prefix, groups, offsets, BN);
         for (int kb = tile == first ? npre : 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                  kErrTimeoutProducer)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
-          load_weights(s, kb, wrow, pol_w);
-          tma_load_2d(stage_b(s), &tm_a, kb * kBK, ti.row0, full_bar(s), pol_a);
+          mbar_arrive_expect_tx(full_bar(s), bytes);
+          issue(s, kb, ti);
 #pragma unroll
           for (int i = 0; i < C::kStages; ++i)
             if (i == s) last_phase[i] = (int)ph;
@@ -310,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       pdl_wait();
       pdl_launch_dependents();
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     pdl_wait();
     pdl_launch_dependents();
@@ -458,22 +414,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(acce_bar(ab));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(ab));
     }
   }
 
   // ---------------- tear-down ----------------
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
+template <int BN, int BMW, bool GATEUP>
+int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
+        const float* w_scale, const int32_t* offsets, int groups, int N, int K,
+        float* out, cudaStream_t stream, bool pdl) {
+  using C = Cfg<BN, BMW, GATEUP>;
+  CUtensorMap tm_w, tm_a;
+  const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
+  if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;
+  if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
+  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return -3;
+  const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / BMW);
+  const int grid = (int)std::min<int64_t>(upper, sm_count());
+  if (grid <= 0) return 0;
+  const cudaError_t e = launch_kernel(
+      pdl, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, kern, tm_w, tm_a,
+      a_scale, w_scale, offsets, groups, N, K, out, device_error_word());
+  return e == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+namespace {
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -488,8 +471,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major [rows, K] uint8 matrix, box = 128 bytes of K x box_rows rows,
-// 128-byte swizzle; rows past the end read as zero.
+}  // namespace
+
+namespace gemm {
+
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
                int box_rows) {
   auto fn = encode_fn();
@@ -516,29 +501,15 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int BN, int BMW, bool GATEUP>
-int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
-        const float* w_scale, const int32_t* offsets, int groups, int N, int K,
-        float* out, cudaStream_t stream, bool pdl) {
-  using C = Cfg<BN, BMW, GATEUP>;
-  CUtensorMap tm_w, tm_a;
-  const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
-  if (!make_tmap(&tm_w, W, w_rows, K, BMW)) return -3;
-  if (!make_tmap(&tm_a, A, a_rows, K, BN)) return -3;
-  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess)
-    return -3;
-  const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / BMW);
-  const int grid = (int)std::min<int64_t>(upper, sm_count());
-  if (grid <= 0) return 0;
-  const cudaError_t e = launch_kernel(
-      pdl, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, kern, tm_w, tm_a,
-      a_scale, w_scale, offsets, groups, N, K, out, device_error_word());
-  return e == cudaSuccess ? 0 : -3;
+bool cta_pair_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("MOE_GEMM_CTA_PAIR");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
 }
 
-}  // namespace
+}  // namespace gemm
 
 int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         int64_t a_rows, const uint8_t* W, const float* w_scale,
@@ -547,6 +518,13 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
+  // Wide token tiles can run one M = 256 MMA over a pair of SMs (each loads
+  // half the token tile). Measured slower than the single-CTA kernel on the
+  // prefill shapes so far, so it is opt-in: MOE_GEMM_CTA_PAIR=1.
+  if (avg > 64 && cta_pair_enabled() && grouped_gemm_pair_supported(kind, N))
+    return launch_grouped_gemm_pair(kind, A, a_scale, a_rows, W, w_scale, offsets,
+                                    groups, N, K, out, avg <= 128 ? 128 : 256,
+                                    stream, pdl);
   if (kind == 0) {
     if (avg <= 16) return run<16, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
     if (avg <= 32) return run<32, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);

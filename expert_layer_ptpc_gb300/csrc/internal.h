@@ -78,6 +78,15 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         float* out, int rows_hint, cudaStream_t stream,
                         bool pdl);
 
+// The CTA-pair (cta_group::2) grouped GEMM for wide token tiles (bn 128 or
+// 256); needs N divisible by 128 (gate/up) or 256 (down). Returns a status.
+bool grouped_gemm_pair_supported(int kind, int N);
+int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
+                             int64_t a_rows, const uint8_t* W,
+                             const float* w_scale, const int32_t* offsets,
+                             int groups, int N, int K, float* out, int bn,
+                             cudaStream_t stream, bool pdl);
+
 cudaError_t launch_combine(const float* y, const int32_t* f2s,
                            const float* topk_w, int T, int k, int D,
                            const float* y_shared, const float* shared_gate,

@@ -206,6 +206,7 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
     (5, [300, 0, 257, 511, 2], 384, 384, 0),         # BN 128 / 256, tails
     (2, [1000, 24], 128, 4096, 0),                   # long K
     (2, [600, 301], 256, 512, 0),                    # BN 256 (wide tiles)
+    (4, [130, 0, 300, 77], 512, 256, 0),             # CTA pairs, BN 128
     (6, [5, 9, 0, 300, 2, 3], 256, 256, 16),         # hint forces BN 16
 ])
 def test_grouped_gemm(gateup, G, counts, N, K, hint):
@@ -267,3 +268,20 @@ def test_combine(T, k, D, shared):
     # fp32 sum of k+1 products, then one bf16 rounding (half a bf16 ulp)
     bound = (k + 2) * U32 * absref + 2.0 ** -8 * np.abs(ref) * (1 + 1e-6)
     assert np.all(np.abs(got - ref) <= bound + 1e-30)
+
+
+def test_grouped_gemm_cta_pair_variant():
+    """The CTA-pair (cta_group::2) kernel, opt-in through MOE_GEMM_CTA_PAIR=1,
+    on the wide-tile cases, in a child process that enables it."""
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, MOE_GEMM_CTA_PAIR="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m",
+           "gpu", os.path.join(root, "tests", "test_gpu_ops.py"), "-k",
+           "test_grouped_gemm and (counts2 or counts3 or counts4 or counts5 or counts6)"]
+    r = subprocess.run(cmd, env=env, cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
