@@ -88,6 +88,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
                int box_rows);
 
+// Row-major [rows, cols] fp32 matrix as a 2D TMA tensor map for stores of
+// box_rows x box_cols boxes (no swizzle).
+bool make_tmap_f32(CUtensorMap* map, void* base, int64_t rows, int cols,
+                   int box_rows, int box_cols);
+
 // Streaming multiprocessors of the current device (cached).
 int sm_count();
 

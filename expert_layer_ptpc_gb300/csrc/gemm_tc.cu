@@ -70,8 +70,13 @@ struct Cfg {
   static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols);
   static constexpr int kNumBars = 2 * kStages + 7;
   static constexpr int kXBytes = (GATEUP && kPacked) ? 64 * 16 * 4 : 0;
-  static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes +
+  // wide tiles stage each epilogue warp's 32 channels x 32 tokens of fp32
+  // output in shared memory and write it with one TMA store
+  static constexpr bool kStagedOut = !kPacked && BN >= 64;
+  static constexpr int kOutBytes = kStagedOut ? 4 * 32 * 32 * 4 : 0;
+  static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
                                     kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(BMW == 64 || BMW == 128, "tile width");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kStages >= 2, "pipeline depth");
@@ -80,7 +85,8 @@ struct Cfg {
 template <int BN, int BMW, bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w,
-    const __grid_constant__ CUtensorMap tm_a, const float* __restrict__ a_scale,
+    const __grid_constant__ CUtensorMap tm_a,
+    const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
     unsigned* __restrict__ err) {
@@ -89,8 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
+  float* outstage = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kXBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
-                                               C::kXBytes);
+                                               C::kXBytes + C::kOutBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
@@ -324,6 +331,30 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const int m = q * 32 + lane;          // accumulator row (lane) of this thread
     int it = 0;
     uint32_t xc = 0;                      // gate/up exchanges so far (packed)
+    // Output of 32 tokens (v[j] = token n0 + j) for this warp's 32 channels
+    // ch0 + lane. A full 32-token box inside the expert goes through shared
+    // memory and one TMA store; a partial box at the expert's end is stored
+    // directly, so rows of the next expert are never written.
+    float* obuf = outstage + (warp - kEpiWarp0) * 32 * 32;   // [token][channel]
+    auto emit = [&](const TileInfo& ti, int n0, int nvalid, int ch0,
+                    const float (&v)[32]) {
+      if (n0 + 32 <= nvalid) {
+        if (lane == 0) bulk_wait_read_all();   // the previous box has left obuf
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) obuf[j * 32 + lane] = v[j];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_out, ch0, ti.row0 + n0, smem_u32(obuf));
+          bulk_commit();
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n0 + j < nvalid) out[(int64_t)(ti.row0 + n0 + j) * N + ch0 + lane] = v[j];
+      }
+    };
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++it) {
       const int ab = it % C::kAccBufs;
@@ -377,6 +408,42 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             }
           }
         }
+      } else if (GATEUP && C::kStagedOut) {
+        const int ch0 = ti.ctile * kBM + q * 32;
+        const float swg = w_scale[(int64_t)ti.group * 2 * N + ch0 + lane];
+        const float swu = w_scale[(int64_t)ti.group * 2 * N + N + ch0 + lane];
+        for (int n0 = 0; n0 < nvalid; n0 += 32) {
+          float ag[32], au[32], v[32];
+          tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&ag[0]));
+          tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&ag[16]));
+          tmem_ld_x16(taddr + BN + n0, *reinterpret_cast<float(*)[16]>(&au[0]));
+          tmem_ld_x16(taddr + BN + n0 + 16, *reinterpret_cast<float(*)[16]>(&au[16]));
+          tmem_ld_wait();
+          // one coalesced load of the 32 token scales, broadcast by shuffle
+          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float sx = __shfl_sync(0xffffffffu, sx_l, j);
+            const float g = ag[j] * sx * swg;
+            const float u = au[j] * sx * swu;
+            v[j] = g / (1.0f + expf(-g)) * u;
+          }
+          emit(ti, n0, nvalid, ch0, v);
+        }
+      } else if (C::kStagedOut) {   // down projection, wide tiles
+        const int ch0 = ti.ctile * BMW + q * 32;
+        const float sw = w_scale[(int64_t)ti.group * N + ch0 + lane];
+        for (int n0 = 0; n0 < nvalid; n0 += 32) {
+          float acc[32], v[32];
+          tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
+          tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
+          tmem_ld_wait();
+          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = acc[j] * __shfl_sync(0xffffffffu, sx_l, j) * sw;
+          emit(ti, n0, nvalid, ch0, v);
+        }
       } else if (GATEUP) {
         const int ch = ti.ctile * kBM + m;
         const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
@@ -417,6 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(ab));
     }
+    // this warp's output stores are complete before the kernel ends
+    if (C::kStagedOut && lane == 0) bulk_wait_all();
   }
 
   // ---------------- tear-down ----------------
@@ -437,6 +506,8 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
+  CUtensorMap tm_out{};
+  if (C::kStagedOut && !make_tmap_f32(&tm_out, out, a_rows, N, 32, 32)) return -3;
   auto kern = grouped_gemm_kernel<BN, BMW, GATEUP>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
@@ -446,7 +517,7 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   if (grid <= 0) return 0;
   const cudaError_t e = launch_kernel(
       pdl, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, kern, tm_w, tm_a,
-      a_scale, w_scale, offsets, groups, N, K, out, device_error_word());
+      tm_out, a_scale, w_scale, offsets, groups, N, K, out, device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
 
@@ -486,6 +557,20 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_f32(CUtensorMap* map, void* base, int64_t rows, int cols,
+                   int box_rows, int box_cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
