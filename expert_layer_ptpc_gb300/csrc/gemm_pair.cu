@@ -189,10 +189,11 @@ struct PairCfg {
   static constexpr int kXBytes = GATEUP ? 64 * kChunk * 4 : 0;
   static constexpr int kTileCh = GATEUP ? 128 : 256;     // channels per tile
   static constexpr int kNumBars = 2 * kStages + 7;
-  // Reserved after the stages: one more token half-tile, so that any operand
-  // read starting at a stage stays inside this CTA's allocation.
-  static constexpr int kPadBytes = kBTile;
-  static constexpr int kSmemBytes = 1024 + kStages * kStage + kPadBytes + kXBytes +
+  // output staging for TMA stores: per epilogue warp a box of 32 channels x
+  // 32 tokens (down) or x 16 tokens (gate/up, after the SwiGLU exchange)
+  static constexpr int kOutRows = GATEUP ? 16 : 32;
+  static constexpr int kOutBytes = 4 * kOutRows * 32 * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
                                     kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
@@ -202,7 +203,8 @@ struct PairCfg {
 template <int BN, bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap tm_w,
-    const __grid_constant__ CUtensorMap tm_a, const float* __restrict__ a_scale,
+    const __grid_constant__ CUtensorMap tm_a,
+    const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
     unsigned* __restrict__ err) {
@@ -210,9 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kPadBytes);
+  float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
+  float* outstage = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kXBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
-                                               C::kPadBytes + C::kXBytes);
+                                               C::kXBytes + C::kOutBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
@@ -439,6 +442,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     int it = 0;
     uint32_t xc = 0;
     bool ok = true;
+    // Output of C::kOutRows tokens from token r0 on, for this warp's 32
+    // channels ch0 + lane (v[j] = token r0 + j). A box inside the expert goes
+    // through shared memory and one TMA store; a box crossing the expert's end
+    // is stored directly, so rows of the next expert are never written.
+    float* obuf = outstage + (warp - kEpiWarp0) * C::kOutRows * 32;
+    auto emit = [&](int r0, int row_end, int ch0, const float* v) {
+      if (r0 + C::kOutRows <= row_end) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < C::kOutRows; ++j) obuf[j * 32 + lane] = v[j];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_out, ch0, r0, smem_u32(obuf));
+          bulk_commit();
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < C::kOutRows; ++j)
+          if (r0 + j < row_end) out[(int64_t)(r0 + j) * N + ch0 + lane] = v[j];
+      }
+    };
     for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step, ++it) {
       const int ab = it % C::kAccBufs;
       const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
@@ -495,16 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(xempty_bar);
+          float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float sx = __shfl_sync(0xffffffffu, sx_l, c0 + j);
-            if (n0 + c0 + j < nvalid) {
-              const float gg = g[j] * sx * swg;
-              const float uu = u[j] * sx * swu;
-              out[(int64_t)(ti.row0 + n0 + c0 + j) * N + ch] =
-                  gg / (1.0f + expf(-gg)) * uu;
-            }
+            const float gg = g[j] * sx * swg;
+            const float uu = u[j] * sx * swu;
+            hv[j] = gg / (1.0f + expf(-gg)) * uu;
           }
+          emit(ti.row0 + n0 + c0, ti.row0 + nvalid, ch - lane, hv);
         }
       } else {
         const int ch = ti.ctile * 256 + (int)rank * 128 + m;
@@ -515,12 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
           tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
           tmem_ld_wait();
           const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float sx = __shfl_sync(0xffffffffu, sx_l, j);
-            if (n0 + j < nvalid)
-              out[(int64_t)(ti.row0 + n0 + j) * N + ch] = acc[j] * sx * sw;
-          }
+          for (int j = 0; j < 32; ++j) v[j] = acc[j] * __shfl_sync(0xffffffffu, sx_l, j) * sw;
+          emit(ti.row0 + n0, ti.row0 + nvalid, ch - lane, v);
         }
       }
       tc_fence_before_sync();
@@ -530,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
         else mbar_arrive_cluster(map_to_rank(acce_bar(ab), 0));
       }
     }
+    if (lane == 0) bulk_wait_all();   // this warp's output stores are complete
   }
 
   // ---------------- tear-down ----------------
@@ -551,6 +575,8 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
+  CUtensorMap tm_out;
+  if (!make_tmap_f32(&tm_out, out, a_rows, N, C::kOutRows, 32)) return -3;
   auto kern = grouped_gemm_pair_kernel<BN, GATEUP>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
@@ -587,8 +613,8 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, a_scale, w_scale, offsets, groups,
-                         N, K, out, device_error_word());
+      cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
+                         groups, N, K, out, device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
 
