@@ -22,6 +22,7 @@ enum : unsigned {
   kErrTimeoutEpilogue = 1u << 2,
   kErrTimeoutDrain = 1u << 3,
   kErrBadIndex = 1u << 4,
+  kErrTimeoutSched = 1u << 5,
 };
 
 // Wall-clock limit of one wait (ns). Every wait in these kernels normally

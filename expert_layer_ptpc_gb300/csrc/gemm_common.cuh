@@ -17,11 +17,12 @@ constexpr int kMmaWarp = 0;        // TMEM allocation and MMA issue
 constexpr int kEpiWarp0 = 1;       // warps 1-4: epilogue (one TMEM lane quarter each)
 constexpr int kProdWarp0 = 5;      // warps 5-10: producers, one box of a stage each
 constexpr int kMaxBoxes = 6;
-constexpr int kThreads = 32 * (kProdWarp0 + kMaxBoxes);
+constexpr int kSchedWarp = kProdWarp0 + kMaxBoxes;   // warp 11: tile scheduler
+constexpr int kThreads = 32 * (kSchedWarp + 1);
 
 // Index of the box a warp loads (-1 for warps that are not producers).
 __device__ __forceinline__ int producer_box(int warp) {
-  return warp >= kProdWarp0 ? warp - kProdWarp0 : -1;
+  return warp >= kProdWarp0 && warp < kSchedWarp ? warp - kProdWarp0 : -1;
 }
 constexpr int kBK = 128;        // K bytes per stage = one 128-byte swizzle row
 constexpr int kStageBudget = 200 * 1024;
@@ -83,6 +84,235 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
 }
 
 
+// ---------------------------------------------------------------------------
+// Cluster helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier that other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                     volatile int* abort_flag,
+                                                     unsigned* err, unsigned code) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((spin & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, code);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dynamic tile scheduler (cluster launch control)
+// ---------------------------------------------------------------------------
+// The grid has one CTA (or CTA pair) per possible tile, more than can be
+// resident. A CTA that runs takes its own tile, then cancels the launch of a
+// CTA that has not started yet and takes that CTA's tile instead
+// (clusterlaunchcontrol.try_cancel), until no launch is left to cancel. Tiles
+// are thus handed out one at a time, in launch order (neighbouring tiles,
+// which share weight and token tiles in L2, still run side by side), to
+// whichever SM frees up first: ragged experts, narrowed tail tiles and
+// unequal tile costs no longer leave some SMs with more work than others.
+//
+// One scheduler thread per CTA publishes the sequence to the CTA's roles
+// through a small ring in shared memory; -1 ends it. The next tile is
+// requested only when the first producer has taken the last one, so a CTA
+// holds at most one tile in reserve beyond those in its pipeline. In a CTA
+// pair the leader requests, the response is multicast to both CTAs, and both
+// schedulers publish the same sequence.
+constexpr int kRing = 4;
+
+struct Sched {
+  alignas(16) uint4 resp[2];   // cancel responses (double-buffered)
+  uint64_t full[kRing];        // tile[i] written
+  uint64_t empty[kRing];       // every consumer has read tile[i]
+  uint64_t taken;              // the first producer took a tile
+  uint64_t resp_bar[2];        // a response landed (16 bytes expected)
+  uint64_t resp_free[2];       // pair: the peer has read a response
+  int tile[kRing];
+};
+
+// `consumers`: arrivals that free a ring slot (one per consuming thread or
+// warp of this CTA). Called by one thread before the CTA's first barrier.
+__device__ __forceinline__ void sched_init(Sched& sc, int consumers) {
+  for (int i = 0; i < kRing; ++i) {
+    mbar_init(smem_u32(&sc.full[i]), 1);
+    mbar_init(smem_u32(&sc.empty[i]), consumers);
+  }
+  mbar_init(smem_u32(&sc.taken), 1);
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(smem_u32(&sc.resp_bar[b]), 1);
+    mbar_init(smem_u32(&sc.resp_free[b]), 1);
+  }
+}
+
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar, bool multicast) {
+  if (multicast)
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes."
+        "multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes."
+        "b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Whether the request cancelled a launch, and the x index of the first CTA of
+// the cancelled cluster.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& x) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 v;\n\t"
+      "ld.shared.b128 v, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, v;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, v;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  return ok != 0;
+}
+
+// The scheduler thread. `first`: this CTA's (pair's) own tile; `cta_per_tile`:
+// 1, or 2 for CTA pairs; `rank`: rank in the pair (0 requests).
+__device__ inline void sched_run(Sched& sc, int first, int total, int cta_per_tile,
+                                 uint32_t rank, volatile int* abort_flag,
+                                 unsigned* err) {
+  int slot = 0;
+  uint32_t ph = 0;
+  uint32_t resp_ph[2] = {0u, 0u}, free_ph[2] = {0u, 0u};
+  int uses[2] = {0, 0};
+  uint32_t taken_ph = 0;
+  auto publish = [&](int t) -> bool {
+    if (!mbar_wait_bounded(smem_u32(&sc.empty[slot]), ph ^ 1u, abort_flag, err,
+                           kErrTimeoutSched))
+      return false;
+    *reinterpret_cast<volatile int*>(&sc.tile[slot]) = t;
+    mbar_arrive(smem_u32(&sc.full[slot]));
+    if (++slot == kRing) {
+      slot = 0;
+      ph ^= 1u;
+    }
+    return true;
+  };
+  bool ok = true, pending_take = false;
+  if (first < total) {
+    ok = publish(first);
+    pending_take = true;
+  }
+  int b = 0;
+  while (ok) {
+    if (rank == 0 && pending_take) {   // request just in time
+      if (!mbar_wait_bounded(smem_u32(&sc.taken), taken_ph, abort_flag, err,
+                             kErrTimeoutSched))
+        break;
+      taken_ph ^= 1u;
+    }
+    pending_take = false;
+    mbar_arrive_expect_tx(smem_u32(&sc.resp_bar[b]), 16);
+    if (rank == 0) {
+      if (cta_per_tile > 1 && uses[b] > 0) {   // the peer read this buffer
+        if (!wait_cluster_bounded(smem_u32(&sc.resp_free[b]), free_ph[b], abort_flag,
+                                  err, kErrTimeoutSched))
+          break;
+        free_ph[b] ^= 1u;
+      }
+      fence_proxy_async_smem();
+      clc_try_cancel(smem_u32(&sc.resp[b]), smem_u32(&sc.resp_bar[b]), cta_per_tile > 1);
+    }
+    ++uses[b];
+    if (!mbar_wait_bounded(smem_u32(&sc.resp_bar[b]), resp_ph[b], abort_flag, err,
+                           kErrTimeoutSched))
+      break;
+    resp_ph[b] ^= 1u;
+    uint32_t x = 0;
+    const bool got = clc_query(smem_u32(&sc.resp[b]), x);
+    if (cta_per_tile > 1 && rank != 0)
+      mbar_arrive_cluster(map_to_rank(smem_u32(&sc.resp_free[b]), 0));
+    b ^= 1;
+    if (!got) break;   // nothing left to cancel: never request again
+    const int t = (int)(x / (uint32_t)cta_per_tile);
+    if (t < total) {
+      ok = publish(t);
+      pending_take = true;
+    }
+  }
+  publish(-1);
+}
+
+// A consumer's position in the ring.
+struct TileCursor {
+  int slot = 0;
+  uint32_t phase = 0;
+};
+
+// Next tile for a role run by one thread (-1: no more, or a wait ran out).
+// `take` marks the first producer, whose taking releases the next request.
+__device__ __forceinline__ int next_tile_thread(Sched& sc, TileCursor& c, bool take,
+                                                volatile int* abort_flag, unsigned* err,
+                                                unsigned code) {
+  if (!mbar_wait_bounded(smem_u32(&sc.full[c.slot]), c.phase, abort_flag, err, code))
+    return -1;
+  const int t = *reinterpret_cast<volatile int*>(&sc.tile[c.slot]);
+  mbar_arrive(smem_u32(&sc.empty[c.slot]));
+  if (take && t >= 0) mbar_arrive(smem_u32(&sc.taken));
+  if (++c.slot == kRing) {
+    c.slot = 0;
+    c.phase ^= 1u;
+  }
+  return t;
+}
+
+// Next tile for a role run by a whole warp (the same answer in every lane).
+__device__ __forceinline__ int next_tile_warp(Sched& sc, TileCursor& c,
+                                              volatile int* abort_flag, unsigned* err,
+                                              unsigned code) {
+  if (!warp_wait(smem_u32(&sc.full[c.slot]), c.phase, abort_flag, err, code)) return -1;
+  const int t = *reinterpret_cast<volatile int*>(&sc.tile[c.slot]);
+  __syncwarp();
+  if (lane_id() == 0) mbar_arrive(smem_u32(&sc.empty[c.slot]));
+  if (++c.slot == kRing) {
+    c.slot = 0;
+    c.phase ^= 1u;
+  }
+  return t;
+}
+
 // Row-major [rows, K] uint8 matrix as a 2D TMA tensor map: box = 128 bytes
 // of K x box_rows rows, 128-byte swizzle; rows past the end read as zero.
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
@@ -96,8 +326,9 @@ bool make_tmap_f32(CUtensorMap* map, void* base, int64_t rows, int cols,
 // Streaming multiprocessors of the current device (cached).
 int sm_count();
 
-// Whether wide token tiles use the CTA-pair kernel (MOE_GEMM_CTA_PAIR=1).
-bool cta_pair_enabled();
+// MOE_GEMM_CTA_PAIR: 1 forces the CTA-pair kernel for wide token tiles, 0
+// disables it, unset (-1) leaves the choice to the dispatch rule.
+int cta_pair_mode();
 
 }  // namespace gemm
 }  // namespace moe

@@ -35,42 +35,10 @@ namespace {
 
 using namespace gemm;
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 __device__ __forceinline__ uint32_t cluster_index() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
   return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// Address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                   cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 __device__ __forceinline__ void cluster_sync() {
   __syncwarp();
@@ -128,25 +96,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void* 
       : "memory");
 }
 
-// Bounded waits on barriers that other CTAs of the cluster arrive on.
-__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity,
-                                                     volatile int* abort_flag,
-                                                     unsigned* err, unsigned code) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (uint32_t spin = 0;; ++spin) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((spin & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicOr(err, code);
-        return false;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag,
                                                   unsigned* err, unsigned code) {
@@ -200,6 +149,17 @@ struct PairCfg {
   static_assert(kStages >= 3, "pipeline depth");
 };
 
+// MMA width (token columns) of a tile with `nvalid` token rows: BN, halved
+// while half of it still covers them, down to 64 so that each CTA's share is
+// at least one 32-row token box. An expert's last, partial tile then neither
+// loads nor multiplies the rows past its end.
+template <int BN>
+__device__ __forceinline__ int pair_width(int nvalid) {
+  int n = BN;
+  while (n > 64 && n / 2 >= nvalid) n /= 2;
+  return n;
+}
+
 template <int BN, bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap tm_w,
@@ -220,11 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
   __shared__ int warp_tot[kThreads / 32 + 1];
+  __shared__ Sched sched;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_rank();        // 0: the leader issues the MMAs
-  const int first_tile = (int)cluster_index();
-  const int tile_step = (int)cluster_count();
+  const int first_tile = (int)cluster_index();  // handed out first
   const int n_ctiles = N / C::kTileCh;
   const int kblocks = K / kBK;
 
@@ -253,6 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     mbar_init(drain_bar, 1);
     mbar_init(xfull_bar, 4);       // one per epilogue warp
     mbar_init(xempty_bar, 4);
+    // ring consumers: each producer, each epilogue warp, the leader's MMA issuer
+    sched_init(sched, C::kBoxes + 4 + (rank == 0 ? 1 : 0));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -306,7 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   };
 
   const int box = producer_box(warp);
-  if (box >= 0) {
+  if (warp == kSchedWarp) {
+    // ---------------- tile scheduler (both CTAs; the leader requests) ----------------
+    if (lane == 0)
+      sched_run(sched, first_tile, total_tiles, 2, rank, abort_flag, err);
+  } else if (box >= 0) {
     // ---------------- TMA producers (both CTAs): box `box` of every stage ----------------
     const bool weight_box = box < 2;
     if (lane == 0 && box < C::kBoxes) {
@@ -322,12 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
                pol);
         else {               // 32 rows of this CTA's half of the token tile
           const int t = box - 2;
-          load(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
-               ti.row0 + (int)rank * C::kHalfB + t * C::kTBoxRows, s, pol);
+          const int half = pair_width<BN>(ti.row_end - ti.row0) / 2;
+          if (t * C::kTBoxRows < half)
+            load(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
+                 ti.row0 + (int)rank * half + t * C::kTBoxRows, s, pol);
         }
       };
-      auto expect = [&](int s) {
-        if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+      // a token box past the tile's MMA width is not loaded by either CTA
+      auto expect = [&](int s, const TileInfo& ti) {
+        if (rank != 0) return;
+        const bool used = weight_box || (box - 2) * C::kTBoxRows <
+                                            pair_width<BN>(ti.row_end - ti.row0) / 2;
+        mbar_arrive_expect_tx(full_bar(s), used ? 2 * bytes : 0u);
       };
       int last_phase[C::kStages];
 #pragma unroll
@@ -342,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
         t0 = decode_tile(first_tile, prefix, groups, offsets, BN);
         npre = kblocks < C::kStages ? kblocks : C::kStages;
         for (int kb = 0; kb < npre; ++kb) {
-          expect(kb);
+          expect(kb, t0);
           issue(kb, kb, t0);
 #pragma unroll
           for (int i = 0; i < C::kStages; ++i)
@@ -353,17 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       }
       pdl_wait();
       pdl_launch_dependents();
-      for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step) {
-        const TileInfo ti = (tile == first_tile && npre > 0)
-                                ? t0
-                                : decode_tile(tile, prefix, groups, offsets, BN);
-        for (int kb = tile == first_tile ? npre : 0; kb < kblocks; ++kb) {
+      TileCursor cur;
+      for (bool first = true; ok; first = false) {
+        const int tile = next_tile_thread(sched, cur, box == 0 && rank == 0, abort_flag,
+                                          err, kErrTimeoutProducer);
+        if (tile < 0) break;
+        const bool pre = first && npre > 0 && tile == first_tile;
+        const TileInfo ti = pre ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
+        for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!wait_cluster_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                     kErrTimeoutProducer)) {
             ok = false;
             break;
           }
-          expect(s);
+          expect(s, ti);
           issue(s, kb, ti);
 #pragma unroll
           for (int i = 0; i < C::kStages; ++i)
@@ -398,18 +373,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     pdl_launch_dependents();
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (leader) ----------------
-      constexpr uint32_t idesc = idesc_e4m3_f32(256, BN);
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step, ++it) {
+      TileCursor cur;
+      for (; ok; ++it) {
+        const int tile = next_tile_thread(sched, cur, false, abort_flag, err, kErrTimeoutMma);
+        if (tile < 0) break;
         const int ab = it % C::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
         if (!wait_cluster_bounded(acce_bar(ab), acc_ph ^ 1, abort_flag, err,
                                   kErrTimeoutMma)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+        const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
+        const uint32_t idesc =
+            idesc_e4m3_f32(256, pair_width<BN>(ti.row_end - ti.row0));
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_cluster_bounded(full_bar(s), ph, abort_flag, err, kErrTimeoutMma)) {
             ok = false;
@@ -465,7 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
           if (r0 + j < row_end) out[(int64_t)(r0 + j) * N + ch0 + lane] = v[j];
       }
     };
-    for (int tile = first_tile; ok && tile < total_tiles; tile += tile_step, ++it) {
+    TileCursor cur;
+    for (; ok; ++it) {
+      const int tile = next_tile_warp(sched, cur, abort_flag, err, kErrTimeoutEpilogue);
+      if (tile < 0) break;
       const int ab = it % C::kAccBufs;
       const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
       if (!warp_wait_cluster(accf_bar(ab), acc_ph, abort_flag, err,
@@ -527,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
             const float sx = __shfl_sync(0xffffffffu, sx_l, c0 + j);
             const float gg = g[j] * sx * swg;
             const float uu = u[j] * sx * swu;
-            hv[j] = gg / (1.0f + expf(-gg)) * uu;
+            hv[j] = __fdividef(gg * uu, 1.0f + __expf(-gg));
           }
           emit(ti.row0 + n0 + c0, ti.row0 + nvalid, ch - lane, hv);
         }
@@ -583,11 +566,10 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
     return -3;
   const int64_t upper =
       ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / C::kTileCh);
-  // Persistent clusters: launch no more than can be resident at once (the
-  // SM pairs a cluster needs are fewer than half the SMs on some parts).
-  static int resident[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
+  // one cluster per possible tile; the ones that run first take the rest
+  // over (cluster launch control, see the scheduler)
+  if (upper <= 0) return 0;
+  if (2 * upper > INT32_MAX) return -2;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -596,21 +578,11 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * upper));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (resident[dev] == 0) {
-    int n = 0;
-    cfg.gridDim = dim3(2 * (sm_count() / 2));
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
-      n = sm_count() / 2;
-    resident[dev] = n;
-  }
-  const int clusters = (int)std::min<int64_t>(upper, resident[dev]);
-  if (clusters <= 0) return 0;
-  cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
   __shared__ int warp_tot[kThreads / 32 + 1];
+  __shared__ Sched sched;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_ctiles = N / BMW;
@@ -134,6 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     mbar_init(drain_bar, 1);
     mbar_init(xfull_bar, 64);
     mbar_init(xempty_bar, 64);
+    // ring consumers: each producer, the MMA issuer, each epilogue warp
+    sched_init(sched, C::kBoxes + 1 + 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -179,7 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   };
 
   const int box = producer_box(warp);
-  if (box >= 0) {
+  if (warp == kSchedWarp) {
+    // ---------------- tile scheduler ----------------
+    // (touches nothing the previous kernel writes)
+    if (lane == 0) sched_run(sched, blockIdx.x, total_tiles, 1, 0, abort_flag, err);
+  } else if (box >= 0) {
     // ---------------- TMA producers: box `box` of every stage ----------------
     const bool weight_box = box < C::kWBoxes;
     if (lane == 0 && box < C::kBoxes) {
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       // The weights and the tile map (offsets come from the permutation, two
       // launches back) do not depend on the previous kernel: the weight
       // producers fill the first stages before waiting for it.
-      const int first = blockIdx.x;
+      const int first = blockIdx.x;   // the scheduler hands this tile out first
       int npre = 0;
       TileInfo t0{};
       if (weight_box && first < total_tiles) {
@@ -239,11 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
       pdl_wait();
       pdl_launch_dependents();
-      for (int tile = first; ok && tile < total_tiles; tile += gridDim.x) {
-        const TileInfo ti = (tile == first && npre > 0)
-                                ? t0
-                                : decode_tile(tile, prefix, groups, offsets, BN);
-        for (int kb = tile == first ? npre : 0; kb < kblocks; ++kb) {
+      TileCursor cur;
+      for (bool first_tile = true; ok; first_tile = false) {
+        const int tile = next_tile_thread(sched, cur, box == 0, abort_flag, err,
+                                          kErrTimeoutProducer);
+        if (tile < 0) break;
+        const bool pre = first_tile && npre > 0 && tile == first;
+        const TileInfo ti = pre ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
+        for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                  kErrTimeoutProducer)) {
             ok = false;
@@ -278,13 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     pdl_wait();
     pdl_launch_dependents();
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles;
-           tile += gridDim.x, ++it) {
+      TileCursor cur;
+      for (; ok; ++it) {
+        const int tile = next_tile_thread(sched, cur, false, abort_flag, err,
+                                          kErrTimeoutMma);
+        if (tile < 0) break;
         const int ab = it % C::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
         if (!mbar_wait_bounded(acce_bar(ab), acc_ph ^ 1, abort_flag, err,
@@ -292,6 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + (uint32_t)(ab * C::kAccCols);
         const uint32_t d1 = d0 + BN;
+        // An expert's last token tile is usually partial: narrow the MMA to
+        // the smallest width (halving BN, not below 32) that covers its rows.
+        int n_mma = BN;
+        {
+          const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
+          const int nvalid = ti.row_end - ti.row0;
+          while (n_mma >= 64 && n_mma / 2 >= nvalid) n_mma /= 2;
+        }
+        const uint32_t idesc = idesc_e4m3_f32(kBM, n_mma);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(full_bar(s), ph, abort_flag, err,
                                  kErrTimeoutMma)) {
@@ -356,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
     };
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++it) {
+    TileCursor cur;
+    for (; ok; ++it) {
+      const int tile = next_tile_warp(sched, cur, abort_flag, err, kErrTimeoutEpilogue);
+      if (tile < 0) break;
       const int ab = it % C::kAccBufs;
       const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
       if (!warp_wait(accf_bar(ab), acc_ph, abort_flag, err, kErrTimeoutEpilogue))
@@ -403,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
                 const float sx = a_scale[row];
                 const float g = a[j] * sx * swg;
                 const float uu = u[j] * sx * swu;
-                out[(int64_t)row * N + ch] = g / (1.0f + expf(-g)) * uu;
+                out[(int64_t)row * N + ch] = __fdividef(g * uu, 1.0f + __expf(-g));
               }
             }
           }
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             const float sx = __shfl_sync(0xffffffffu, sx_l, j);
             const float g = ag[j] * sx * swg;
             const float u = au[j] * sx * swu;
-            v[j] = g / (1.0f + expf(-g)) * u;
+            v[j] = __fdividef(g * u, 1.0f + __expf(-g));
           }
           emit(ti, n0, nvalid, ch0, v);
         }
@@ -460,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
               const float sx = a_scale[row];
               const float g = ag[j] * sx * swg;
               const float u = au[j] * sx * swu;
-              out[(int64_t)row * N + ch] = g / (1.0f + expf(-g)) * u;
+              out[(int64_t)row * N + ch] = __fdividef(g * u, 1.0f + __expf(-g));
             }
           }
         }
@@ -512,12 +536,28 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
+  // one CTA per possible tile; the ones that run first take the rest over
+  // (cluster launch control, see the scheduler)
   const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / BMW);
-  const int grid = (int)std::min<int64_t>(upper, sm_count());
-  if (grid <= 0) return 0;
-  const cudaError_t e = launch_kernel(
-      pdl, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, kern, tm_w, tm_a,
-      tm_out, a_scale, w_scale, offsets, groups, N, K, out, device_error_word());
+  if (upper <= 0) return 0;
+  if (upper > INT32_MAX) return -2;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)upper);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
+                         groups, N, K, out, device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
 
@@ -586,12 +626,13 @@ int sm_count() {
   return cached[dev];
 }
 
-bool cta_pair_enabled() {
-  static const bool on = [] {
+int cta_pair_mode() {
+  static const int mode = [] {
     const char* v = std::getenv("MOE_GEMM_CTA_PAIR");
-    return v != nullptr && v[0] == '1';
+    if (v == nullptr || v[0] == '\0') return -1;
+    return v[0] == '1' ? 1 : v[0] == '0' ? 0 : -1;
   }();
-  return on;
+  return mode;
 }
 
 }  // namespace gemm
@@ -603,10 +644,17 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
-  // Wide token tiles can run one M = 256 MMA over a pair of SMs (each loads
-  // half the token tile). Measured slower than the single-CTA kernel on the
-  // prefill shapes so far, so it is opt-in: MOE_GEMM_CTA_PAIR=1.
-  if (avg > 64 && cta_pair_enabled() && grouped_gemm_pair_supported(kind, N))
+  // Wide token tiles of the gate/up projection run one M = 256 MMA over a
+  // pair of SMs (each loads half of the token tile, one N = 256 instruction
+  // per K step instead of two N = 128 ones). On GB300 that wins from about
+  // 256 rows per expert on; the down projection, bound by its fp32 output
+  // writes, stays on the single-CTA kernel. MOE_GEMM_CTA_PAIR=1 / =0 forces
+  // the pair kernel on (every shape with more than 64 rows per expert) / off.
+  const int pair_mode = cta_pair_mode();
+  const bool pair = pair_mode == 1   ? avg > 64
+                    : pair_mode == 0 ? false
+                                     : kind == 0 && avg >= 256;
+  if (pair && grouped_gemm_pair_supported(kind, N))
     return launch_grouped_gemm_pair(kind, A, a_scale, a_rows, W, w_scale, offsets,
                                     groups, N, K, out, avg <= 128 ? 128 : 256,
                                     stream, pdl);

@@ -190,8 +190,12 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
             dsilu = np.abs(sig * (1 + gg * (1 - sig)))
             out[r0:r1] = silu * uu
             # first-order propagation plus the fp32 evaluation of silu * u
+            # with the fast exponential and division: CUDA documents at most
+            # 2 + floor(1.173 |x|) ulp for __expf(x) and 2 ulp for
+            # __fdividef in this range, plus the scaling multiplies
+            ulps = 16 + 2 + np.floor(1.173 * np.abs(gg))
             bound[r0:r1] = dsilu * np.abs(uu) * eg + np.abs(silu) * eu + \
-                16 * U32 * np.abs(silu * uu) + 1e-30
+                ulps * U32 * np.abs(silu * uu) + 1e-30
         else:
             out[r0:r1] = full
             bound[r0:r1] = gemm_bound(absacc, K) + 1e-30
@@ -270,13 +274,17 @@ def test_combine(T, k, D, shared):
     assert np.all(np.abs(got - ref) <= bound + 1e-30)
 
 
-def test_grouped_gemm_cta_pair_variant():
-    """The CTA-pair (cta_group::2) kernel, opt-in through MOE_GEMM_CTA_PAIR=1,
-    on the wide-tile cases, in a child process that enables it."""
+@pytest.mark.parametrize("mode", ["1", "0"])
+def test_grouped_gemm_cta_pair_variant(mode):
+    """The wide-tile cases with the kernel choice forced, in a child process:
+    MOE_GEMM_CTA_PAIR=1 runs the CTA-pair (cta_group::2) kernel for every
+    shape with more than 64 rows per expert (the down projection included),
+    =0 the single-CTA kernel everywhere (the gate/up shapes that otherwise
+    take the pair)."""
     import os
     import subprocess
     import sys
-    env = dict(os.environ, MOE_GEMM_CTA_PAIR="1")
+    env = dict(os.environ, MOE_GEMM_CTA_PAIR=mode)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     cmd = [sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m",
            "gpu", os.path.join(root, "tests", "test_gpu_ops.py"), "-k",
