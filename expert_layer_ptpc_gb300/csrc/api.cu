@@ -361,7 +361,9 @@ int moe_device_status(moe_stream_t stream, unsigned* detail) {
       return MOE_ERR_CUDA;
   }
   if (detail) *detail = word;
-  return word != 0 ? MOE_ERR_TIMEOUT : MOE_OK;
+  if (word == 0) return MOE_OK;
+  // a tile map larger than the launch alone: group offsets past a_rows
+  return word == moe::kErrBadIndex ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
 }
 
 }  // extern "C"

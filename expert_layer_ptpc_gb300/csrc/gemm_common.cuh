@@ -230,6 +230,8 @@ __device__ inline void sched_run(Sched& sc, int first, int total, int cta_per_ti
     }
     return true;
   };
+  // offsets that need more tiles than the grid has CTAs (rows past a_rows)
+  if ((int64_t)total * cta_per_tile > (int64_t)gridDim.x) atomicOr(err, kErrBadIndex);
   bool ok = true, pending_take = false;
   if (first < total) {
     ok = publish(first);
@@ -311,6 +313,18 @@ __device__ __forceinline__ int next_tile_warp(Sched& sc, TileCursor& c,
     c.phase ^= 1u;
   }
   return t;
+}
+
+// Upper bound on the token tiles of `groups` expert slices that hold
+// `a_rows` rows in all, BN rows per tile. A non-empty slice of r rows has
+// floor((r - 1) / BN) + 1 tiles, and at most min(groups, a_rows) slices are
+// non-empty, so the total is at most floor((a_rows - ne) / BN) + ne with
+// ne = min(groups, a_rows). The grid has one CTA (pair) per possible tile,
+// and every surplus one costs a cancellation round trip, so the bound is
+// kept tight (exact when every slice holds at most BN rows).
+inline int64_t token_tiles_upper(int64_t a_rows, int groups, int bn) {
+  const int64_t ne = a_rows < groups ? a_rows : (int64_t)groups;
+  return (a_rows - ne) / bn + ne;
 }
 
 // Row-major [rows, K] uint8 matrix as a 2D TMA tensor map: box = 128 bytes

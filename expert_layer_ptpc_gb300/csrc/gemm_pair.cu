@@ -564,8 +564,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
-  const int64_t upper =
-      ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / C::kTileCh);
+  const int64_t upper = token_tiles_upper(a_rows, groups, BN) * (int64_t)(N / C::kTileCh);
   // one cluster per possible tile; the ones that run first take the rest
   // over (cluster launch control, see the scheduler)
   if (upper <= 0) return 0;

@@ -538,7 +538,7 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
     return -3;
   // one CTA per possible tile; the ones that run first take the rest over
   // (cluster launch control, see the scheduler)
-  const int64_t upper = ((a_rows + BN - 1) / BN + groups) * (int64_t)(N / BMW);
+  const int64_t upper = token_tiles_upper(a_rows, groups, BN) * (int64_t)(N / BMW);
   if (upper <= 0) return 0;
   if (upper > INT32_MAX) return -2;
   cudaLaunchAttribute attr[2];

@@ -265,9 +265,14 @@ MOE_API int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
 
 /*
  * moe_device_status - synchronise `stream`, then read and clear the device
- * error word that kernels set when a bounded wait expires. Returns MOE_OK,
- * MOE_ERR_TIMEOUT, or MOE_ERR_CUDA if the stream reported a CUDA error.
- * `detail` (nullable) receives the raw error bits.
+ * error word that kernels set when a bounded wait expires or a grouped GEMM
+ * finds group offsets that describe more rows than `a_rows`. Returns MOE_OK;
+ * MOE_ERR_INVALID_ARG when the offsets bit alone is set; MOE_ERR_TIMEOUT when
+ * a wait expired; MOE_ERR_CUDA if the stream reported a CUDA error.
+ * `detail` (nullable) receives the raw error bits:
+ *   1 TMA producer wait, 2 MMA issuer wait, 4 epilogue wait, 8 drain wait,
+ *   16 tile map larger than the launch (offsets past a_rows; those tiles are
+ *   not computed), 32 tile scheduler wait.
  */
 MOE_API int moe_device_status(moe_stream_t stream, unsigned* detail);
 
