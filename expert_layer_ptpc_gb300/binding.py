@@ -52,6 +52,10 @@ _SIGNATURES = {
     "moe_grouped_gemm": (_I, [_I, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _I,
                               _I, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_scale_max": (_I, [_P, _I, _I, _P, _P]),
+    "moe_grouped_gemm_down_f16": (_I, [_P, _P, _I64, _P, _P, _P, _P, _I, _I, _I,
+                                       _P, _P, _I, _P]),
+    "moe_combine_f16": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_forward_workspace_size": (_SZ, [ctypes.POINTER(moe_dims)]),
     "moe_forward": (_I, [ctypes.POINTER(moe_dims), _P, _P, _P, _P, _P, _P, _P,
                          _P, _P, _P, _P, _P, _SZ, _P]),
@@ -59,6 +63,7 @@ _SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P, _P, _SZ,
                                   ctypes.POINTER(ctypes.c_void_p), _I, _P]),
     "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "moe_debug_expire_wait": (_I, [_I, _P]),
 }
 
 MOE_FORWARD_EVENTS = 9
@@ -251,6 +256,59 @@ def moe_combine(y, flat_to_sorted, topk_w, y_shared=None, shared_gate=None,
     return out
 
 
+def moe_scale_max(scale, bound=None, stream=None):
+    """bound[g] = max_n scale[g, n] for a [G, N] fp32 tensor."""
+    _need(scale, torch.float32, "scale")
+    G, N = scale.shape
+    if bound is None:
+        bound = torch.empty(G, dtype=torch.float32, device=scale.device)
+    _check("moe_scale_max", load_library().moe_scale_max(
+        _ptr(scale), G, N, _ptr(bound), _stream(stream)))
+    return bound
+
+
+def moe_grouped_gemm_down_f16(A, a_scale, W, w_scale, w_bound, group_offsets,
+                              y16=None, row_scale=None, rows_hint=0, stream=None):
+    """Down projection W [G, N, K] with y = row_scale[:, None] * y16:
+    returns (y16 [rows, N] fp16, row_scale [rows] fp32)."""
+    _need(A, torch.uint8, "A")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(W, torch.uint8, "W")
+    _need(w_scale, torch.float32, "w_scale")
+    _need(w_bound, torch.float32, "w_bound")
+    _need(group_offsets, torch.int32, "group_offsets")
+    a_rows, K = A.shape
+    G, N = W.shape[0], W.shape[1]
+    if W.shape[2] != K or group_offsets.numel() != G + 1:
+        raise ValueError("shape mismatch")
+    if y16 is None:
+        y16 = torch.empty((a_rows, N), dtype=torch.float16, device=A.device)
+    if row_scale is None:
+        row_scale = torch.empty(a_rows, dtype=torch.float32, device=A.device)
+    _check("moe_grouped_gemm_down_f16", load_library().moe_grouped_gemm_down_f16(
+        _ptr(A), _ptr(a_scale), a_rows, _ptr(W), _ptr(w_scale), _ptr(w_bound),
+        _ptr(group_offsets), G, N, K, _ptr(y16), _ptr(row_scale), rows_hint,
+        _stream(stream)))
+    return y16, row_scale
+
+
+def moe_combine_f16(y16, row_scale, flat_to_sorted, topk_w, y16_shared=None,
+                    row_scale_shared=None, shared_gate=None, out=None, stream=None):
+    _need(y16, torch.float16, "y16")
+    _need(row_scale, torch.float32, "row_scale")
+    _need(flat_to_sorted, torch.int32, "flat_to_sorted")
+    _need(topk_w, torch.float32, "topk_w")
+    T, k = topk_w.shape
+    D = y16.shape[1]
+    if out is None:
+        out = torch.empty((T, D), dtype=torch.bfloat16, device=y16.device)
+    _check("moe_combine_f16", load_library().moe_combine_f16(
+        _ptr(y16), _ptr(row_scale), _ptr(flat_to_sorted), _ptr(topk_w), T, k, D,
+        _ptr(y16_shared), _ptr(row_scale_shared), _ptr(shared_gate), _ptr(out),
+        _stream(stream)))
+    return out
+
+
 def make_dims(T, D, E, k, I, shared, renormalize=True):
     return moe_dims(T, D, E, k, I, int(bool(shared)), int(bool(renormalize)))
 
@@ -295,6 +353,13 @@ def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,
         _check("moe_forward_profiled", lib.moe_forward_profiled(
             *args, handles, MOE_FORWARD_EVENTS, _stream(stream)))
     return out
+
+
+def moe_debug_expire_wait(limit_us, stream=None):
+    """Launch a bounded wait that nothing completes (expires after limit_us);
+    the next moe_device_status() reports it. Raises MoeError on bad input."""
+    _check("moe_debug_expire_wait",
+           load_library().moe_debug_expire_wait(int(limit_us), _stream(stream)))
 
 
 def moe_device_status(stream=None):

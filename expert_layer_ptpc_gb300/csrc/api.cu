@@ -27,6 +27,23 @@ unsigned* device_error_word() {
   return addr[dev];
 }
 
+// One thread waits, with a bounded wait like every wait of the layer's
+// kernels, on an mbarrier that nothing arrives on; the wait expires after
+// `limit_ns` and records the expiry in the error word.
+__global__ void expire_wait_kernel(unsigned long long limit_ns, unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_barrier_init();
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(smem_u32(&bar), 0)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrDebugWait);
+      return;
+    }
+  }
+}
+
 namespace {
 
 inline bool aligned16(const void* p) {
@@ -42,8 +59,16 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Byte offsets of the intermediates inside the moe_forward workspace.
 struct ForwardLayout {
   size_t ids, w, logits, counts, offsets, s2f, f2s, perm, xq, sx, gate, h, hq,
-      sh, y, total;
+      sh, y, row_scale, w_bound, total;
 };
+
+// The expert output y goes through HBM in fp32 while it is small, and in the
+// fp16 encoding (half the bytes, one factor per row) once its fp32 size
+// reaches 32 MiB; below that the extra bound kernel costs more than it saves.
+inline bool y_in_fp16(const moe_dims& d) {
+  const int64_t rows = (int64_t)d.T * d.k + (d.shared ? d.T : 0);
+  return rows * d.D * 4 >= (int64_t(32) << 20);
+}
 
 ForwardLayout forward_layout(const moe_dims& d) {
   const int64_t R = (int64_t)d.T * d.k;
@@ -70,7 +95,9 @@ ForwardLayout forward_layout(const moe_dims& d) {
   L.h = take(rows * d.I * 4);
   L.hq = take(rows * d.I);
   L.sh = take(rows * 4);
-  L.y = take(rows * d.D * 4);
+  L.y = take(rows * d.D * 4);   // fp32, or fp16 codes in the first half
+  L.row_scale = take(rows * 4);
+  L.w_bound = take(G * 4);
   L.total = off;
   return L;
 }
@@ -199,6 +226,52 @@ int moe_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                              stream, false);
 }
 
+int moe_scale_max(const float* scale, int groups, int N, float* bound,
+                  moe_stream_t stream) {
+  if (groups < 0 || N <= 0) return MOE_ERR_INVALID_ARG;
+  if (groups == 0) return MOE_OK;
+  if (!scale || !bound) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_scale_max(scale, groups, N, bound, stream, false));
+}
+
+int moe_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
+                              int64_t a_rows, const uint8_t* W, const float* w_scale,
+                              const float* w_bound, const int32_t* group_offsets,
+                              int groups, int N, int K, uint16_t* y16,
+                              float* row_scale, int rows_hint, moe_stream_t stream) {
+  if (a_rows < 0 || groups < 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  if (a_rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (a_rows == 0 || groups == 0) return MOE_OK;
+  if (!A || !a_scale || !W || !w_scale || !w_bound || !group_offsets || !y16 ||
+      !row_scale)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(y16)) return MOE_ERR_INVALID_ARG;
+  return launch_grouped_gemm_down_f16(A, a_scale, a_rows, W, w_scale, w_bound,
+                                      group_offsets, groups, N, K, y16, row_scale,
+                                      rows_hint, stream, false);
+}
+
+int moe_combine_f16(const uint16_t* y16, const float* row_scale,
+                    const int32_t* flat_to_sorted, const float* topk_w, int T, int k,
+                    int D, const uint16_t* y16_shared, const float* row_scale_shared,
+                    const float* shared_gate, uint16_t* out, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || D <= 0 || D % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  const bool s1 = y16_shared != nullptr, s2 = row_scale_shared != nullptr,
+             s3 = shared_gate != nullptr;
+  if (s1 != s2 || s1 != s3) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y16 || !row_scale || !flat_to_sorted || !topk_w || !out || !aligned16(y16) ||
+      !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (s1 && !aligned16(y16_shared)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_f16(y16, row_scale, flat_to_sorted, topk_w, T, k,
+                                        D, y16_shared, row_scale_shared, shared_gate,
+                                        out, stream, false));
+}
+
 int moe_combine(const float* y, const int32_t* flat_to_sorted,
                 const float* topk_w, int T, int k, int D, const float* y_shared,
                 const float* shared_gate, uint16_t* out, moe_stream_t stream) {
@@ -264,23 +337,34 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
   auto* hq = static_cast<uint8_t*>(at(L.hq));
   auto* sh = static_cast<float*>(at(L.sh));
   auto* y = static_cast<float*>(at(L.y));
+  auto* y16 = static_cast<uint16_t*>(at(L.y));
+  auto* row_scale = static_cast<float*>(at(L.row_scale));
+  auto* w_bound = static_cast<float*>(at(L.w_bound));
+  const bool f16 = y_in_fp16(d);
 
-  mark(0);
-  const float* logits = router_logits;
-  if (router_w != nullptr) {
-    auto* lg = static_cast<float*>(at(L.logits));
-    st = cuda_status(
-        launch_router_logits(x, router_w, d.T, d.E, d.D, lg, stream, false));
-    if (st != MOE_OK) return st;
-    logits = lg;
-  }
-  mark(1);
   // Kernels after the first overlap their launch with the previous kernel's
   // tail (programmatic dependent launch); each orders itself with pdl_wait().
   // Event marks between the steps serialise them instead.
   const bool pdl = ev == nullptr;
+  mark(0);
+  bool first = true;
+  if (f16) {   // the down weights' scale bound of every group (weights only)
+    st = cuda_status(launch_scale_max(s_d, G, d.D, w_bound, stream, false));
+    if (st != MOE_OK) return st;
+    first = false;
+  }
+  const float* logits = router_logits;
+  if (router_w != nullptr) {
+    auto* lg = static_cast<float*>(at(L.logits));
+    st = cuda_status(
+        launch_router_logits(x, router_w, d.T, d.E, d.D, lg, stream, pdl && !first));
+    if (st != MOE_OK) return st;
+    logits = lg;
+    first = false;
+  }
+  mark(1);
   st = cuda_status(launch_route(logits, d.T, d.E, d.k, d.renormalize ? 1 : 0, ids,
-                                tw, stream, pdl && router_w != nullptr));
+                                tw, stream, pdl && !first));
   if (st != MOE_OK) return st;
   mark(2);
   st = cuda_status(launch_permute(ids, R, d.E, counts, offsets, s2f, f2s,
@@ -306,13 +390,23 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
                                 /*release_early=*/true));
   if (st != MOE_OK) return st;
   mark(6);
-  st = launch_grouped_gemm(MOE_GEMM_DOWN, hq, sh, rows, w_d, s_d, offsets, G,
-                           d.D, d.I, y, hint, stream, pdl);
+  if (f16)
+    st = launch_grouped_gemm_down_f16(hq, sh, rows, w_d, s_d, w_bound, offsets, G,
+                                      d.D, d.I, y16, row_scale, hint, stream, pdl);
+  else
+    st = launch_grouped_gemm(MOE_GEMM_DOWN, hq, sh, rows, w_d, s_d, offsets, G,
+                             d.D, d.I, y, hint, stream, pdl);
   if (st != MOE_OK) return st;
   mark(7);
-  st = cuda_status(launch_combine(y, f2s, tw, d.T, d.k, d.D,
-                                  d.shared ? y + R * d.D : nullptr,
-                                  d.shared ? gate : nullptr, out, stream, pdl));
+  if (f16)
+    st = cuda_status(launch_combine_f16(
+        y16, row_scale, f2s, tw, d.T, d.k, d.D, d.shared ? y16 + R * d.D : nullptr,
+        d.shared ? row_scale + R : nullptr, d.shared ? gate : nullptr, out, stream,
+        pdl));
+  else
+    st = cuda_status(launch_combine(y, f2s, tw, d.T, d.k, d.D,
+                                    d.shared ? y + R * d.D : nullptr,
+                                    d.shared ? gate : nullptr, out, stream, pdl));
   if (st != MOE_OK) return st;
   mark(8);
   return MOE_OK;
@@ -347,6 +441,15 @@ int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
   return forward_impl(dims, x, router_logits, router_w, w_gu, s_gu, w_d, s_d,
                       shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
                       reinterpret_cast<cudaEvent_t const*>(events), stream);
+}
+
+int moe_debug_expire_wait(int limit_us, moe_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  unsigned* err = moe::device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  moe::expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      1000ull * (unsigned long long)limit_us, err);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int moe_device_status(moe_stream_t stream, unsigned* detail) {

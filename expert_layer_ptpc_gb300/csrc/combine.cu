@@ -7,6 +7,8 @@
 //   out[t] = bf16_rne( sum_{j<k} w[t, j] * y[flat_to_sorted[t k + j]]
 //                      + gate[t] * y_shared[t] )
 // summed in fp32, slot order j = 0..k-1, shared term last.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -65,7 +67,67 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   }
 }
 
+// The same reduction over the down projection's fp16 encoding: the row
+// factor folds into the slot weight, c_j = w[t, j] * row_scale[r_j], and
+// out = bf16_rne( sum_j c_j * y16[r_j] + (gate[t] * row_scale_shared[t]) *
+// y16_shared[t] ), in fp32 and slot order like combine_kernel.
+__global__ void __launch_bounds__(kThreads) combine_f16_kernel(
+    const __half* __restrict__ y16, const float* __restrict__ row_scale,
+    const int32_t* __restrict__ f2s, const float* __restrict__ topk_w, int k, int D,
+    const __half* __restrict__ y16_shared, const float* __restrict__ row_scale_shared,
+    const float* __restrict__ gate, __nv_bfloat16* __restrict__ out) {
+  const int t = blockIdx.x;
+  __shared__ int32_t rows[kMaxTopK];
+  __shared__ float coef[kMaxTopK];
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x < k) {
+    const int32_t r = f2s[(int64_t)t * k + threadIdx.x];
+    rows[threadIdx.x] = r;
+    coef[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x] * row_scale[r];
+  }
+  __syncthreads();
+  const int c = (blockIdx.y * kThreads + threadIdx.x) * kVec;
+  if (c >= D) return;
+  float acc[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) acc[i] = 0.f;
+  auto add = [&](const __half* src, float w) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(src);
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(h[i]);
+      acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+    }
+  };
+  for (int j = 0; j < k; ++j) add(y16 + (int64_t)rows[j] * D + c, coef[j]);
+  if (y16_shared != nullptr)
+    add(y16_shared + (int64_t)t * D + c, gate[t] * row_scale_shared[t]);
+  uint4 packed;
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+  *reinterpret_cast<uint4*>(out + (int64_t)t * D + c) = packed;
+}
+
 }  // namespace
+
+cudaError_t launch_combine_f16(const uint16_t* y16, const float* row_scale,
+                               const int32_t* f2s, const float* topk_w, int T,
+                               int k, int D, const uint16_t* y16_shared,
+                               const float* row_scale_shared,
+                               const float* shared_gate, uint16_t* out,
+                               cudaStream_t stream, bool pdl) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid((unsigned)T, (unsigned)((D / kVec + kThreads - 1) / kThreads));
+  return launch_kernel(pdl, grid, dim3(kThreads), 0, stream, combine_f16_kernel,
+                       reinterpret_cast<const __half*>(y16), row_scale, f2s, topk_w,
+                       k, D, reinterpret_cast<const __half*>(y16_shared),
+                       row_scale_shared, shared_gate,
+                       reinterpret_cast<__nv_bfloat16*>(out));
+}
 
 cudaError_t launch_combine(const float* y, const int32_t* f2s,
                            const float* topk_w, int T, int k, int D,

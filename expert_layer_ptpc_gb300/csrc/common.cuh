@@ -23,6 +23,7 @@ enum : unsigned {
   kErrTimeoutDrain = 1u << 3,
   kErrBadIndex = 1u << 4,
   kErrTimeoutSched = 1u << 5,
+  kErrDebugWait = 1u << 6,
 };
 
 // Wall-clock limit of one wait (ns). Every wait in these kernels normally

@@ -332,10 +332,10 @@ inline int64_t token_tiles_upper(int64_t a_rows, int groups, int bn) {
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
                int box_rows);
 
-// Row-major [rows, cols] fp32 matrix as a 2D TMA tensor map for stores of
-// box_rows x box_cols boxes (no swizzle).
-bool make_tmap_f32(CUtensorMap* map, void* base, int64_t rows, int cols,
-                   int box_rows, int box_cols);
+// Row-major [rows, cols] fp32 (elem_bytes 4) or fp16 (2) matrix as a 2D TMA
+// tensor map for stores of box_rows x box_cols boxes (no swizzle).
+bool make_tmap_out(CUtensorMap* map, void* base, int64_t rows, int cols,
+                   int box_rows, int box_cols, int elem_bytes);
 
 // Streaming multiprocessors of the current device (cached).
 int sm_count();

@@ -559,7 +559,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
   CUtensorMap tm_out;
-  if (!make_tmap_f32(&tm_out, out, a_rows, N, C::kOutRows, 32)) return -3;
+  if (!make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, 32, 4)) return -3;
   auto kern = grouped_gemm_pair_kernel<BN, GATEUP>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)

@@ -30,6 +30,8 @@
 // Every wait is bounded (common.cuh): a wait that runs out raises the device
 // error word, the CTA's roles stop, in-flight copies and MMAs are drained and
 // the TMEM is freed before the kernel returns.
+#include <cuda_fp16.h>
+
 #include <cstdlib>
 #include <mutex>
 
@@ -42,6 +44,18 @@ namespace {
 using namespace gemm;
 
 constexpr int kBM = 128;   // output channels per tile (MMA M)
+
+// Factor that maps the down projection's scaled accumulator into fp16 range
+// for an expert whose largest weight scale is `bound`: every product of two
+// e4m3 codes is at most 448^2 in magnitude, so |acc| <= 448^2 K and
+// |acc * s_d * rho| <= 60000 < 65504 (the largest finite fp16) for every
+// s_d <= bound. Computed in fp64, once per tile, so every CTA gets the same
+// value.
+__device__ __forceinline__ float fp16_rho(float bound, int K) {
+  double r = 60000.0 / (200704.0 * (double)K * (double)bound);
+  if (!(r <= 3.0e38)) r = 3.0e38;   // a zero bound: any finite factor works
+  return (float)r;
+}
 
 template <int BN, int BMW, bool GATEUP>
 struct Cfg {
@@ -82,14 +96,18 @@ struct Cfg {
   static_assert(kStages >= 2, "pipeline depth");
 };
 
-template <int BN, int BMW, bool GATEUP>
+// OUT16 (down projection only): y is written as fp16 codes with one fp32
+// factor per row instead of fp32 values (see the down epilogue).
+template <int BN, int BMW, bool GATEUP, bool OUT16>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
-    unsigned* __restrict__ err) {
+    __half* __restrict__ out16, float* __restrict__ row_scale,
+    const float* __restrict__ w_bound, unsigned* __restrict__ err) {
+  static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
   using C = Cfg<BN, BMW, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -362,8 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       if (n0 + 32 <= nvalid) {
         if (lane == 0) bulk_wait_read_all();   // the previous box has left obuf
         __syncwarp();
+        if constexpr (OUT16) {
+          __half* o16 = reinterpret_cast<__half*>(obuf);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) obuf[j * 32 + lane] = v[j];
+          for (int j = 0; j < 32; ++j) o16[j * 32 + lane] = __float2half_rn(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) obuf[j * 32 + lane] = v[j];
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -372,8 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n0 + j < nvalid) out[(int64_t)(ti.row0 + n0 + j) * N + ch0 + lane] = v[j];
+        for (int j = 0; j < 32; ++j) {
+          if (n0 + j < nvalid) {
+            const int64_t o = (int64_t)(ti.row0 + n0 + j) * N + ch0 + lane;
+            if constexpr (OUT16) out16[o] = __float2half_rn(v[j]);
+            else out[o] = v[j];
+          }
+        }
       }
     };
     bool ok = true;
@@ -390,6 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       const int nvalid = min(BN, ti.row_end - ti.row0);
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
+      // fp16 output: y16 = acc * s_d * rho with rho from the expert's scale
+      // bound, so |y16| <= 60000 whatever the data; the row's factor
+      // a_scale / rho (written once, by the tile of the first channels)
+      // turns the codes back into y.
+      float rho = 1.0f;
+      if constexpr (OUT16) {
+        rho = fp16_rho(w_bound[ti.group], K);
+        if (ti.ctile == 0) {
+          for (int r = (warp - kEpiWarp0) * 32 + lane; r < nvalid; r += 128)
+            row_scale[ti.row0 + r] = __fdiv_rn(a_scale[ti.row0 + r], rho);
+        }
+      }
       if (GATEUP && C::kPacked) {
         // lanes 0-63: gate of channels ctile*64 + m; lanes 64-127: up of the
         // same channels. Up values pass to the gate threads through xbuf.
@@ -457,15 +498,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       } else if (C::kStagedOut) {   // down projection, wide tiles
         const int ch0 = ti.ctile * BMW + q * 32;
         const float sw = w_scale[(int64_t)ti.group * N + ch0 + lane];
+        const float swr = sw * rho;
         for (int n0 = 0; n0 < nvalid; n0 += 32) {
           float acc[32], v[32];
           tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
           tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
           tmem_ld_wait();
-          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+          if constexpr (OUT16) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            v[j] = acc[j] * __shfl_sync(0xffffffffu, sx_l, j) * sw;
+            for (int j = 0; j < 32; ++j) v[j] = acc[j] * swr;
+          } else {
+            const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              v[j] = acc[j] * __shfl_sync(0xffffffffu, sx_l, j) * sw;
+          }
           emit(ti, n0, nvalid, ch0, v);
         }
       } else if (GATEUP) {
@@ -491,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       } else if (m < BMW) {   // down projection (packed: lanes 0-63 only)
         const int ch = ti.ctile * BMW + m;
         const float sw = w_scale[(int64_t)ti.group * N + ch];
+        const float swr = sw * rho;
         for (int n0 = 0; n0 < nvalid; n0 += 16) {
           float acc[16];
           tmem_ld_x16(taddr + n0, acc);
@@ -499,7 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           for (int j = 0; j < 16; ++j) {
             if (n0 + j < nvalid) {
               const int row = ti.row0 + n0 + j;
-              out[(int64_t)row * N + ch] = acc[j] * a_scale[row] * sw;
+              if constexpr (OUT16)
+                out16[(int64_t)row * N + ch] = __float2half_rn(acc[j] * swr);
+              else
+                out[(int64_t)row * N + ch] = acc[j] * a_scale[row] * sw;
             }
           }
         }
@@ -521,18 +572,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   }
 }
 
-template <int BN, int BMW, bool GATEUP>
+// out (fp32) or, with OUT16, out16 + row_scale given w_bound (down only).
+template <int BN, int BMW, bool GATEUP, bool OUT16 = false>
 int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
         const float* w_scale, const int32_t* offsets, int groups, int N, int K,
-        float* out, cudaStream_t stream, bool pdl) {
+        float* out, cudaStream_t stream, bool pdl, __half* out16 = nullptr,
+        float* row_scale = nullptr, const float* w_bound = nullptr) {
   using C = Cfg<BN, BMW, GATEUP>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
   CUtensorMap tm_out{};
-  if (C::kStagedOut && !make_tmap_f32(&tm_out, out, a_rows, N, 32, 32)) return -3;
-  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP>;
+  if (C::kStagedOut) {
+    const bool made = OUT16 ? make_tmap_out(&tm_out, out16, a_rows, N, 32, 32, 2)
+                            : make_tmap_out(&tm_out, out, a_rows, N, 32, 32, 4);
+    if (!made) return -3;
+  }
+  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP, OUT16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
@@ -557,7 +614,8 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
-                         groups, N, K, out, device_error_word());
+                         groups, N, K, out, out16, row_scale, w_bound,
+                         device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
 
@@ -600,15 +658,17 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_tmap_f32(CUtensorMap* map, void* base, int64_t rows, int cols,
-                   int box_rows, int box_cols) {
+bool make_tmap_out(CUtensorMap* map, void* base, int64_t rows, int cols,
+                   int box_rows, int box_cols, int elem_bytes) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+  const CUtensorMapDataType type =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return fn(map, type, 2, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -669,6 +729,26 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   if (avg <= 64) return run<64, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   if (avg <= 128) return run<128, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   return run<256, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+}
+
+int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
+                                 int64_t a_rows, const uint8_t* W,
+                                 const float* w_scale, const float* w_bound,
+                                 const int32_t* offsets, int groups, int N, int K,
+                                 uint16_t* y16, float* row_scale, int rows_hint,
+                                 cudaStream_t stream, bool pdl) {
+  if (a_rows == 0 || groups == 0) return 0;
+  const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
+  __half* o = reinterpret_cast<__half*>(y16);
+#define MOE_DOWN16(bn)                                                             \
+  return run<bn, 128, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, \
+                                   N, K, nullptr, stream, pdl, o, row_scale, w_bound)
+  if (avg <= 16) MOE_DOWN16(16);
+  if (avg <= 32) MOE_DOWN16(32);
+  if (avg <= 64) MOE_DOWN16(64);
+  if (avg <= 128) MOE_DOWN16(128);
+  MOE_DOWN16(256);
+#undef MOE_DOWN16
 }
 
 }  // namespace moe

@@ -92,4 +92,25 @@ cudaError_t launch_combine(const float* y, const int32_t* f2s,
                            const float* y_shared, const float* shared_gate,
                            uint16_t* out, cudaStream_t stream, bool pdl);
 
+// The down projection with y written as fp16 codes plus one fp32 factor per
+// row (single-CTA kernel). Returns a moe_status.
+int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
+                                 int64_t a_rows, const uint8_t* W,
+                                 const float* w_scale, const float* w_bound,
+                                 const int32_t* offsets, int groups, int N, int K,
+                                 uint16_t* y16, float* row_scale, int rows_hint,
+                                 cudaStream_t stream, bool pdl);
+
+// bound[g] = max_n scale[g, n] over a [groups, N] fp32 array.
+cudaError_t launch_scale_max(const float* scale, int groups, int N, float* bound,
+                             cudaStream_t stream, bool pdl);
+
+// combine over fp16 codes: y[r] = row_scale[r] * y16[r].
+cudaError_t launch_combine_f16(const uint16_t* y16, const float* row_scale,
+                               const int32_t* f2s, const float* topk_w, int T,
+                               int k, int D, const uint16_t* y16_shared,
+                               const float* row_scale_shared,
+                               const float* shared_gate, uint16_t* out,
+                               cudaStream_t stream, bool pdl);
+
 }  // namespace moe

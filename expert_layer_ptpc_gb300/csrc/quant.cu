@@ -197,6 +197,34 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                      release_early);
 }
 
+// bound[g] = max over n of scale[g, n]: one block per group. The scales are
+// positive (max(amax, 1e-12) / 448), and fmaxf is exact, so the result is
+// independent of the reduction order.
+__global__ void __launch_bounds__(256) scale_max_kernel(const float* __restrict__ scale,
+                                                        int N, float* __restrict__ bound) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float part[8];
+  const float* row = scale + (int64_t)blockIdx.x * N;
+  float m = 0.f;
+  for (int n = threadIdx.x; n < N; n += 256) m = fmaxf(m, row[n]);
+  m = warp_max(m);
+  if (lane_id() == 0) part[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = part[0];
+    for (int w = 1; w < 8; ++w) r = fmaxf(r, part[w]);
+    bound[blockIdx.x] = r;
+  }
+}
+
+cudaError_t launch_scale_max(const float* scale, int groups, int N, float* bound,
+                             cudaStream_t stream, bool pdl) {
+  if (groups == 0) return cudaSuccess;
+  return launch_kernel(pdl, dim3(groups), dim3(256), 0, stream, scale_max_kernel,
+                       scale, N, bound);
+}
+
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
                                int D, float* gate, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;

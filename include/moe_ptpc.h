@@ -220,6 +220,58 @@ MOE_API int moe_combine(const float* y, const int32_t* flat_to_sorted,
                         uint16_t* out, moe_stream_t stream);
 
 /*
+ * The down projection's output y in fp16 (an encoding between the down GEMM
+ * and the combine; the pages leave y's precision open). Rounding y to bf16
+ * (8 significant bits) would breach the layer's accuracy bound on the
+ * largest outputs; fp16 keeps 11 bits and halves y's HBM traffic against
+ * fp32. Its range is guaranteed by construction:
+ *   y16[r, n] = fp16_rne( acc[r, n] * w_scale[g, n] * rho_g ),
+ *   rho_g = 60000 / (448^2 * K * w_bound[g])   (computed in fp64 -> fp32),
+ *   row_scale[r] = a_scale[r] / rho_g           (IEEE fp32 division),
+ * so that y[r, n] = row_scale[r] * y16[r, n] up to fp16 rounding, where acc
+ * is the fp32 dot product of the codes. Every product of two e4m3 codes is
+ * at most 448^2 in magnitude, so |y16| <= 60000 < 65504 whenever
+ * w_bound[g] >= w_scale[g, n] for every n. Values below fp16's normal range
+ * (6.1e-5, about 1e-9 of that bound) keep an absolute error of at most
+ * 2^-25 * row_scale.
+ */
+
+/*
+ * moe_scale_max - bound[g] = max_n scale[g, n] over a [groups, N] fp32
+ * array (w_bound for the down weights' scales s_d). Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
+ */
+MOE_API int moe_scale_max(const float* scale, int groups, int N, float* bound,
+                          moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_down_f16 - moe_grouped_gemm(MOE_GEMM_DOWN) with y written
+ * in the fp16 encoding above. Arguments as for moe_grouped_gemm, plus
+ * w_bound [groups] fp32 (from moe_scale_max of w_scale), y16 [a_rows, N]
+ * fp16 (written, 16-byte aligned) and row_scale [a_rows] fp32 (written for
+ * the rows of the groups). Returns as moe_grouped_gemm.
+ */
+MOE_API int moe_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
+                                      int64_t a_rows, const uint8_t* W,
+                                      const float* w_scale, const float* w_bound,
+                                      const int32_t* group_offsets, int groups,
+                                      int N, int K, uint16_t* y16, float* row_scale,
+                                      int rows_hint, moe_stream_t stream);
+
+/*
+ * moe_combine_f16 - moe_combine over the fp16 encoding:
+ *   out[t, :] = bf16_rne( sum_{j<k} (topk_w[t, j] * row_scale[r_j]) * y16[r_j, :]
+ *                + (shared_gate[t] * row_scale_shared[t]) * y16_shared[t, :] ),
+ *   r_j = flat_to_sorted[t k + j], in fp32, slot order, the shared term last.
+ *   y16_shared, row_scale_shared and shared_gate are all NULL or all set.
+ */
+MOE_API int moe_combine_f16(const uint16_t* y16, const float* row_scale,
+                            const int32_t* flat_to_sorted, const float* topk_w,
+                            int T, int k, int D, const uint16_t* y16_shared,
+                            const float* row_scale_shared, const float* shared_gate,
+                            uint16_t* out, moe_stream_t stream);
+
+/*
  * moe_forward - the whole layer, every step above chained on `stream`.
  *   x [T, D] bf16. Router input: exactly one of router_logits [T, E] fp32 and
  *   router_w [E, D] bf16 (then the logits are computed by moe_router_logits).
@@ -272,9 +324,21 @@ MOE_API int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
  * `detail` (nullable) receives the raw error bits:
  *   1 TMA producer wait, 2 MMA issuer wait, 4 epilogue wait, 8 drain wait,
  *   16 tile map larger than the launch (offsets past a_rows; those tiles are
- *   not computed), 32 tile scheduler wait.
+ *   not computed), 32 tile scheduler wait, 64 moe_debug_expire_wait.
  */
 MOE_API int moe_device_status(moe_stream_t stream, unsigned* detail);
+
+/*
+ * moe_debug_expire_wait - failure-detection check without a GPU fault: one
+ * thread waits on an mbarrier that nothing arrives on, bounded exactly like
+ * the waits of the layer's kernels but with a limit of `limit_us`
+ * microseconds (1 .. 1,000,000), and records the expiry in the device error
+ * word. The kernel then ends normally and the context stays usable: the next
+ * moe_device_status() returns MOE_ERR_TIMEOUT with `detail` bit 64 and clears
+ * it. No counterpart in the pages (test support). Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG (limit out of range, nothing launched) or MOE_ERR_CUDA.
+ */
+MOE_API int moe_debug_expire_wait(int limit_us, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -62,6 +62,17 @@ def test_argument_errors_need_no_gpu(lib):
     bad = binding.make_dims(16, 4000, 128, 8, 1536, False)
     assert lib.moe_forward_workspace_size(ctypes.byref(bad)) == 0
     assert lib.moe_forward(ctypes.byref(bad), *([None] * 12), 0, None) == -2
+    # the fp16 encoding of y: shapes and pointer sets checked on the host
+    assert lib.moe_scale_max(None, -1, 4, None, None) == -1
+    assert lib.moe_scale_max(None, 0, 4, None, None) == 0        # no groups
+    assert lib.moe_grouped_gemm_down_f16(None, None, 8, None, None, None, None,
+                                         2, 100, 256, None, None, 0, None) == -2
+    fake16 = ctypes.c_void_p(0x1000)
+    assert lib.moe_combine_f16(fake16, fake16, fake16, fake16, 4, 2, 256, fake16,
+                               None, None, fake16, None) == -1    # partial shared set
+    # the failure-detection check validates its limit before touching CUDA
+    assert lib.moe_debug_expire_wait(0, None) == -1
+    assert lib.moe_debug_expire_wait(2000000, None) == -1
     # workspace too small is reported before any launch
     fake = ctypes.c_void_p(0x1000)
     rc = lib.moe_forward(ctypes.byref(d), fake, fake, None, fake, fake, fake,

@@ -121,6 +121,8 @@ class _Run:
     syn.LayerConfig("s4", 1, 256, 64, 6, 128, True, "normal"),
     syn.LayerConfig("s5", 129, 256, 1, 1, 256, False, "normal"),
     syn.LayerConfig("s6", 40, 256, 12, 2, 128, True, "weights"),
+    # rows x D x 4 bytes >= 32 MiB: the expert output takes the fp16 encoding
+    syn.LayerConfig("s7", 1024, 1024, 16, 8, 256, True, "normal"),
 ], ids=lambda c: c.name)
 def test_small_layer_all_tokens(cfg):
     _Run(cfg).check(cfg)

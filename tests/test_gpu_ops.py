@@ -242,6 +242,45 @@ def test_grouped_gemm_leaves_other_rows_alone():
     assert np.all(o[:5] == 7.0) and np.all(o[35:] == 7.0)
 
 
+def test_scale_max():
+    rng = np.random.default_rng(11)
+    sc = rng.uniform(1e-4, 2e-2, (37, 4096)).astype(np.float32)
+    sc[5, 4095] = 0.5                      # the maximum in the last column
+    got = B().moe_scale_max(cuda(sc)).cpu().numpy()
+    assert np.array_equal(got, sc.max(axis=1))
+
+
+@pytest.mark.parametrize("G,counts,N,K,hint", [
+    (4, [3, 0, 17, 1], 128, 256, 0),                 # BN 16, ragged, empty
+    (8, [40, 33, 0, 0, 64, 1, 90, 7], 256, 512, 0),  # BN 32
+    (3, [200, 129, 64], 128, 1024, 0),               # BN 128
+    (5, [300, 0, 257, 511, 2], 384, 384, 0),         # BN 256, tails
+    (2, [1000, 24], 256, 1536, 0),                   # long K
+])
+def test_grouped_gemm_down_f16(G, counts, N, K, hint):
+    """The fp16 encoding of y: row_scale * y16 against the oracle's y, within
+    the fp32 accumulation bound plus fp16 rounding (half an ulp, 2^-11
+    relative; 2^-25 absolute below fp16's normal range) and four fp32
+    roundings (s_d * rho, the product, a_scale / rho)."""
+    aq, sa, wq, sw, offs = _grouped_case(G, counts, N, K, False, seed=G * 7 + N + K)
+    bound_w = B().moe_scale_max(cuda(sw))
+    y16, rs = B().moe_grouped_gemm_down_f16(cuda(aq), cuda(sa), cuda(wq), cuda(sw),
+                                            bound_w, cuda(offs), rows_hint=hint)
+    st, bits = B().moe_device_status()
+    assert st == 0, bits
+    y16 = y16.float().cpu().numpy().astype(np.float64)
+    rs = rs.cpu().numpy().astype(np.float64)
+    rows = int(offs[-1])
+    assert np.all(np.isfinite(y16[:rows])) and np.all(np.abs(y16[:rows]) <= 60000)
+    got = rs[:rows, None] * y16[:rows]
+    ref, gbound = _ref_grouped(aq, sa, wq, sw, offs, N, False)
+    tol = gbound * (1 + 1e-3) + np.abs(ref) * (2.0 ** -11 + 4 * U32) + \
+        rs[:rows, None] * 2.0 ** -25 + 1e-30
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), (np.argwhere(bad)[:5], err[bad][:5], tol[bad][:5])
+
+
 # ---------------------------------------------------------------------------
 # combine
 # ---------------------------------------------------------------------------
@@ -271,6 +310,40 @@ def test_combine(T, k, D, shared):
             absref[t] += np.abs(gate[t].astype(np.float64) * ys[t])
     # fp32 sum of k+1 products, then one bf16 rounding (half a bf16 ulp)
     bound = (k + 2) * U32 * absref + 2.0 ** -8 * np.abs(ref) * (1 + 1e-6)
+    assert np.all(np.abs(got - ref) <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("T,k,D,shared", [(64, 2, 256, False), (17, 8, 4096, True),
+                                          (5, 10, 1024, True), (1, 1, 128, False)])
+def test_combine_f16(T, k, D, shared):
+    rng = np.random.default_rng(T * k + D + 1)
+    R = T * k
+    rows = R + (T if shared else 0)
+    y16 = (rng.standard_normal((rows, D)) * 300).astype(np.float16)
+    rs = rng.uniform(1e-4, 1e-2, rows).astype(np.float32)
+    f2s = rng.permutation(R).astype(np.int32)
+    w = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    gate = rng.uniform(0, 1, T).astype(np.float32) if shared else None
+    out = B().moe_combine_f16(
+        cuda(y16), cuda(rs), cuda(f2s), cuda(w),
+        y16_shared=cuda(y16[R:]) if shared else None,
+        row_scale_shared=cuda(rs[R:]) if shared else None,
+        shared_gate=cuda(gate) if shared else None)
+    got = out.float().cpu().numpy().astype(np.float64)
+    yd = y16.astype(np.float64)
+    ref = np.zeros((T, D))
+    absref = np.zeros((T, D))
+    for t in range(T):
+        terms = [(w[t, j].astype(np.float64) * rs[f2s[t * k + j]], yd[f2s[t * k + j]])
+                 for j in range(k)]
+        if shared:
+            terms.append((gate[t].astype(np.float64) * rs[R + t], yd[R + t]))
+        for c, yr in terms:
+            ref[t] += c * yr
+            absref[t] += np.abs(c * yr)
+    # one rounding of each coefficient, fp32 sum of k+1 products, one bf16
+    # rounding (half a bf16 ulp)
+    bound = (k + 3) * U32 * absref + 2.0 ** -8 * np.abs(ref) * (1 + 1e-6)
     assert np.all(np.abs(got - ref) <= bound + 1e-30)
 
 
