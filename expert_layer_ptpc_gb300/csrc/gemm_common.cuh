@@ -33,6 +33,18 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
+// Factor that maps the down projection's scaled accumulator into fp16 range
+// for an expert whose largest weight scale is `bound`: every product of two
+// e4m3 codes is at most 448^2 in magnitude, so |acc| <= 448^2 K and
+// |acc * s_d * rho| <= 60000 < 65504 (the largest finite fp16) for every
+// s_d <= bound. Computed in fp64, once per tile, so every CTA gets the same
+// value.
+__device__ __forceinline__ float fp16_rho(float bound, int K) {
+  double r = 60000.0 / (200704.0 * (double)K * (double)bound);
+  if (!(r <= 3.0e38)) r = 3.0e38;   // a zero bound: any finite factor works
+  return (float)r;
+}
+
 struct TileInfo {
   int group, ctile, row0, row_end;
 };

@@ -26,6 +26,8 @@
 // The leader's commits are multicast to both CTAs (stage free, accumulator
 // ready); both CTAs' epilogues release an accumulator buffer by arriving on
 // the leader's barrier. All waits are bounded (common.cuh).
+#include <cuda_fp16.h>
+
 #include <algorithm>
 
 #include "gemm_common.cuh"
@@ -160,14 +162,18 @@ __device__ __forceinline__ int pair_width(int nvalid) {
   return n;
 }
 
-template <int BN, bool GATEUP>
+// OUT16 (down projection only): y as fp16 codes plus one factor per row, the
+// encoding of the single-CTA kernel (gemm_tc.cu, fp16_rho).
+template <int BN, bool GATEUP, bool OUT16>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
-    unsigned* __restrict__ err) {
+    __half* __restrict__ out16, float* __restrict__ row_scale,
+    const float* __restrict__ w_bound, unsigned* __restrict__ err) {
+  static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
   using C = PairCfg<BN, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -431,8 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       if (r0 + C::kOutRows <= row_end) {
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
+        if constexpr (OUT16) {
+          __half* o16 = reinterpret_cast<__half*>(obuf);
 #pragma unroll
-        for (int j = 0; j < C::kOutRows; ++j) obuf[j * 32 + lane] = v[j];
+          for (int j = 0; j < C::kOutRows; ++j) o16[j * 32 + lane] = __float2half_rn(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < C::kOutRows; ++j) obuf[j * 32 + lane] = v[j];
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -441,8 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < C::kOutRows; ++j)
-          if (r0 + j < row_end) out[(int64_t)(r0 + j) * N + ch0 + lane] = v[j];
+        for (int j = 0; j < C::kOutRows; ++j) {
+          if (r0 + j < row_end) {
+            const int64_t o = (int64_t)(r0 + j) * N + ch0 + lane;
+            if constexpr (OUT16) out16[o] = __float2half_rn(v[j]);
+            else out[o] = v[j];
+          }
+        }
       }
     };
     TileCursor cur;
@@ -517,15 +534,30 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       } else {
         const int ch = ti.ctile * 256 + (int)rank * 128 + m;
         const float sw = w_scale[(int64_t)ti.group * N + ch];
+        float swr = sw;
+        if constexpr (OUT16) {
+          const float rho = fp16_rho(w_bound[ti.group], K);
+          swr = sw * rho;
+          if (ti.ctile == 0 && rank == 0) {   // one factor per row
+            for (int r = (warp - kEpiWarp0) * 32 + lane; r < nvalid; r += 128)
+              row_scale[ti.row0 + r] = __fdiv_rn(a_scale[ti.row0 + r], rho);
+          }
+        }
         for (int n0 = 0; n0 < nvalid; n0 += 32) {
           float acc[32];
           tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
           tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
           tmem_ld_wait();
-          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
           float v[32];
+          if constexpr (OUT16) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = acc[j] * __shfl_sync(0xffffffffu, sx_l, j) * sw;
+            for (int j = 0; j < 32; ++j) v[j] = acc[j] * swr;
+          } else {
+            const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              v[j] = acc[j] * __shfl_sync(0xffffffffu, sx_l, j) * sw;
+          }
           emit(ti.row0 + n0, ti.row0 + nvalid, ch - lane, v);
         }
       }
@@ -549,18 +581,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   }
 }
 
-template <int BN, bool GATEUP>
+template <int BN, bool GATEUP, bool OUT16 = false>
 int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
              const uint8_t* W, const float* w_scale, const int32_t* offsets,
-             int groups, int N, int K, float* out, cudaStream_t stream, bool pdl) {
+             int groups, int N, int K, float* out, cudaStream_t stream, bool pdl,
+             __half* out16 = nullptr, float* row_scale = nullptr,
+             const float* w_bound = nullptr) {
   using C = PairCfg<BN, GATEUP>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
   CUtensorMap tm_out;
-  if (!make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, 32, 4)) return -3;
-  auto kern = grouped_gemm_pair_kernel<BN, GATEUP>;
+  const bool made = OUT16 ? make_tmap_out(&tm_out, out16, a_rows, N, C::kOutRows, 32, 2)
+                          : make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, 32, 4);
+  if (!made) return -3;
+  auto kern = grouped_gemm_pair_kernel<BN, GATEUP, OUT16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
@@ -585,7 +621,8 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
-                         groups, N, K, out, device_error_word());
+                         groups, N, K, out, out16, row_scale, w_bound,
+                         device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
 
@@ -612,6 +649,20 @@ int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
                                 K, out, stream, pdl);
   return run_pair<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
                               out, stream, pdl);
+}
+
+int launch_grouped_gemm_pair_down_f16(const uint8_t* A, const float* a_scale,
+                                      int64_t a_rows, const uint8_t* W,
+                                      const float* w_scale, const float* w_bound,
+                                      const int32_t* offsets, int groups, int N,
+                                      int K, uint16_t* y16, float* row_scale, int bn,
+                                      cudaStream_t stream, bool pdl) {
+  __half* o = reinterpret_cast<__half*>(y16);
+  if (bn <= 128)
+    return run_pair<128, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups,
+                                      N, K, nullptr, stream, pdl, o, row_scale, w_bound);
+  return run_pair<256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
+                                    K, nullptr, stream, pdl, o, row_scale, w_bound);
 }
 
 }  // namespace moe

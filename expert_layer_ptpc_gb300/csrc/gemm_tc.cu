@@ -45,18 +45,6 @@ using namespace gemm;
 
 constexpr int kBM = 128;   // output channels per tile (MMA M)
 
-// Factor that maps the down projection's scaled accumulator into fp16 range
-// for an expert whose largest weight scale is `bound`: every product of two
-// e4m3 codes is at most 448^2 in magnitude, so |acc| <= 448^2 K and
-// |acc * s_d * rho| <= 60000 < 65504 (the largest finite fp16) for every
-// s_d <= bound. Computed in fp64, once per tile, so every CTA gets the same
-// value.
-__device__ __forceinline__ float fp16_rho(float bound, int K) {
-  double r = 60000.0 / (200704.0 * (double)K * (double)bound);
-  if (!(r <= 3.0e38)) r = 3.0e38;   // a zero bound: any finite factor works
-  return (float)r;
-}
-
 template <int BN, int BMW, bool GATEUP>
 struct Cfg {
   // BMW = output channels per tile. 128: the MMA's 128 rows are 128 channels
@@ -739,6 +727,11 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
                                  cudaStream_t stream, bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
+  // single-CTA kernel unless MOE_GEMM_CTA_PAIR=1 forces the pair
+  if (cta_pair_mode() == 1 && avg > 64 && grouped_gemm_pair_supported(1, N))
+    return launch_grouped_gemm_pair_down_f16(A, a_scale, a_rows, W, w_scale, w_bound,
+                                             offsets, groups, N, K, y16, row_scale,
+                                             avg <= 128 ? 128 : 256, stream, pdl);
   __half* o = reinterpret_cast<__half*>(y16);
 #define MOE_DOWN16(bn)                                                             \
   return run<bn, 128, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, \

@@ -101,6 +101,14 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
                                  uint16_t* y16, float* row_scale, int rows_hint,
                                  cudaStream_t stream, bool pdl);
 
+// The same on the CTA pair (N a multiple of 256, bn 128 or 256).
+int launch_grouped_gemm_pair_down_f16(const uint8_t* A, const float* a_scale,
+                                      int64_t a_rows, const uint8_t* W,
+                                      const float* w_scale, const float* w_bound,
+                                      const int32_t* offsets, int groups, int N,
+                                      int K, uint16_t* y16, float* row_scale, int bn,
+                                      cudaStream_t stream, bool pdl);
+
 // bound[g] = max_n scale[g, n] over a [groups, N] fp32 array.
 cudaError_t launch_scale_max(const float* scale, int groups, int N, float* bound,
                              cudaStream_t stream, bool pdl);
