@@ -9,8 +9,11 @@ failure. This checks that the pins constrain every step of the oracle.
 import numpy as np
 import pytest
 
+import oracle
 import oracle.moe_ref as ref
+import oracle.norm_ref as nref
 from tests import test_oracle_layer as layer_pins
+from tests import test_oracle_norm as norm_pins
 from tests import test_oracle_route as route_pins
 
 
@@ -83,6 +86,42 @@ _orig_route = ref.route_ref
 _orig_permute = ref.permute_ref
 
 
+def _norm_variant(no_gamma=False, d_minus_1=False, eps_outside=False, no_bf16=False):
+    def f(x, res, gamma, eps):
+        x32 = np.asarray(x, np.float32)
+        res32 = np.asarray(res, np.float32)
+        g32 = np.asarray(gamma, np.float32)
+        T, D = x32.shape
+        s = (x32 + res32).astype(np.float32)
+        r = s if no_bf16 else oracle.bf16_round(s.astype(np.float64))
+        v = np.empty((T, D), np.float32)
+        inv = np.empty(T, np.float32)
+        for t in range(T):
+            ms = np.float32(np.sum(r[t].astype(np.float64) ** 2) / (D - 1 if d_minus_1 else D))
+            if eps_outside:
+                inv[t] = np.float32(1.0 / (np.sqrt(np.float64(ms)) + eps))
+            else:
+                inv[t] = nref.rsqrt_f32_rn(np.float32(ms + np.float32(eps)))
+            v[t] = (r[t] * inv[t]).astype(np.float32) * (np.float32(1) if no_gamma else g32)
+        return r, v, inv
+    return f
+
+
+def _mut_rsqrt_two_roundings(a):
+    a32 = np.float32(a)
+    return np.float32(np.float32(1.0) / np.sqrt(a32))
+
+
+def _norm_pins():
+    for a in [1e-6, 0.25, 0.3, 1.0, 2.0, 3.0, 7.5, 1234.5678, 6.02e23, 1.1754944e-38, 3.0e38]:
+        norm_pins.test_rsqrt_is_correctly_rounded(a)
+    norm_pins.test_residual_matches_torch_bf16_add()
+    norm_pins.test_matches_torch_rms_norm()
+    norm_pins.test_constant_row_closed_form()
+    norm_pins.test_scale_invariance_without_eps()
+    norm_pins.test_zero_row_quantises_to_zero()
+
+
 def _layer_pins():
     for params in [(25, 128, 6, 3, 128, True, "normal"),
                    (33, 256, 8, 2, 128, False, "weights")]:
@@ -120,6 +159,16 @@ MUTANTS = {
     "quant_wrong_fp8_max": (ref, "quant_rows_ref", _mut_quant_wrong_max,
                             _quant_pins),
     "shared_gate_ignored": (ref, "sigmoid_ref", _mut_sigmoid_gate, _layer_pins),
+    "norm_drops_gamma": (nref, "add_rmsnorm_ref", _norm_variant(no_gamma=True),
+                         _norm_pins),
+    "norm_mean_over_d_minus_1": (nref, "add_rmsnorm_ref",
+                                 _norm_variant(d_minus_1=True), _norm_pins),
+    "norm_eps_outside_sqrt": (nref, "add_rmsnorm_ref",
+                              _norm_variant(eps_outside=True), _norm_pins),
+    "norm_residual_not_bf16": (nref, "add_rmsnorm_ref", _norm_variant(no_bf16=True),
+                               _norm_pins),
+    "rsqrt_two_roundings": (nref, "rsqrt_f32_rn", _mut_rsqrt_two_roundings,
+                            _norm_pins),
 }
 
 
@@ -127,7 +176,10 @@ MUTANTS = {
 def test_mutant_is_caught(monkeypatch, name):
     module, attr, fn, pins = MUTANTS[name]
     monkeypatch.setattr(module, attr, fn)
-    # the pin modules imported some oracle functions by name
+    # the pin modules imported some oracle functions by name, and the norm
+    # pins call them through the package
+    if hasattr(oracle, attr):
+        monkeypatch.setattr(oracle, attr, fn)
     for pin_mod in (layer_pins, route_pins):
         if hasattr(pin_mod, attr):
             monkeypatch.setattr(pin_mod, attr, fn)
