@@ -181,8 +181,11 @@ def kernel_launches_per_step(cfg):
     R = cfg.T * cfg.k
     permute = 1 if R <= 8192 else 3
     router = 1 if cfg.router == "weights" else 0
+    # the down weights' scale bound, when y takes the fp16 encoding (its fp32
+    # size reaches 32 MiB)
+    bound = 1 if cfg.rows * cfg.D * 4 >= (32 << 20) else 0
     # router, route, permute, quant, gate/up GEMM, requant, down GEMM, combine
-    return router + 1 + permute + 1 + 1 + 1 + 1 + 1
+    return bound + router + 1 + permute + 1 + 1 + 1 + 1 + 1
 
 
 def algorithmic_bytes(cfg, counts):
@@ -380,6 +383,15 @@ def run_ours(args, cfg, rank, world, local_rank):
     x = syn.gen_x(cfg, dev, 0)
     logits = None if cfg.router == "weights" else syn.gen_logits(cfg, dev, 0)
     out = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=dev)
+    pre = {}
+    if args.prenorm:   # layer input = RMSNorm(x + residual) * gamma
+        if logits is None:
+            raise SystemExit("--prenorm needs a workload with router logits")
+        g = torch.Generator(device="cpu").manual_seed(12345)
+        res = (torch.randn(cfg.T, cfg.D, generator=g) * 0.5).to(torch.bfloat16).to(dev)
+        gamma = (1.0 + 0.1 * torch.randn(cfg.D, generator=g)).to(torch.bfloat16).to(dev)
+        pre = {"residual": res, "gamma": gamma, "eps": 1e-6,
+               "residual_out": torch.empty_like(res)}
     ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
     tw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -395,7 +407,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         return evs
 
     def step(evs=None):
-        layer.forward(x, logits, out=out, topk_ids=ids, topk_w=tw, events=evs)
+        layer.forward(x, logits, out=out, topk_ids=ids, topk_w=tw, events=evs, **pre)
 
     # warm-up (also validates the run)
     warm = make_events(1)[0]
@@ -472,12 +484,22 @@ def run_ours(args, cfg, rank, world, local_rank):
     out_h = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16).pin_memory()
     x_d = torch.empty_like(x)
     lg_d = torch.empty_like(logits) if logits is not None else None
+    if pre:   # the residual stream goes in and comes back too
+        res_h = pre["residual"].cpu().pin_memory()
+        res_out_h = torch.empty_like(res_h).pin_memory()
+        res_d = torch.empty_like(pre["residual"])
 
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
         if lg_d is not None:
             lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward(x_d, lg_d, out=out)
+        if pre:
+            res_d.copy_(res_h, non_blocking=True)
+            layer.forward(x_d, lg_d, out=out, residual=res_d, gamma=pre["gamma"],
+                          eps=pre["eps"], residual_out=pre["residual_out"])
+            res_out_h.copy_(pre["residual_out"], non_blocking=True)
+        else:
+            layer.forward(x_d, lg_d, out=out)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(max(args.warmup, 1)):
@@ -497,16 +519,22 @@ def run_ours(args, cfg, rank, world, local_rank):
     e2e_max = max_over_ranks(e2e_mean, dev)
     h2d = x.numel() * 2 + (logits.numel() * 4 if logits is not None else 0)
     d2h = out.numel() * 2
+    if pre:
+        h2d += pre["residual"].numel() * 2
+        d2h += pre["residual"].numel() * 2
 
     if rank != 0:
         return
     counts = torch.bincount(ids.view(-1).long(), minlength=cfg.E).cpu().numpy()
     B, touched = algorithmic_bytes(cfg, counts)
+    if pre:   # the residual read and the new residual written, gamma
+        B += 2 * cfg.T * cfg.D * 2 + 2 * cfg.D
     F = layer_flops(cfg)
     hbm, bf16, peak_src = peaks()
     gemm_ms = sum(phase_ms[4]) / len(phase_ms[4])
     gu_bytes = gateup_bytes(cfg, touched)
-    names = ["router", "route", "permute", "quant_x", "gateup_gemm", "requant",
+    names = ["router", "route", "permute",
+             "addnorm_quant_x" if pre else "quant_x", "gateup_gemm", "requant",
              "down_gemm", "combine"]
     kernel_ms = {n: round(sum(p) / len(p), 5) for n, p in zip(names, phase_ms)}
     dominant = max(kernel_ms, key=kernel_ms.get)
@@ -544,6 +572,20 @@ def run_ours(args, cfg, rank, world, local_rank):
         "achieved_fp8_tflops": F / (max_ms * 1e-3) / 1e12,
         "t_roof_ms": t_roof * 1e3, "frac": t_roof / (max_ms * 1e-3)}
     clocks = sampler.summary(t_wall0, t_wall1)
+    prenorm = None
+    if pre:
+        # the fused add + RMSNorm + quant launch: x, residual and gamma in;
+        # the new residual, the codes of every destination row (k + shared)
+        # and their scales (and the gate) out. Unfused, the normalised bf16
+        # activations would be written and read once more.
+        q_ms = sum(phase_ms[3]) / len(phase_ms[3])
+        qb = 3 * cfg.T * cfg.D * 2 + 2 * cfg.D + cfg.rows * (cfg.D + 4) + \
+            (4 * cfg.T + 2 * cfg.D if cfg.shared else 0)
+        prenorm = {"kernel": "add + RMSNorm + per-token FP8 quant (fused)",
+                   "ms_per_launch": q_ms, "algorithmic_bytes_per_launch": qb,
+                   "achieved_gbs": qb / (q_ms * 1e-3) / 1e9,
+                   "frac": qb / (q_ms * 1e-3) / 1e9 / hbm, "peak_gbs": hbm,
+                   "unfused_extra_bytes": 2 * cfg.T * cfg.D * 2}
     tokens_per_s = replica_tokens_per_s(cfg.T, world, max_ms)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s",
@@ -568,6 +610,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         "gpu_launches": kernel_launches_per_step(cfg) * args.steps,
         "clocks": clocks,
     }
+    if prenorm is not None:
+        line["config"]["prenorm"] = {"eps": pre["eps"], "input": "RMSNorm(x + residual) * gamma"}
+        line["prenorm"] = prenorm
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     print(json.dumps(line), flush=True)
@@ -581,6 +626,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prenorm", action="store_true",
+                    help="feed the layer from the residual stream: fused add + "
+                         "RMSNorm + quant replaces the quantisation step")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the forward directly instead of replaying a "
                          "CUDA graph of it")

@@ -34,6 +34,11 @@ class moe_dims(ctypes.Structure):
                 ("renormalize", ctypes.c_int32)]
 
 
+class moe_prenorm(ctypes.Structure):
+    _fields_ = [("residual", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("residual_out", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -64,6 +69,10 @@ _SIGNATURES = {
                                   ctypes.POINTER(ctypes.c_void_p), _I, _P]),
     "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "moe_debug_expire_wait": (_I, [_I, _P]),
+    "moe_add_rmsnorm_quant": (_I, [_P, _P, _P, ctypes.c_float, _I64, _I, _P, _P, _I,
+                                   _I64, _P, _P, _P, _P, _P]),
+    "moe_forward_prenorm": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 _SZ, _P, _I, _P]),
 }
 
 MOE_FORWARD_EVENTS = 9
@@ -319,10 +328,13 @@ def moe_forward_workspace_size(dims):
 
 def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,
                 router_w=None, shared_gate_w=None, out=None, ws=None,
-                topk_ids=None, topk_w=None, stream=None, events=None):
+                topk_ids=None, topk_w=None, stream=None, events=None,
+                residual=None, gamma=None, eps=1e-6, residual_out=None):
     """The whole layer; returns out [T, D] bf16. `events`: optional list of
     MOE_FORWARD_EVENTS torch.cuda.Event(enable_timing=True), recorded at the
-    step boundaries (moe_forward_profiled)."""
+    step boundaries (moe_forward_profiled). With `residual` and `gamma` the
+    layer input is RMSNorm(x + residual) (moe_forward_prenorm): the new
+    residual goes to `residual_out` (default: residual, updated in place)."""
     _need(x, torch.bfloat16, "x")
     for t, n in ((w_gu, "w_gu"), (w_d, "w_d")):
         _need(t, torch.uint8, n)
@@ -340,6 +352,26 @@ def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,
     need = lib.moe_forward_workspace_size(ctypes.byref(dims))
     if ws is None:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual")
+        _need(gamma, torch.bfloat16, "gamma")
+        if residual_out is None:
+            residual_out = residual
+        _need(residual_out, torch.bfloat16, "residual_out")
+        pre = moe_prenorm(residual.data_ptr(), gamma.data_ptr(), float(eps),
+                          residual_out.data_ptr())
+        handles = None
+        if events is not None:
+            if len(events) != MOE_FORWARD_EVENTS:
+                raise ValueError(f"need {MOE_FORWARD_EVENTS} events")
+            handles = (ctypes.c_void_p * MOE_FORWARD_EVENTS)(
+                *[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check("moe_forward_prenorm", lib.moe_forward_prenorm(
+            ctypes.byref(dims), ctypes.byref(pre), _ptr(x), _ptr(router_logits),
+            _ptr(w_gu), _ptr(s_gu), _ptr(w_d), _ptr(s_d), _ptr(shared_gate_w),
+            _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(), handles,
+            MOE_FORWARD_EVENTS if handles is not None else 0, _stream(stream)))
+        return out
     args = (ctypes.byref(dims), _ptr(x), _ptr(router_logits), _ptr(router_w),
             _ptr(w_gu), _ptr(s_gu), _ptr(w_d), _ptr(s_d), _ptr(shared_gate_w),
             _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel())
@@ -353,6 +385,34 @@ def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,
         _check("moe_forward_profiled", lib.moe_forward_profiled(
             *args, handles, MOE_FORWARD_EVENTS, _stream(stream)))
     return out
+
+
+def moe_add_rmsnorm_quant(x, residual, gamma, eps=1e-6, dst_rows=None, copies=1,
+                          extra_row_base=-1, out_rows=None, residual_out=None,
+                          out_q=None, out_scale=None, gate_w=None, gate_out=None,
+                          stream=None):
+    """residual_out = bf16(x + residual); codes / scales of RMSNorm(.) * gamma
+    written like moe_quant_ptpc. Returns (residual_out, out_q, out_scale,
+    gate_out)."""
+    _need(x, torch.bfloat16, "x")
+    _need(residual, torch.bfloat16, "residual")
+    _need(gamma, torch.bfloat16, "gamma")
+    rows, cols = x.shape
+    if out_rows is None:
+        out_rows = rows
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    if out_q is None:
+        out_q = torch.empty((out_rows, cols), dtype=torch.uint8, device=x.device)
+    if out_scale is None:
+        out_scale = torch.empty(out_rows, dtype=torch.float32, device=x.device)
+    if gate_w is not None and gate_out is None:
+        gate_out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check("moe_add_rmsnorm_quant", load_library().moe_add_rmsnorm_quant(
+        _ptr(x), _ptr(residual), _ptr(gamma), float(eps), rows, cols,
+        _ptr(residual_out), _ptr(dst_rows), copies, extra_row_base, _ptr(out_q),
+        _ptr(out_scale), _ptr(gate_w), _ptr(gate_out), _stream(stream)))
+    return residual_out, out_q, out_scale, gate_out
 
 
 def moe_debug_expire_wait(limit_us, stream=None):

@@ -295,7 +295,7 @@ size_t moe_forward_workspace_size(const moe_dims* dims) {
 
 namespace {
 
-int forward_impl(const moe_dims* dims, const uint16_t* x,
+int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x,
                  const float* router_logits, const uint16_t* router_w,
                  const uint8_t* w_gu, const float* s_gu, const uint8_t* w_d,
                  const float* s_d, const uint16_t* shared_gate_w, uint16_t* out,
@@ -316,6 +316,13 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
     return MOE_ERR_INVALID_ARG;
   if (router_w != nullptr && !aligned16(router_w)) return MOE_ERR_INVALID_ARG;
   if (shared_gate_w != nullptr && !aligned16(shared_gate_w)) return MOE_ERR_INVALID_ARG;
+  if (pre != nullptr) {   // the layer input comes from the residual stream
+    if (router_w != nullptr) return MOE_ERR_UNSUPPORTED;
+    if (!pre->residual || !pre->gamma || !pre->residual_out ||
+        !aligned16(pre->residual) || !aligned16(pre->gamma) ||
+        !aligned16(pre->residual_out) || !(pre->eps >= 0.0f))
+      return MOE_ERR_INVALID_ARG;
+  }
   const ForwardLayout L = forward_layout(d);
   if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
 
@@ -373,11 +380,16 @@ int forward_impl(const moe_dims* dims, const uint16_t* x,
   mark(3);
   // x -> FP8 codes written straight into each token's k expert rows (and its
   // shared-expert row R + t), plus the shared-expert gate.
-  st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
-                                d.shared ? R : -1, xq, sx,
-                                d.shared ? shared_gate_w : nullptr,
-                                d.shared ? gate : nullptr, stream, pdl,
-                                false));
+  if (pre != nullptr)   // r = x + residual, RMSNorm, then the same quantiser
+    st = cuda_status(launch_add_rmsnorm_quant(
+        x, pre->residual, pre->gamma, pre->eps, d.T, d.D, pre->residual_out, f2s,
+        d.k, d.shared ? R : -1, xq, sx, d.shared ? shared_gate_w : nullptr,
+        d.shared ? gate : nullptr, stream, pdl));
+  else
+    st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
+                                  d.shared ? R : -1, xq, sx,
+                                  d.shared ? shared_gate_w : nullptr,
+                                  d.shared ? gate : nullptr, stream, pdl, false));
   if (st != MOE_OK) return st;
   mark(4);
   const int hint = (int)std::max<int64_t>(1, R / d.E);
@@ -422,9 +434,50 @@ int moe_forward(const moe_dims* dims, const uint16_t* x,
                 const float* s_d, const uint16_t* shared_gate_w, uint16_t* out,
                 int32_t* topk_ids_out, float* topk_w_out, void* ws,
                 size_t ws_bytes, moe_stream_t stream) {
-  return forward_impl(dims, x, router_logits, router_w, w_gu, s_gu, w_d, s_d,
-                      shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
+  return forward_impl(dims, nullptr, x, router_logits, router_w, w_gu, s_gu, w_d,
+                      s_d, shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
                       nullptr, stream);
+}
+
+int moe_forward_prenorm(const moe_dims* dims, const moe_prenorm* pre,
+                        const uint16_t* x, const float* router_logits,
+                        const uint8_t* w_gu, const float* s_gu, const uint8_t* w_d,
+                        const float* s_d, const uint16_t* shared_gate_w,
+                        uint16_t* out, int32_t* topk_ids_out, float* topk_w_out,
+                        void* ws, size_t ws_bytes, void* const* events, int n_events,
+                        moe_stream_t stream) {
+  if (pre == nullptr || router_logits == nullptr) return MOE_ERR_INVALID_ARG;
+  if (events != nullptr) {
+    if (n_events != MOE_FORWARD_EVENTS) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i)
+      if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+  return forward_impl(dims, pre, x, router_logits, nullptr, w_gu, s_gu, w_d, s_d,
+                      shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
+                      reinterpret_cast<cudaEvent_t const*>(events), stream);
+}
+
+int moe_add_rmsnorm_quant(const uint16_t* x, const uint16_t* residual,
+                          const uint16_t* gamma, float eps, int64_t rows, int cols,
+                          uint16_t* residual_out, const int32_t* dst_rows, int copies,
+                          int64_t extra_row_base, uint8_t* out_q, float* out_scale,
+                          const uint16_t* gate_w, float* gate_out,
+                          moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || copies < 1 || !(eps >= 0.0f))
+    return MOE_ERR_INVALID_ARG;
+  if (cols > kMaxQuantCols || copies > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (dst_rows == nullptr && copies != 1) return MOE_ERR_INVALID_ARG;
+  if ((gate_w == nullptr) != (gate_out == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !residual || !gamma || !residual_out || !out_q || !out_scale)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(gamma) ||
+      !aligned16(residual_out) || !aligned16(out_q) ||
+      (gate_w != nullptr && !aligned16(gate_w)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_add_rmsnorm_quant(
+      x, residual, gamma, eps, rows, cols, residual_out, dst_rows, copies,
+      extra_row_base, out_q, out_scale, gate_w, gate_out, stream, false));
 }
 
 int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
@@ -438,8 +491,8 @@ int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
   if (events == nullptr || n_events != MOE_FORWARD_EVENTS) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < n_events; ++i)
     if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
-  return forward_impl(dims, x, router_logits, router_w, w_gu, s_gu, w_d, s_d,
-                      shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
+  return forward_impl(dims, nullptr, x, router_logits, router_w, w_gu, s_gu, w_d,
+                      s_d, shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
                       reinterpret_cast<cudaEvent_t const*>(events), stream);
 }
 

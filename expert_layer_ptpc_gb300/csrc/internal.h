@@ -65,6 +65,16 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          float* gate_out, cudaStream_t stream, bool pdl,
                          bool release_early);
 
+// Add + RMSNorm + per-token quantisation (see quant.cu); same destinations
+// and limits as launch_quant.
+cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
+                                     const uint16_t* gamma, float eps, int64_t rows,
+                                     int cols, uint16_t* res_out,
+                                     const int32_t* dst_rows, int copies,
+                                     int64_t extra_row_base, uint8_t* out_q,
+                                     float* out_scale, const uint16_t* gate_w,
+                                     float* gate_out, cudaStream_t stream, bool pdl);
+
 // Largest row length launch_quant handles.
 constexpr int kMaxQuantCols = 32768;
 

@@ -137,6 +137,179 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
   }
 }
 
+// Add + RMSNorm + PTPC quantisation of one token row per block ("Ultimate
+// Latency Optimization of Qwen3 and Qwen3-VL on AMD MI300X Series", section
+// 2.1.5: AddRMSNorm and per-token quant fused into one operator):
+//   r = bf16_rne(x + res)                  (written back: the new residual)
+//   ms = fp32(S / D), S = sum r^2          (S exact, see below)
+//   inv = fp32_rn(1 / sqrt(fp32(ms + eps)))  (__frsqrt_rn, correctly rounded)
+//   v = fp32(fp32(r * inv) * gamma)
+// then the quantiser of quant_rows_kernel on v, and optionally the shared
+// expert's gate sigmoid(v . w_g). The row stays in registers throughout: x,
+// res and gamma are read once, r and the codes written once per destination.
+//
+// S in integers: a bf16 value is r = s * 2^(e - 134) with an 8-bit integer
+// significand s (e the fp32 exponent field), so r^2 = s^2 * 2^(2e - 268) with
+// s^2 < 2^16. Every square is placed on the grid 2^(2 emax - 268 - sbits) of
+// the row's largest exponent emax and the row is summed in a 64-bit integer,
+// which is exact and independent of the summation order (sbits leaves room
+// for cols squares of up to 2^16). A square more than 2^sbits below the
+// largest (|r| under 2^-17 of the row's largest for cols = 4096) keeps only
+// its bits on the grid. The one rounding to double of the integer sum then
+// equals the exactly rounded sum the reference takes. (A plain fp64 sum
+// would also be exact, but GB300's fp64 rate made it the kernel's
+// bottleneck.)
+template <int UNITS>
+__global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* res,   // res_out may
+    const __nv_bfloat16* __restrict__ gamma, float eps, int cols,     // alias res
+    __nv_bfloat16* res_out, const int32_t* __restrict__ dst_rows,
+    int copies, int64_t extra_row_base, uint8_t* __restrict__ out_q,
+    float* __restrict__ out_scale, const __nv_bfloat16* __restrict__ gate_w,
+    float* __restrict__ gate_out, int sbits) {
+  __shared__ unsigned long long red_sq[kMaxThreads / 32];
+  __shared__ int red_e[kMaxThreads / 32];
+  __shared__ float red_max[kMaxThreads / 32];
+  __shared__ float red_dot[kMaxThreads / 32];
+  __shared__ int64_t dst[kMaxTopK + 1];
+  __shared__ float s_inv;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int nunits = cols / kVec;
+
+  float v[UNITS][kVec];
+  int emax = 0;
+#pragma unroll
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = tid + i * blockDim.x;
+    if (u < nunits) {
+      float a[kVec], b[kVec];
+      load_vec(x + r * cols + u * kVec, a);
+      load_vec(res + r * cols + u * kVec, b);
+      uint32_t packed[kVec / 2];
+#pragma unroll
+      for (int j = 0; j < kVec; j += 2) {
+        const __nv_bfloat162 p =
+            __floats2bfloat162_rn(__fadd_rn(a[j], b[j]), __fadd_rn(a[j + 1], b[j + 1]));
+        v[i][j] = __low2float(p);
+        v[i][j + 1] = __high2float(p);
+        packed[j / 2] = *reinterpret_cast<const uint32_t*>(&p);
+        emax = max(emax, max((int)((__float_as_uint(v[i][j]) >> 23) & 0xFFu),
+                             (int)((__float_as_uint(v[i][j + 1]) >> 23) & 0xFFu)));
+      }
+      uint4* o = reinterpret_cast<uint4*>(res_out + r * cols + u * kVec);
+      o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+  }
+  // the row's largest exponent field
+  emax = __reduce_max_sync(0xffffffffu, emax);
+  if (lane == 0) red_e[warp] = emax;
+  __syncthreads();
+  emax = 1;   // zeros and subnormals sit at exponent 1
+  for (int w = 0; w < nwarps; ++w) emax = max(emax, red_e[w]);
+  unsigned long long sq = 0;
+#pragma unroll
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = tid + i * blockDim.x;
+    if (u < nunits) {
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        const uint32_t b = __float_as_uint(v[i][j]);
+        int e = (int)((b >> 23) & 0xFFu);
+        uint32_t sig = (b >> 16) & 0x7Fu;
+        if (e != 0) sig |= 0x80u; else e = 1;
+        const unsigned long long s2 = (unsigned long long)(sig * sig);
+        const int sh = sbits - 2 * (emax - e);
+        sq += sh >= 0 ? (s2 << sh) : (sh > -32 ? (s2 >> -sh) : 0ull);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  if (lane == 0) red_sq[warp] = sq;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long t = 0;
+    for (int w = 0; w < nwarps; ++w) t += red_sq[w];
+    // S = t * 2^(2 emax - 268 - sbits): one rounding (of t), then exact
+    const double S = ldexp(__ull2double_rn(t), 2 * emax - 268 - sbits);
+    const float ms = (float)(S / (double)cols);
+    s_inv = __frsqrt_rn(__fadd_rn(ms, eps));
+  }
+  __syncthreads();
+  const float inv = s_inv;
+
+  float amax = 0.f, dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = tid + i * blockDim.x;
+    if (u < nunits) {
+      float g[kVec];
+      load_vec(gamma + u * kVec, g);
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        v[i][j] = __fmul_rn(__fmul_rn(v[i][j], inv), g[j]);
+        amax = fmaxf(amax, fabsf(v[i][j]));
+      }
+      if (gate_w != nullptr) {
+        float w[kVec];
+        load_vec(gate_w + u * kVec, w);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) dot = fmaf(v[i][j], w[j], dot);
+      }
+    }
+  }
+  amax = warp_max(amax);
+  dot = warp_sum(dot);
+  if (lane == 0) {
+    red_max[warp] = amax;
+    red_dot[warp] = dot;
+  }
+  const int nmain = dst_rows != nullptr ? copies : 1;
+  const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
+  if (tid < ndst) {
+    dst[tid] = tid < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + tid] : r)
+                           : extra_row_base + r;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float a = lane < nwarps ? red_max[lane] : 0.f;
+    float d = lane < nwarps ? red_dot[lane] : 0.f;
+    a = warp_max(a);
+    d = warp_sum(d);
+    if (lane == 0) {
+      red_max[0] = a;
+      red_dot[0] = d;
+    }
+  }
+  __syncthreads();
+  const float s = __fdiv_rn(fmaxf(red_max[0], 1e-12f), 448.0f);
+  if (tid < ndst) out_scale[dst[tid]] = s;
+  if (gate_w != nullptr && tid == 0) gate_out[r] = 1.0f / (1.0f + expf(-red_dot[0]));
+#pragma unroll
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = tid + i * blockDim.x;
+    if (u < nunits) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[i][4 * q], s),
+                                            __fdiv_rn(v[i][4 * q + 1], s));
+        const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[i][4 * q + 2], s),
+                                            __fdiv_rn(v[i][4 * q + 3], s));
+        w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int d = 0; d < ndst; ++d)
+        *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) shared_gate_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
     int T, int D, float* __restrict__ gate) {
@@ -195,6 +368,35 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                      extra_row_base, out_q, out_scale,
                      (const __nv_bfloat16*)nullptr, (float*)nullptr, stream, pdl,
                      release_early);
+}
+
+cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
+                                     const uint16_t* gamma, float eps, int64_t rows,
+                                     int cols, uint16_t* res_out,
+                                     const int32_t* dst_rows, int copies,
+                                     int64_t extra_row_base, uint8_t* out_q,
+                                     float* out_scale, const uint16_t* gate_w,
+                                     float* gate_out, cudaStream_t stream, bool pdl) {
+  if (rows == 0) return cudaSuccess;
+  const int nunits = cols / kVec;
+  const int threads = std::min(kMaxThreads, ((nunits + 31) / 32) * 32);
+  const int units = (nunits + threads - 1) / threads;
+  const dim3 grid((unsigned)rows), block(threads);
+  auto bf = [](const uint16_t* p) { return reinterpret_cast<const __nv_bfloat16*>(p); };
+  // grid of the integer sum of squares: cols squares below 2^16 each must
+  // stay under 2^64
+  int lg = 0;
+  while ((1 << lg) < cols) ++lg;
+  const int sbits = 63 - 16 - lg;
+  auto go = [&](auto kern) {
+    return launch_kernel(pdl, grid, block, 0, stream, kern, bf(x), bf(res), bf(gamma),
+                         eps, cols, reinterpret_cast<__nv_bfloat16*>(res_out),
+                         dst_rows, copies, extra_row_base, out_q, out_scale,
+                         bf(gate_w), gate_out, sbits);
+  };
+  if (units <= 1) return go(add_rmsnorm_quant_kernel<1>);
+  if (units <= 2) return go(add_rmsnorm_quant_kernel<2>);
+  return go(add_rmsnorm_quant_kernel<4>);
 }
 
 // bound[g] = max over n of scale[g, n]: one block per group. The scales are

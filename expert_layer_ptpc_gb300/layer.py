@@ -48,12 +48,21 @@ class MoELayer:
         return self._ws
 
     def forward(self, x, router_logits=None, out=None, topk_ids=None,
-                topk_w=None, stream=None, events=None):
+                topk_w=None, stream=None, events=None, residual=None, gamma=None,
+                eps=1e-6, residual_out=None):
+        """The layer on x (bf16 [T, D]); with `residual` and `gamma` on
+        RMSNorm(x + residual) * gamma, the new residual written to
+        `residual_out` (default: in place). The pre-normed form needs
+        router_logits."""
         T = x.shape[0]
-        if self.router_w is not None:
+        router_w = self.router_w
+        if router_w is not None and residual is None:
             router_logits = None
+        elif residual is not None:
+            router_w = None
         return binding.moe_forward(
             self.dims(T), x, self.w_gu, self.s_gu, self.w_d, self.s_d,
-            router_logits=router_logits, router_w=self.router_w,
+            router_logits=router_logits, router_w=router_w,
             shared_gate_w=self.shared_gate_w, out=out, ws=self.workspace(T),
-            topk_ids=topk_ids, topk_w=topk_w, stream=stream, events=events)
+            topk_ids=topk_ids, topk_w=topk_w, stream=stream, events=events,
+            residual=residual, gamma=gamma, eps=eps, residual_out=residual_out)

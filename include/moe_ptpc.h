@@ -173,6 +173,34 @@ MOE_API int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
                            float* out_scale, moe_stream_t stream);
 
 /*
+ * moe_add_rmsnorm_quant - the MoE block's FP8 input straight from the
+ * residual stream: add + RMSNorm + per-token quantisation in one pass (MI300X
+ * page, section 2.1.5, the fusion table; the AllReduce of that operator needs
+ * tensor parallelism and is not part of it here). For each row t < rows:
+ *   r = bf16_rne(fp32(x[t]) + fp32(residual[t]))       -> residual_out[t]
+ *   ms = fp32(sum_d r[d]^2 / cols)                      (squares summed in fp64)
+ *   inv = fp32_rn(1 / sqrt(fp32(ms + eps)))             (correctly rounded)
+ *   v = fp32(fp32(r * inv) * gamma)
+ *   s_t = fp32(max(amax(v), 1e-12) / 448), q = e4m3_rne_sat(fp32(v / s_t))
+ * and, when gate_w is set, gate_out[t] = sigmoid(v . gate_w).
+ *   x, residual, residual_out [rows, cols] bf16; gamma, gate_w [cols] bf16;
+ *   destinations of q / s_t as for moe_quant_ptpc (dst_rows, copies,
+ *   extra_row_base). residual_out may alias residual (each row is read
+ *   before it is written, by the same block).
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned pointers, cols not a
+ *         positive multiple of 16, eps < 0 or NaN, copies < 1, gate_w and
+ *         gate_out not both set or both NULL), MOE_ERR_UNSUPPORTED (cols >
+ *         32768 or copies > 32).
+ */
+MOE_API int moe_add_rmsnorm_quant(const uint16_t* x, const uint16_t* residual,
+                                  const uint16_t* gamma, float eps, int64_t rows,
+                                  int cols, uint16_t* residual_out,
+                                  const int32_t* dst_rows, int copies,
+                                  int64_t extra_row_base, uint8_t* out_q,
+                                  float* out_scale, const uint16_t* gate_w,
+                                  float* gate_out, moe_stream_t stream);
+
+/*
  * moe_shared_gate - shared-expert gate sigmoid(x[t] . w_g), fp32 (the TPU
  * page's shared expert runs on every token; its gate is a sigmoid).
  *   x [T, D] bf16 (D a multiple of 16);  w_g [D] bf16;  gate [T] fp32.
@@ -327,6 +355,32 @@ MOE_API int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
  *   not computed), 32 tile scheduler wait, 64 moe_debug_expire_wait.
  */
 MOE_API int moe_device_status(moe_stream_t stream, unsigned* detail);
+
+/*
+ * moe_forward_prenorm - moe_forward fed from the residual stream: the
+ * quantisation step becomes moe_add_rmsnorm_quant(x, pre->residual,
+ * pre->gamma, pre->eps), which also writes pre->residual_out, and the shared
+ * gate takes the normalised activations. The routing comes from
+ * router_logits (required; there is no router_w form, the router would read
+ * the normalised activations). Other arguments as for moe_forward. `events`
+ * is NULL, or MOE_FORWARD_EVENTS events as for moe_forward_profiled (then
+ * the steps are serialised and marked).
+ */
+typedef struct moe_prenorm {
+  const uint16_t* residual;   /* [T, D] bf16 */
+  const uint16_t* gamma;      /* [D] bf16 */
+  float eps;                  /* >= 0 */
+  uint16_t* residual_out;     /* [T, D] bf16, may alias residual */
+} moe_prenorm;
+
+MOE_API int moe_forward_prenorm(const moe_dims* dims, const moe_prenorm* pre,
+                                const uint16_t* x, const float* router_logits,
+                                const uint8_t* w_gu, const float* s_gu,
+                                const uint8_t* w_d, const float* s_d,
+                                const uint16_t* shared_gate_w, uint16_t* out,
+                                int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                                size_t ws_bytes, void* const* events, int n_events,
+                                moe_stream_t stream);
 
 /*
  * moe_debug_expire_wait - failure-detection check without a GPU fault: one

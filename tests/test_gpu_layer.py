@@ -162,6 +162,43 @@ def test_sweep_layer(sweep_run, T):
     sweep_run.check(cfg, n_sample=4)
 
 
+@pytest.mark.parametrize("cfg", [
+    syn.LayerConfig("p1", 300, 512, 16, 4, 256, True, "normal"),
+    syn.LayerConfig("p2", 1024, 1024, 16, 8, 256, False, "normal"),   # fp16 y
+], ids=lambda c: c.name)
+def test_prenorm_layer_all_tokens(cfg):
+    """moe_forward_prenorm: the layer on RMSNorm(x + residual) * gamma. The new
+    residual is compared bit for bit with the oracle's; the output against the
+    oracle layer evaluated on the oracle's normalised activations v."""
+    from expert_layer_ptpc_gb300 import binding
+    run = _Run(cfg)
+    x, logits = run.inputs(cfg)
+    g = torch.Generator().manual_seed(99)
+    res = (torch.randn(cfg.T, cfg.D, generator=g) * 0.5).to(torch.bfloat16)
+    gamma = (1.0 + 0.2 * torch.randn(cfg.D, generator=g)).to(torch.bfloat16)
+    res_d = res.cuda()
+    res_out = torch.empty_like(res_d)
+    out = run.layer.forward(x, logits, residual=res_d, gamma=gamma.cuda(),
+                            eps=1e-6, residual_out=res_out)
+    st, bits = binding.moe_device_status()
+    assert st == 0, bits
+    ref = oracle.add_rmsnorm_ref(x.float().cpu().numpy(), res.float().numpy(),
+                                 gamma.float().numpy(), 1e-6)
+    assert np.array_equal(res_out.float().cpu().numpy(), ref[0])
+    assert torch.equal(res_d.cpu(), res)             # residual itself untouched
+    ln = logits.cpu().numpy()
+    rid, _ = oracle.route_ref(ln, cfg.k, cfg.renormalize)
+    touched = sorted(set(int(e) for e in rid.ravel()))
+    if cfg.shared:
+        touched.append(cfg.E)
+    qmap = run.expert_weights(touched)
+    wg = run.layer.shared_gate_w.float().cpu().numpy() if cfg.shared else None
+    r = oracle.moe_forward_ref(ref[1], cfg.k, lambda e: qmap[e], cfg.E, logits=ln,
+                               w_g=wg, renormalize=cfg.renormalize)
+    ok, max_rel, l1 = layer_tolerance_ok(out.float().cpu().numpy(), r["out64"])
+    assert ok, f"{cfg.name}: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
+
+
 def test_forward_is_deterministic():
     cfg = syn.LayerConfig("det", 2000, 512, 32, 4, 256, True, "normal")
     run = _Run(cfg)

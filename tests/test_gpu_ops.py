@@ -135,6 +135,59 @@ def test_quant_scatter_with_extra_rows():
     assert np.array_equal(s[R:], rs)
 
 
+@pytest.mark.parametrize("T,D,k,shared,inplace,wide", [
+    (1, 256, 1, False, False, False), (37, 512, 4, True, False, False),
+    (300, 4096, 8, False, True, False), (64, 7168, 2, True, True, False),
+    (200, 2048, 2, False, False, True)])
+def test_add_rmsnorm_quant(T, D, k, shared, inplace, wide):
+    """Fused add + RMSNorm + quant against the oracle: the new residual, the
+    codes at every destination row and the scales bit for bit, the gate
+    within its fp32 evaluation bound. `wide`: a tenth of the entries are
+    scaled by 2^-20, and a few rows are all zero or hold one nonzero entry."""
+    rng = np.random.default_rng(T * 7 + D + k)
+    bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    xa = rng.standard_normal((T, D))
+    if wide:
+        xa[rng.random((T, D)) < 0.1] *= 2.0 ** -20
+        xa[0] = 0.0
+        xa[1] = 0.0
+        xa[1, 5] = 3.0
+    x = bf(xa)
+    ra = rng.standard_normal((T, D)) * 0.5
+    if wide:
+        ra[0] = 0.0
+        ra[1] = 0.0
+    res = bf(ra)
+    gamma = bf(1.0 + 0.2 * rng.standard_normal(D))
+    wg = bf(rng.standard_normal(D) * 0.02) if shared else None
+    R = T * k
+    f2s = rng.permutation(R).astype(np.int32)
+    res_d = res.cuda()
+    out_rows = R + (T if shared else 0)
+    r_out, q, sc, gate = B().moe_add_rmsnorm_quant(
+        x.cuda(), res_d, gamma.cuda(), 1e-6, dst_rows=cuda(f2s), copies=k,
+        extra_row_base=R if shared else -1, out_rows=out_rows,
+        residual_out=res_d if inplace else None,
+        gate_w=wg.cuda() if shared else None)
+    ref = oracle.add_rmsnorm_quant_ref(x.float().numpy(), res.float().numpy(),
+                                       gamma.float().numpy(), 1e-6,
+                                       w_g=wg.float().numpy() if shared else None)
+    assert np.array_equal(r_out.float().cpu().numpy(), ref["r"])
+    q = q.cpu().numpy()
+    sc = sc.cpu().numpy()
+    for f in range(R):
+        assert np.array_equal(q[f2s[f]], ref["codes"][f // k]), f
+        assert sc[f2s[f]].view(np.uint32) == ref["scales"][f // k].view(np.uint32)
+    if shared:
+        assert np.array_equal(q[R:], ref["codes"])
+        assert np.array_equal(sc[R:].view(np.uint32), ref["scales"].view(np.uint32))
+        v = ref["v"].astype(np.float64)
+        absdot = np.abs(v) @ np.abs(wg.float().numpy().astype(np.float64))
+        g = ref["gate"]
+        bound = D * U32 * absdot * g * (1 - g) + 8 * U32
+        assert np.all(np.abs(gate.cpu().numpy() - g) <= bound)
+
+
 def test_shared_gate():
     rng = np.random.default_rng(4)
     x = torch.from_numpy(rng.standard_normal((70, 2048)).astype(np.float32)).to(
