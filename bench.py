@@ -57,7 +57,8 @@ def workload_config(name):
 
 def describe(cfg):
     s = (f"{cfg.name}: T={cfg.T} D={cfg.D} E={cfg.E} top-{cfg.k} I={cfg.I}"
-         f"{' + shared expert' if cfg.shared else ''}, PTPC FP8 e4m3")
+         f"{' + shared expert' if cfg.shared else ''}, PTPC FP8 e4m3"
+         f"{', bf16 router GEMM' if cfg.router == 'weights' else ''}")
     return s
 
 
@@ -180,12 +181,16 @@ def physical_gpu(local_rank):
 def kernel_launches_per_step(cfg):
     R = cfg.T * cfg.k
     permute = 1 if R <= 8192 else 3
-    router = 1 if cfg.router == "weights" else 0
+    # routing: one kernel (route) from given logits; from router weights the
+    # fused router GEMM + top-k where it applies, else router GEMM + route
+    fused = (cfg.E <= 512 and cfg.k <= 16 and cfg.D % 64 == 0 and
+             cfg.T * cfg.E * cfg.D >= (1 << 20))
+    routing = 2 if cfg.router == "weights" and not fused else 1
     # the down weights' scale bound, when y takes the fp16 encoding (its fp32
     # size reaches 32 MiB)
     bound = 1 if cfg.rows * cfg.D * 4 >= (32 << 20) else 0
-    # router, route, permute, quant, gate/up GEMM, requant, down GEMM, combine
-    return bound + router + 1 + permute + 1 + 1 + 1 + 1 + 1
+    # routing, permute, quant, gate/up GEMM, requant, down GEMM, combine
+    return bound + routing + permute + 1 + 1 + 1 + 1 + 1
 
 
 def algorithmic_bytes(cfg, counts):
@@ -208,7 +213,8 @@ def gateup_bytes(cfg, touched):
 
 
 def layer_flops(cfg):
-    return 2.0 * cfg.rows * cfg.D * 2 * cfg.I + 2.0 * cfg.rows * cfg.I * cfg.D
+    router = 2.0 * cfg.T * cfg.D * cfg.E if cfg.router == "weights" else 0.0
+    return 2.0 * cfg.rows * cfg.D * 2 * cfg.I + 2.0 * cfg.rows * cfg.I * cfg.D + router
 
 
 # ---------------------------------------------------------------------------
@@ -626,6 +632,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router-gemm", action="store_true",
+                    help="route every workload from a bf16 router matrix: the "
+                         "fused tensor-core router GEMM + top-k is in the step")
     ap.add_argument("--prenorm", action="store_true",
                     help="feed the layer from the residual stream: fused add + "
                          "RMSNorm + quant replaces the quantisation step")
@@ -639,6 +648,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = workload_config(args.workload)
+    if args.router_gemm and cfg.router != "weights":
+        # route from a bf16 router matrix (N(0, 0.02)) through the layer's
+        # fused router GEMM + top-k instead of the workload's given logits
+        from dataclasses import replace
+        cfg = replace(cfg, router="weights")
 
     if args.impl == "reference":
         if rank == 0:

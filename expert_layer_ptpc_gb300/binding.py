@@ -69,6 +69,7 @@ _SIGNATURES = {
                                   ctypes.POINTER(ctypes.c_void_p), _I, _P]),
     "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "moe_debug_expire_wait": (_I, [_I, _P]),
+    "moe_router_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_add_rmsnorm_quant": (_I, [_P, _P, _P, ctypes.c_float, _I64, _I, _P, _P, _I,
                                    _I64, _P, _P, _P, _P, _P]),
     "moe_forward_prenorm": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -385,6 +386,24 @@ def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,
         _check("moe_forward_profiled", lib.moe_forward_profiled(
             *args, handles, MOE_FORWARD_EVENTS, _stream(stream)))
     return out
+
+
+def moe_router_topk(x, w_r, k, renormalize=True, ids=None, weights=None,
+                    logits=None, stream=None):
+    """Router GEMM + top-k + softmax in one kernel; returns (ids, weights).
+    `logits`: optional [T, E] fp32 tensor that receives the GEMM result."""
+    _need(x, torch.bfloat16, "x")
+    _need(w_r, torch.bfloat16, "w_r")
+    T, D = x.shape
+    E = w_r.shape[0]
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    _check("moe_router_topk", load_library().moe_router_topk(
+        _ptr(x), _ptr(w_r), T, D, E, k, int(bool(renormalize)), _ptr(ids),
+        _ptr(weights), _ptr(logits), _stream(stream)))
+    return ids, weights
 
 
 def moe_add_rmsnorm_quant(x, residual, gamma, eps=1e-6, dst_rows=None, copies=1,

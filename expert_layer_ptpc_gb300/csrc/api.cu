@@ -361,7 +361,19 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
     first = false;
   }
   const float* logits = router_logits;
-  if (router_w != nullptr) {
+  // router weights: the tensor-core router with the top-k in its epilogue
+  // where it applies and the projection has at least 2^20 multiply-adds;
+  // below that (launch latency dominates) and for unsupported shapes, the
+  // exactly rounded router GEMM and the route kernel
+  const bool fused_router =
+      router_w != nullptr && router_topk_supported(d.E, d.k, d.D) &&
+      (int64_t)d.T * d.E * d.D >= (int64_t(1) << 20);
+  if (fused_router) {
+    st = launch_router_topk(x, router_w, d.T, d.D, d.E, d.k, d.renormalize ? 1 : 0,
+                            ids, tw, nullptr, stream, pdl && !first);
+    if (st != MOE_OK) return st;
+    first = false;
+  } else if (router_w != nullptr) {
     auto* lg = static_cast<float*>(at(L.logits));
     st = cuda_status(
         launch_router_logits(x, router_w, d.T, d.E, d.D, lg, stream, pdl && !first));
@@ -370,9 +382,11 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
     first = false;
   }
   mark(1);
-  st = cuda_status(launch_route(logits, d.T, d.E, d.k, d.renormalize ? 1 : 0, ids,
-                                tw, stream, pdl && !first));
-  if (st != MOE_OK) return st;
+  if (!fused_router) {
+    st = cuda_status(launch_route(logits, d.T, d.E, d.k, d.renormalize ? 1 : 0, ids,
+                                  tw, stream, pdl && !first));
+    if (st != MOE_OK) return st;
+  }
   mark(2);
   st = cuda_status(launch_permute(ids, R, d.E, counts, offsets, s2f, f2s,
                                   d.shared ? d.T : -1, at(L.perm), stream, pdl));
@@ -455,6 +469,18 @@ int moe_forward_prenorm(const moe_dims* dims, const moe_prenorm* pre,
   return forward_impl(dims, pre, x, router_logits, nullptr, w_gu, s_gu, w_d, s_d,
                       shared_gate_w, out, topk_ids_out, topk_w_out, ws, ws_bytes,
                       reinterpret_cast<cudaEvent_t const*>(events), stream);
+}
+
+int moe_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int E,
+                    int k, int renormalize, int32_t* topk_ids, float* topk_w,
+                    float* logits_out, moe_stream_t stream) {
+  if (T < 0 || D <= 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (!router_topk_supported(E, k, D)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_r || !topk_ids || !topk_w || !aligned16(x) || !aligned16(w_r))
+    return MOE_ERR_INVALID_ARG;
+  return launch_router_topk(x, w_r, T, D, E, k, renormalize ? 1 : 0, topk_ids, topk_w,
+                            logits_out, stream, false);
 }
 
 int moe_add_rmsnorm_quant(const uint16_t* x, const uint16_t* residual,

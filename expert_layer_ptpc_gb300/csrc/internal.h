@@ -75,6 +75,13 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
                                      float* out_scale, const uint16_t* gate_w,
                                      float* gate_out, cudaStream_t stream, bool pdl);
 
+// Router projection (tcgen05, bf16) with the top-k selection and softmax in
+// its epilogue (router_gemm.cu). Returns a moe_status.
+bool router_topk_supported(int E, int k, int D);
+int launch_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int E,
+                       int k, int renormalize, int32_t* ids, float* weights,
+                       float* logits_out, cudaStream_t stream, bool pdl);
+
 // Largest row length launch_quant handles.
 constexpr int kMaxQuantCols = 32768;
 

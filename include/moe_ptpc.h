@@ -173,6 +173,25 @@ MOE_API int moe_quant_ptpc(const void* in, int in_dtype, int64_t rows, int cols,
                            float* out_scale, moe_stream_t stream);
 
 /*
+ * moe_router_topk - router projection and top-k selection in one kernel (TPU
+ * page, closing roadmap paragraph: the top-k fused with the router matmul).
+ *   logits[t, e] = sum_d x[t, d] * w_r[e, d] on the tensor cores (bf16
+ *   operands, fp32 accumulation; the accumulation order is the hardware's,
+ *   so the logits are the fp32 GEMM result, not moe_router_logits' exactly
+ *   rounded ones); then, per token, the selection and weights of moe_route
+ *   on those logits: the k largest in decreasing order, equal values to the
+ *   lower expert index; softmax over the chosen k (renormalize) or over all E.
+ *   x [T, D] bf16, w_r [E, D] bf16; topk_ids [T, k] int32 and topk_w [T, k]
+ *   fp32 written; logits_out [T, E] fp32 written when not NULL (testing).
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned pointers, k > E),
+ *         MOE_ERR_UNSUPPORTED (E > 512, k > 16 or D not a multiple of 64;
+ *         moe_router_logits + moe_route cover those).
+ */
+MOE_API int moe_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D,
+                            int E, int k, int renormalize, int32_t* topk_ids,
+                            float* topk_w, float* logits_out, moe_stream_t stream);
+
+/*
  * moe_add_rmsnorm_quant - the MoE block's FP8 input straight from the
  * residual stream: add + RMSNorm + per-token quantisation in one pass (MI300X
  * page, section 2.1.5, the fusion table; the AllReduce of that operator needs
@@ -302,7 +321,10 @@ MOE_API int moe_combine_f16(const uint16_t* y16, const float* row_scale,
 /*
  * moe_forward - the whole layer, every step above chained on `stream`.
  *   x [T, D] bf16. Router input: exactly one of router_logits [T, E] fp32 and
- *   router_w [E, D] bf16 (then the logits are computed by moe_router_logits).
+ *   router_w [E, D] bf16. With router_w the routing is moe_router_topk's
+ *   (tensor-core logits, top-k fused) where that op applies (E <= 512,
+ *   k <= 16, D a multiple of 64) and T * E * D >= 2^20; otherwise
+ *   moe_router_logits + moe_route (exactly rounded logits).
  *   Weights, pre-quantised per output channel with moe_quant_ptpc:
  *     w_gu [G, 2I, D] e4m3, s_gu [G, 2I];  w_d [G, D, I] e4m3, s_d [G, D],
  *   where G = E + dims->shared and group E is the shared expert.

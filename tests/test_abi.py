@@ -70,6 +70,13 @@ def test_argument_errors_need_no_gpu(lib):
     fake16 = ctypes.c_void_p(0x1000)
     assert lib.moe_combine_f16(fake16, fake16, fake16, fake16, 4, 2, 256, fake16,
                                None, None, fake16, None) == -1    # partial shared set
+    # the fused router: E > 512, k > 16 or D % 64 go to the unfused ops
+    assert lib.moe_router_topk(None, None, 4, 4096, 1024, 8, 1, None, None, None,
+                               None) == -2
+    assert lib.moe_router_topk(None, None, 4, 4096, 128, 17, 1, None, None, None,
+                               None) == -2
+    assert lib.moe_router_topk(None, None, 4, 4096, 8, 9, 1, None, None, None,
+                               None) == -1                       # k > E
     # the failure-detection check validates its limit before touching CUDA
     assert lib.moe_debug_expire_wait(0, None) == -1
     assert lib.moe_debug_expire_wait(2000000, None) == -1

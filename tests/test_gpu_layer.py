@@ -16,8 +16,8 @@ import torch
 
 import oracle
 from expert_layer_ptpc_gb300 import synthetic as syn
-from tests.gpu_helpers import (U32, ensure_library, layer_tolerance_ok,
-                               quantize_experts, require_gpu)
+from tests.gpu_helpers import (U32, ensure_library, gemm_bound,
+                               layer_tolerance_ok, quantize_experts, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -73,21 +73,47 @@ class _Run:
         assert st == 0, f"device status {st} bits {bits:#x}"
 
         xn = x.float().cpu().numpy()
+        w_rtol = 64 * U32
+        amb = np.zeros(T, bool)
         if logits is None:
-            ln = oracle.router_logits_ref(
-                xn, self.layer.router_w.float().cpu().numpy())
+            wr = self.layer.router_w.float().cpu().numpy()
+            ln = oracle.router_logits_ref(xn, wr)
+            if T * E * cfg.D >= (1 << 20):
+                # the layer routes on tensor-core fp32 logits, within the
+                # fp32 accumulation bound of these exact ones. A token whose
+                # top k (or its order) has a gap within twice that bound has
+                # more than one correct selection: its ids must then be a
+                # valid choice, and its output is not compared.
+                bound = gemm_bound(np.abs(xn.astype(np.float64)) @
+                                   np.abs(wr.astype(np.float64)).T, cfg.D)
+                bt = 2 * bound.max(axis=1)
+                srt = -np.sort(-ln.astype(np.float64), axis=1)[:, :min(k + 1, E)]
+                amb = ((srt[:, :-1] - srt[:, 1:]) <= bt[:, None]).any(axis=1)
+                # the bound is the worst case (every partial sum rounding the
+                # same way), so a few percent of the seeded tokens fall in it
+                assert amb.mean() < 0.15, f"{amb.sum()} of {T} tokens near a tie"
+                w_rtol += 4 * float(bound.max())
+                exact = xn.astype(np.float64) @ wr.astype(np.float64).T
+                gid = ids.cpu().numpy()
+                for t in np.flatnonzero(amb):
+                    ch = np.zeros(E, bool)
+                    ch[gid[t]] = True
+                    if not ch.all():
+                        assert exact[t, ch].min() >= exact[t, ~ch].max() - bt[t]
         else:
             ln = logits.cpu().numpy()
         rid, rw = oracle.route_ref(ln, k, cfg.renormalize)
-        assert np.array_equal(ids.cpu().numpy(), rid)
-        np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=64 * U32, atol=0)
-        # permutation of the same ids, full size, bit-exact
-        counts, offs, s2f, f2s = binding.moe_permute(ids, E)
-        rc, ro, rs, rf = oracle.permute_ref(rid, E)
-        assert np.array_equal(counts.cpu().numpy(), rc)
-        assert np.array_equal(offs.cpu().numpy(), ro)
-        assert np.array_equal(s2f.cpu().numpy(), rs)
-        assert np.array_equal(f2s.cpu().numpy(), rf)
+        ok_t = ~amb
+        assert np.array_equal(ids.cpu().numpy()[ok_t], rid[ok_t])
+        np.testing.assert_allclose(tw.cpu().numpy()[ok_t], rw[ok_t], rtol=w_rtol, atol=0)
+        if not amb.any():
+            # permutation of the same ids, full size, bit-exact
+            counts, offs, s2f, f2s = binding.moe_permute(ids, E)
+            rc, ro, rs, rf = oracle.permute_ref(rid, E)
+            assert np.array_equal(counts.cpu().numpy(), rc)
+            assert np.array_equal(offs.cpu().numpy(), ro)
+            assert np.array_equal(s2f.cpu().numpy(), rs)
+            assert np.array_equal(f2s.cpu().numpy(), rf)
 
         if n_sample is None or n_sample >= T:
             tokens = np.arange(T)
@@ -96,6 +122,7 @@ class _Run:
             tokens = np.sort(rng.choice(T, n_sample, replace=False))
             tokens[0] = 0
             tokens[-1] = T - 1            # first and last token always
+        tokens = tokens[ok_t[tokens]]     # unique routing only
         touched = sorted(set(int(e) for e in rid[tokens].ravel()))
         if cfg.shared:
             touched.append(E)
@@ -123,6 +150,8 @@ class _Run:
     syn.LayerConfig("s6", 40, 256, 12, 2, 128, True, "weights"),
     # rows x D x 4 bytes >= 32 MiB: the expert output takes the fp16 encoding
     syn.LayerConfig("s7", 1024, 1024, 16, 8, 256, True, "normal"),
+    # T x E x D >= 2^20 with router weights: the fused tensor-core router
+    syn.LayerConfig("s8", 256, 1024, 16, 4, 256, True, "weights"),
 ], ids=lambda c: c.name)
 def test_small_layer_all_tokens(cfg):
     _Run(cfg).check(cfg)

@@ -135,6 +135,39 @@ def test_quant_scatter_with_extra_rows():
     assert np.array_equal(s[R:], rs)
 
 
+@pytest.mark.parametrize("T,D,E,k,renorm", [
+    (64, 256, 8, 2, True), (300, 4096, 128, 8, True), (1000, 2048, 256, 8, True),
+    (129, 4096, 512, 10, False), (17, 1024, 40, 3, True), (5, 4096, 300, 16, True)])
+def test_router_topk(T, D, E, k, renorm):
+    """Router GEMM + top-k in one kernel. The logits (fp32 GEMM) lie within
+    the fp32 accumulation bound of the exact dot products; the selection and
+    weights are moe_route's on exactly those logits (ids bit for bit); and the
+    chosen set is valid for the exact logits within twice that bound."""
+    rng = np.random.default_rng(T + D + E + k)
+    bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    x = bf(rng.standard_normal((T, D)))
+    w = bf(rng.standard_normal((E, D)) * 0.02)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ids, wts = B().moe_router_topk(x.cuda(), w.cuda(), k, renorm, logits=logits)
+    assert B().moe_device_status() == (0, 0)
+    xd, wd = x.double().numpy(), w.double().numpy()
+    exact = xd @ wd.T
+    bound = gemm_bound(np.abs(xd) @ np.abs(wd).T, D)
+    got_l = logits.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got_l - exact) <= bound)
+    rid, rw = oracle.route_ref(logits.cpu().numpy(), k, renorm)
+    ids = ids.cpu().numpy()
+    assert np.array_equal(ids, rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    for t in range(T):
+        chosen = np.zeros(E, bool)
+        chosen[ids[t]] = True
+        if chosen.all():
+            continue
+        tol = 2 * bound[t].max()
+        assert exact[t, chosen].min() >= exact[t, ~chosen].max() - tol
+
+
 @pytest.mark.parametrize("T,D,k,shared,inplace,wide", [
     (1, 256, 1, False, False, False), (37, 512, 4, True, False, False),
     (300, 4096, 8, False, True, False), (64, 7168, 2, True, True, False),
