@@ -21,17 +21,20 @@
 // the logits here are the fp32 GEMM result, not moe_router_logits' exactly
 // rounded ones. The selection on them is exact.
 //
-// Roles: warp 0 allocates TMEM and issues the MMAs (one thread); warps 4..
-// are TMA producers, one per box of a stage (the token box and the router
-// matrix in boxes of up to 128 rows: a single issuing thread caps an SM's
-// feed far below the MMA rate); warps 0-3 run the epilogue (warp w reads TMEM
-// lanes 32w..32w+31). Every wait is bounded.
+// Roles: warp 0 allocates TMEM and issues the MMAs (one thread); warps 4-7
+// are TMA producers, which split the boxes of every stage between them (the
+// token rows and the router matrix, in boxes of at most kRBoxRows rows: a
+// single issuing thread caps an SM's feed far below the MMA rate); warps 0-3
+// read the accumulators (warp w reads TMEM lanes 32w..32w+31). Every wait is
+// bounded.
 //
-// A batch of at most 64 tokens is one tile, which one SM would stream the
-// whole router matrix for. There, a cluster of C CTAs splits K: each CTA
-// accumulates its D/C slice, parks its partial logits in shared memory, and
-// the cluster's first CTA sums the C partials in rank order (distributed
-// shared memory) before the selection.
+// The projection streams T x D activations and E x D router weights through
+// few tiles, so a grid of one CTA per 128 tokens leaves most SMs idle. A
+// cluster of C CTAs therefore splits K: each CTA accumulates its D/C slice,
+// parks its partial logits in shared memory, and each rank sums the C
+// partials of its own share of the tile's rows in rank order (a fixed
+// summation order, over distributed shared memory) and selects on them, one
+// warp per token.
 #include <math.h>
 
 #include "gemm_common.cuh"
@@ -42,13 +45,15 @@ namespace {
 using namespace gemm;
 
 constexpr int kRProd0 = 4;               // first producer warp
-constexpr int kRBBoxRows = 128;          // router-matrix rows per TMA box
-constexpr int kRMaxBoxes = 1 + 512 / kRBBoxRows;
-constexpr int kRThreads = 32 * (kRProd0 + kRMaxBoxes);
+constexpr int kRProds = 4;               // producer warps
+constexpr int kRThreads = 32 * (kRProd0 + kRProds);
+constexpr int kRWarps = kRThreads / 32;
+constexpr int kRBoxRows = 64;            // rows per TMA box (tokens and router matrix)
 constexpr int kRBK = 64;                 // bf16 elements of K per stage (128 bytes)
-constexpr int kRTile = 128;              // tokens per CTA (MMA M)
+constexpr int kRTile = 128;              // tokens per tile (MMA M)
 constexpr int kRMaxN = 512;              // expert columns (two N = 256 MMAs)
 constexpr int kRMaxK = 16;               // top-k kept in registers (KT <= 16)
+constexpr int kRMaxCluster = 16;
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B, fp32
 // accumulator, both K-major: bits 4-5 D format (1 = f32), 7-9 A format and
@@ -58,13 +63,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// (not volatile: independent loads may overlap; the cluster barriers order
-// them against the stores)
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ void cluster_barrier() {
   __syncwarp();
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -81,21 +79,103 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
-// n_pad: expert columns, E rounded up to a multiple of 16 up to 256, else
-// 512 (two full N = 256 MMAs); stages of 128 token rows + n_pad expert rows
-// of 128 bytes each (rows past E read as zero and are never selected).
+// An unsigned key with the order of the fp32 values (-0 and +0 equal).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (not volatile: independent loads may overlap; the cluster barriers order
+// them against the stores)
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "r"(addr));
+  return v;
+}
+
+// One token's top k over row[0..E) by one warp: lane holds the keys of the
+// experts lane + 32 i (i < NI) in registers; k rounds of a warp argmax (a
+// max of the keys, then the lowest expert index holding it: larger value
+// first, equal values to the lower index, the selection rule of route.cu),
+// then the softmax weights.
+template <int NI>
+__device__ __forceinline__ void select_warp(const float* row, int E, int k,
+                                            int renormalize, int64_t tok,
+                                            int32_t* __restrict__ ids,
+                                            float* __restrict__ weights,
+                                            float* __restrict__ logits_out) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    const float v = e < E ? row[e] : 0.f;
+    key[i] = e < E ? order_key(v) : 0u;   // 0: below every value, never chosen
+    if (logits_out != nullptr && e < E) logits_out[tok * E + e] = v;
+  }
+  int my_idx = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      if (key[i] > bk) {
+        bk = key[i];
+        bi = lane + 32 * i;
+      }
+    }
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)bi : 0xffffffffu);
+    if ((int)(wi & 31u) == lane) {
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (i == (int)(wi >> 5)) key[i] = 0u;
+    }
+    if (j == lane) my_idx = (int)wi;
+  }
+  const float my_val = lane < k ? row[my_idx] : 0.f;
+  const float top = __shfl_sync(0xffffffffu, my_val, 0);
+  float den;
+  if (renormalize) {
+    den = warp_sum(lane < k ? expf(my_val - top) : 0.f);
+  } else {
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) s += expf(row[e] - top);
+    den = warp_sum(s);
+  }
+  if (lane < k) {
+    ids[tok * k + lane] = my_idx;
+    weights[tok * k + lane] = expf(my_val - top) / den;
+  }
+}
+
+// Launch geometry, fixed on the host.
+struct RouterGeom {
+  int n_pad;      // expert columns: E rounded up to 16 up to 256, else 512
+  int stages;
+  int csplit;     // CTAs of a cluster splitting K (1: no split)
+  int chunk;      // expert columns exchanged per round of the split reduction
+  int xbox, nxb;  // token box rows and token boxes per stage
+  int wbox, nwb;  // router-matrix box rows and boxes per stage
+};
+
+// A stage: 128 token rows (the MMA's A; rows past those loaded are never
+// read back) + n_pad expert rows, 128 bytes each (rows past E read as zero
+// and are never selected).
 template <int KT>   // capacity of the running top-k, >= k
 __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-    int T, int D, int E, int n_pad, int k, int renormalize, int stages, int csplit,
+    int T, int D, int E, int k, int renormalize, const RouterGeom g,
     int32_t* __restrict__ ids, float* __restrict__ weights,
     float* __restrict__ logits_out, unsigned* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int n_pad = g.n_pad, stages = g.stages, csplit = g.csplit;
   const int a_bytes = kRTile * 128;
-  const int b_bytes = n_pad * 128;
-  const int stage_bytes = a_bytes + b_bytes;
+  const int stage_bytes = a_bytes + n_pad * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -107,12 +187,14 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
   const int tile0 = (int)(blockIdx.x / csplit) * kRTile;
   const int kpc = D / kRBK / csplit;            // K blocks of this CTA's slice
   const int kb0 = (int)rank * kpc;
+  const int nbox = g.nxb + g.nwb;
+  const int nprod = nbox < kRProds ? nbox : kRProds;
   const uint32_t tmem_cols = n_pad <= 32 ? 32 : n_pad <= 64 ? 64 : n_pad <= 128 ? 128
                              : n_pad <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(full_bar(s), 1 + (n_pad + kRBBoxRows - 1) / kRBBoxRows);   // boxes
+      mbar_init(full_bar(s), (uint32_t)nprod);   // one arrival per producer
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(acc_bar, 1);
@@ -127,40 +209,42 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
   pdl_wait();
   pdl_launch_dependents();
 
-  const int box = warp - kRProd0;        // 0: tokens; 1..: router-matrix rows
-  const int nboxes = 1 + (n_pad + kRBBoxRows - 1) / kRBBoxRows;
-  if (box >= 0 && box < nboxes && lane == 0) {
-    // ---------------- TMA producers: box `box` of every stage ----------------
-    const uint64_t pol = l2_policy_evict_last();   // W_r is read by every CTA
-    const int brow = (box - 1) * kRBBoxRows;
-    const uint32_t bytes =
-        box == 0 ? (uint32_t)a_bytes
-                 : (uint32_t)(min(kRBBoxRows, n_pad - brow) * 128);
+  const int prod = warp - kRProd0;
+  if (prod >= 0 && prod < nprod && lane == 0) {
+    // ---------------- TMA producers: boxes prod, prod + nprod, ... ----------------
+    // W_r is read by every CTA; x again by the quantiser that follows
+    const uint64_t pol = l2_policy_evict_last();
+    uint32_t bytes = 0;
+    for (int b = prod; b < nbox; b += nprod)
+      bytes += (uint32_t)((b < g.nxb ? g.xbox : g.wbox) * 128);
     int s = 0;
     uint32_t ph = 0;
-    int last_phase[8];
-    for (int i = 0; i < 8; ++i) last_phase[i] = -1;
+    int issued = 0;
     for (int kb = kb0; kb < kb0 + kpc; ++kb) {
       if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, err, kErrTimeoutProducer))
         break;
       mbar_arrive_expect_tx(full_bar(s), bytes);
       const uint32_t st = smem_u32(smem + s * stage_bytes);
-      if (box == 0)
-        tma_load_2d(st, &tm_x, kb * kRBK, tile0, full_bar(s), pol);
-      else
-        tma_load_2d(st + a_bytes + brow * 128, &tm_w, kb * kRBK, brow, full_bar(s), pol);
-      last_phase[s] = (int)ph;
+      for (int b = prod; b < nbox; b += nprod) {
+        if (b < g.nxb) {
+          const int r = b * g.xbox;
+          tma_load_2d(st + r * 128, &tm_x, kb * kRBK, tile0 + r, full_bar(s), pol);
+        } else {
+          const int r = (b - g.nxb) * g.wbox;
+          tma_load_2d(st + a_bytes + r * 128, &tm_w, kb * kRBK, r, full_bar(s), pol);
+        }
+      }
+      ++issued;
       if (++s == stages) {
         s = 0;
         ph ^= 1u;
       }
     }
-    for (int i = 0; i < stages; ++i) {   // every copy landed before exit
-      if (last_phase[i] >= 0) {
-        volatile int no_abort = 0;
-        mbar_wait_bounded(full_bar(i), (uint32_t)last_phase[i], &no_abort, err,
-                          kErrTimeoutDrain);
-      }
+    for (int i = 0; i < stages && i < issued; ++i) {   // every copy landed before exit
+      const int last = i + (issued - 1 - i) / stages * stages;   // last use of stage i
+      volatile int no_abort = 0;
+      mbar_wait_bounded(full_bar(i), (uint32_t)((last / stages) & 1), &no_abort, err,
+                        kErrTimeoutDrain);
     }
   } else if (warp == 0 && lane == 0) {
     // ---------------- MMA issuer ----------------
@@ -188,123 +272,105 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
     mma_commit(acc_bar);   // also completes (with no result) after an abort
   }
 
-  // ---------------- epilogue (warps 0-3): thread = token ----------------
+  // ---------------- epilogue ----------------
   __syncwarp();
   const bool epi = warp < 4;
   const bool have = epi && warp_wait(acc_bar, 0, abort_flag, err, kErrTimeoutEpilogue);
   tc_fence_after_sync();
   const int lrow = warp * 32 + lane;
-  const int t = tile0 + lrow;
-  const uint32_t trow = tmem_base + ((uint32_t)(warp * 32) << 16);
-  float vals[KT];
-  int idx[KT];
-#pragma unroll
-  for (int i = 0; i < KT; ++i) {
-    vals[i] = -INFINITY;
-    idx[i] = 0x7fffffff;
-  }
-  float m = -INFINITY, ssum = 0.f;   // online softmax over all experts
-  bool scanned = false;
-  const int ldp = n_pad + 1;
-  float* part = reinterpret_cast<float*>(smem);
-  const bool row_ok = t < T;
+  const int rows_t = min(T - tile0, kRTile);   // token rows of this tile
+  const uint32_t trow = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
   if (csplit > 1) {
-    // partial logits of this K slice -> shared memory (the stages are free:
-    // every copy and MMA has completed), [row][n_pad + 1] fp32
-    if (epi) {
-      for (int c0 = 0; c0 < n_pad; c0 += 16) {
-        float l[16];
-        tmem_ld_x16(trow + (uint32_t)c0, l);
-        tmem_ld_wait();
-        if (row_ok) {
+    // The stages are free (every copy and MMA has completed). part: this
+    // CTA's partial logits of `chunk` columns, [rows_t][chunk + 4] fp32;
+    // fin: the summed logits of this rank's rows, [own][n_pad + 4] (rows of
+    // 16-byte multiples: vector accesses; the +4 keeps the row-per-lane
+    // stores free of bank conflicts).
+    const int cc = g.chunk;
+    const int per = (rows_t + csplit - 1) / csplit;
+    const int own0 = (int)rank * per;
+    const int own = max(0, min(per, rows_t - own0));
+    const int ldp = cc + 4, ldf = n_pad + 4;
+    float* part = reinterpret_cast<float*>(smem);
+    float* fin = part + rows_t * ldp;
+    const int c4n = cc / 4;
+    const int items = own * c4n;   // (row, 4 columns) of this rank's rows
+    constexpr int kU = 4;          // items in flight per thread
+    for (int h = 0; h < n_pad; h += cc) {
+      if (epi) {
+        for (int c0 = 0; c0 < cc; c0 += 16) {
+          float l[16];
+          tmem_ld_x16(trow + (uint32_t)(h + c0), l);
+          tmem_ld_wait();
+          if (lrow < rows_t) {
+            float4* dst = reinterpret_cast<float4*>(part + lrow * ldp + c0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) part[lrow * ldp + c0 + j] = have ? l[j] : 0.f;
+            for (int q = 0; q < 4; ++q)
+              dst[q] = have ? make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3])
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
       }
-    }
-    cluster_barrier();   // every CTA's partials are in place
-    // CTA r sums its slice of the columns over the ranks (in rank order, a
-    // fixed summation order) into the first CTA's buffer
-    if (epi) {   // (row, column) pairs of this CTA's slice over the 128 threads
-      const int cs = n_pad / csplit;
-      const int rows = min(T - tile0, kRTile);
-      for (int p = lrow; p < rows * cs; p += 128) {
-        const int r0 = p / cs, c = (int)rank * cs + p % cs;
-        const uint32_t src = smem_u32(part + r0 * ldp + c);
-        float acc = 0.f;
-        for (int r = 0; r < csplit; ++r) acc += ld_cluster_f32(map_to_rank(src, (uint32_t)r));
-        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(map_to_rank(src, 0)), "f"(acc)
-                     : "memory");
-      }
-    }
-    cluster_barrier();   // the sums are in place; peers' memory no longer read
-    if (epi && rank == 0) {
-      // a warp per token (few tokens here): lanes hold strided experts; k
-      // rounds of a warp argmax, larger value first, equal values to the
-      // lower index (route.cu's rule)
-      const int rows = min(T - tile0, kRTile);
-      for (int r0 = warp; r0 < rows; r0 += 4) {
-        const float* row = part + r0 * ldp;
-        const int tok = tile0 + r0;
-        if (logits_out != nullptr)
-          for (int e = lane; e < E; e += 32) logits_out[(int64_t)tok * E + e] = row[e];
-        uint32_t taken = 0;   // bit i: expert lane + 32 i chosen
-        float my_val = -INFINITY;
-        int my_idx = 0;
-        for (int j = 0; j < k; ++j) {
-          float bv = -INFINITY;
-          int bi = 0x7fffffff;
-          for (int i = 0; lane + 32 * i < E; ++i) {
-            const float v = row[lane + 32 * i];
-            if (!((taken >> i) & 1u) && (v > bv || bi == 0x7fffffff)) {
-              bv = v;
-              bi = lane + 32 * i;
-            }
-          }
+      cluster_barrier();   // every CTA's partials of this chunk are in place
+      for (int p0 = threadIdx.x; p0 < items; p0 += kU * kRThreads) {
+        float4 acc[kU];
+        uint32_t src[kU];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-              bv = ov;
-              bi = oi;
-            }
-          }
-          if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-          if (j == lane) {
-            my_val = bv;
-            my_idx = bi;
+        for (int u = 0; u < kU; ++u) {
+          const int p = min(p0 + u * kRThreads, items - 1);
+          src[u] = smem_u32(part + (own0 + p / c4n) * ldp + 4 * (p % c4n));
+          acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 4
+        for (int r = 0; r < csplit; ++r) {   // rank order: a fixed summation order
+          float4 v[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u) v[u] = ld_cluster_v4(map_to_rank(src[u], (uint32_t)r));
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            acc[u].x += v[u].x;
+            acc[u].y += v[u].y;
+            acc[u].z += v[u].z;
+            acc[u].w += v[u].w;
           }
         }
-        const float top = __shfl_sync(0xffffffffu, my_val, 0);
-        float den = 0.f;
-        if (renormalize) {
-          den = warp_sum(lane < k ? expf(my_val - top) : 0.f);
-        } else {
-          float s = 0.f;
-          for (int e = lane; e < E; e += 32) s += expf(row[e] - top);
-          den = warp_sum(s);
-        }
-        if (lane < k) {
-          ids[(int64_t)tok * k + lane] = my_idx;
-          weights[(int64_t)tok * k + lane] = expf(my_val - top) / den;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int p = p0 + u * kRThreads;
+          if (p < items)
+            *reinterpret_cast<float4*>(fin + (p / c4n) * ldf + h + 4 * (p % c4n)) = acc[u];
         }
       }
+      cluster_barrier();   // peers' partials no longer read
     }
-  }
-  // the scan: from TMEM (one CTA per tile) or from the summed partials (the
-  // cluster's first CTA); a running top-k and the softmax sums
-  const bool from_tmem = csplit == 1;
-  if (from_tmem && have) {
+    __syncthreads();
+    for (int q = warp; q < own; q += kRWarps) {
+      const float* row = fin + q * ldf;
+      const int64_t tok = (int64_t)tile0 + own0 + q;
+      if (E <= 128)
+        select_warp<4>(row, E, k, renormalize, tok, ids, weights, logits_out);
+      else if (E <= 256)
+        select_warp<8>(row, E, k, renormalize, tok, ids, weights, logits_out);
+      else
+        select_warp<16>(row, E, k, renormalize, tok, ids, weights, logits_out);
+    }
+  } else if (have) {
+    // thread = token: scan the logits straight out of TMEM with a running
+    // top-k and the softmax sums
+    const int t = tile0 + lrow;
+    const bool row_ok = lrow < rows_t;
+    float vals[KT];
+    int idx[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+      vals[i] = -INFINITY;
+      idx[i] = 0x7fffffff;
+    }
+    float m = -INFINITY, ssum = 0.f;   // online softmax over all experts
     for (int c0 = 0; c0 < n_pad; c0 += 16) {
       float l[16];
-      if (from_tmem) {
-        tmem_ld_x16(trow + (uint32_t)c0, l);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) l[j] = part[lrow * ldp + c0 + j];
-      }
+      tmem_ld_x16(trow + (uint32_t)c0, l);
+      tmem_ld_wait();
       if (row_ok && logits_out != nullptr) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -339,23 +405,22 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
           if (c0 + j < E) ssum += expf(l[j] - m);
       }
     }
-    scanned = true;
-  }
-  if (epi && scanned && t < T) {
-    float denom;
-    if (renormalize) {
-      denom = 0.f;
+    if (row_ok) {
+      float denom;
+      if (renormalize) {
+        denom = 0.f;
 #pragma unroll
-      for (int i = 0; i < KT; ++i)
-        if (i < k) denom += expf(vals[i] - vals[0]);
-    } else {
-      denom = ssum * expf(m - vals[0]);   // m == vals[0]: the factor is 1
-    }
+        for (int i = 0; i < KT; ++i)
+          if (i < k) denom += expf(vals[i] - vals[0]);
+      } else {
+        denom = ssum * expf(m - vals[0]);   // m == vals[0]: the factor is 1
+      }
 #pragma unroll
-    for (int i = 0; i < KT; ++i) {
-      if (i < k) {
-        ids[(int64_t)t * k + i] = idx[i];
-        weights[(int64_t)t * k + i] = expf(vals[i] - vals[0]) / denom;
+      for (int i = 0; i < KT; ++i) {
+        if (i < k) {
+          ids[(int64_t)t * k + i] = idx[i];
+          weights[(int64_t)t * k + i] = expf(vals[i] - vals[0]) / denom;
+        }
       }
     }
   }
@@ -406,56 +471,111 @@ bool router_topk_supported(int E, int k, int D) {
   return E >= 1 && E <= kRMaxN && k >= 1 && k <= kRMaxK && k <= E && D % kRBK == 0;
 }
 
+namespace {
+
+// Largest K split (a cluster of that many CTAs) that keeps the grid within
+// one CTA per SM, divides the K blocks, fits the exchange buffers in the
+// stages and can be co-scheduled; sets g.chunk for it.
+template <typename Kern>
+int pick_split(Kern kern, RouterGeom& g, int T, int D, size_t smem, cudaLaunchConfig_t cfg,
+               cudaLaunchAttribute* attr) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int tiles = (T + kRTile - 1) / kRTile;
+  const int kblocks = D / kRBK;
+  const size_t avail = (size_t)g.stages * (kRTile * 128 + g.n_pad * 128);
+  const int rows = T < kRTile ? T : kRTile;
+  for (int c = kRMaxCluster; c >= 2; c /= 2) {
+    if (kblocks % c != 0 || tiles * c > sms) continue;
+    const int per = (rows + c - 1) / c;
+    int cc = 0;
+    for (int cand : {g.n_pad, 256, 128}) {
+      if (cand > g.n_pad || g.n_pad % cand != 0) continue;
+      if ((size_t)rows * (cand + 4) * 4 + (size_t)per * (g.n_pad + 4) * 4 <= avail) {
+        cc = cand;
+        break;
+      }
+    }
+    if (cc == 0) continue;
+    // how many clusters of c CTAs with this shared memory can be resident at
+    // once (all tiles in one wave, or a smaller split)
+    static int known[2][kRMaxCluster + 1];   // -1 + count; 0: not asked yet
+    const int slot = g.n_pad > 256 ? 1 : 0;
+    if (known[slot][c] == 0) {
+      if (c > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr[0].val.clusterDim.x = (unsigned)c;
+      cfg.gridDim = dim3((unsigned)(tiles * c));
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+      cudaGetLastError();   // a refused size is not an error of this call
+      known[slot][c] = 1 + n;
+    }
+    if (known[slot][c] - 1 < tiles) continue;
+    g.chunk = cc;
+    return c;
+  }
+  g.chunk = g.n_pad;
+  return 1;
+}
+
+}  // namespace
+
 int launch_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int E,
                        int k, int renormalize, int32_t* ids, float* weights,
                        float* logits_out, cudaStream_t stream, bool pdl) {
   if (T == 0) return 0;
   if (!router_topk_supported(E, k, D)) return -2;
-  const int n_pad = E <= 256 ? (E + 15) / 16 * 16 : 512;
+  RouterGeom g{};
+  g.n_pad = E <= 256 ? (E + 15) / 16 * 16 : 512;
+  const int stage_bytes = kRTile * 128 + g.n_pad * 128;
+  g.stages = (200 * 1024) / stage_bytes;
+  if (g.stages > 8) g.stages = 8;
+  if (g.stages < 2) g.stages = 2;
+  // token boxes cover only the rows a batch of fewer than 128 tokens has
+  const int a_rows = T < kRTile ? (T + 7) / 8 * 8 : kRTile;
+  g.xbox = a_rows < kRBoxRows ? a_rows : kRBoxRows;
+  g.nxb = (a_rows + g.xbox - 1) / g.xbox;
+  g.wbox = g.n_pad < kRBoxRows ? g.n_pad : kRBoxRows;
+  while (g.n_pad % g.wbox != 0) g.wbox /= 2;
+  g.nwb = g.n_pad / g.wbox;
   CUtensorMap tm_x, tm_w;
-  if (!make_tmap_bf16(&tm_x, x, T, D, kRTile)) return -3;
-  if (!make_tmap_bf16(&tm_w, w_r, E, D, n_pad < kRBBoxRows ? n_pad : kRBBoxRows))
-    return -3;
-  const int stage_bytes = kRTile * 128 + n_pad * 128;
-  int stages = (200 * 1024) / stage_bytes;
-  if (stages > 8) stages = 8;
-  if (stages < 2) stages = 2;
-  const int smem = 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16;
+  if (!make_tmap_bf16(&tm_x, x, T, D, g.xbox)) return -3;
+  if (!make_tmap_bf16(&tm_w, w_r, E, D, g.wbox)) return -3;
+  const int smem = 1024 + g.stages * stage_bytes + (2 * g.stages + 1) * 8 + 16;
   auto kern = k <= 2 ? router_topk_kernel<2>
               : k <= 4 ? router_topk_kernel<4>
               : k <= 8 ? router_topk_kernel<8> : router_topk_kernel<16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return -3;
-  // split K over a cluster for a single tile of at most 64 tokens (its
-  // partials, 64 x (n_pad + 1) fp32, fit in the stages)
-  const int kblocks = D / kRBK;
-  int csplit = 1;
-  if (T <= 64)
-    for (int c : {8, 4, 2})
-      if (kblocks % c == 0 && (size_t)T * (n_pad + 1) * 4 <= (size_t)stages * stage_bytes) {
-        csplit = c;
-        break;
-      }
-  const int tiles = (T + kRTile - 1) / kRTile;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)csplit;
+  attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * csplit));
   cfg.blockDim = dim3(kRThreads);
-  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
+  g.csplit = pick_split(kern, g, T, D, (size_t)smem, cfg, attr);
+  // (the answers above are shared by the KT instances; the opt-in is per kernel)
+  if (g.csplit > 8 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess)
+    return -3;
+  const int tiles = (T + kRTile - 1) / kRTile;
+  attr[0].val.clusterDim.x = (unsigned)g.csplit;
+  cfg.gridDim = dim3((unsigned)(tiles * g.csplit));
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, T, D, E, n_pad, k,
-                         renormalize, stages, csplit, ids, weights, logits_out,
-                         device_error_word());
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, T, D, E, k, renormalize,
+                                           g, ids, weights, logits_out, device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
 
