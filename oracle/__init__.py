@@ -9,3 +9,7 @@ from .fp8 import (E4M3_MAX, bf16_bits, bf16_from_bits, bf16_round,  # noqa: F401
                   e4m3_decode, e4m3_encode)
 from .moe_ref import *  # noqa: F401,F403
 from .norm_ref import add_rmsnorm_quant_ref, add_rmsnorm_ref, rsqrt_f32_rn  # noqa: F401
+from .blockscale_ref import (BLOCK_K, BLOCK_N, SUBCHANNEL_K,  # noqa: F401
+                             blockscale_matmul_ref, grouped_blockscale_ref,
+                             quant_blocks_ref, quant_weight_blocks_ref,
+                             subchannel_matmul_ref)

@@ -10,8 +10,10 @@ import numpy as np
 import pytest
 
 import oracle
+import oracle.blockscale_ref as bref
 import oracle.moe_ref as ref
 import oracle.norm_ref as nref
+from tests import test_oracle_blockscale as block_pins
 from tests import test_oracle_layer as layer_pins
 from tests import test_oracle_norm as norm_pins
 from tests import test_oracle_route as route_pins
@@ -146,6 +148,58 @@ def _quant_pins():
     layer_pins.test_quant_matches_torch_quantiser(rng)
 
 
+def _mut_quant_blocks_strided(v, block):
+    v32 = np.asarray(v, dtype=np.float32)
+    R, K = v32.shape
+    nb = K // block
+    # blocks gathered with stride nb instead of contiguous runs
+    pieces = v32.reshape(R, block, nb).transpose(0, 2, 1).reshape(R * nb, block)
+    codes, scales = ref.quant_rows_ref(pieces)
+    return codes.reshape(R, nb, block).transpose(0, 2, 1).reshape(R, K), scales.reshape(R, nb)
+
+
+def _mut_weight_blocks_row_strips(w, bn=128, bk=128):
+    w32 = np.asarray(w, dtype=np.float32)
+    N, K = w32.shape
+    # 1 x (bn * bk) strips of consecutive entries instead of bn x bk tiles
+    codes, scales = ref.quant_rows_ref(w32.reshape(-1, bn * bk))
+    return codes.reshape(N, K), scales.reshape(N // bn, K // bk)
+
+
+def _mut_blockscale_tiled_weight_scale(a_codes, a_scale, w_codes, w_scale):
+    P = bref.block_partials_ref(a_codes, w_codes, 128)
+    sa = np.asarray(a_scale, np.float64)
+    sw = np.tile(np.asarray(w_scale, np.float64), (128, 1))   # n % nn, not n // 128
+    y = np.zeros(P.shape[1:])
+    for b in range(P.shape[0]):
+        y += sa[:, b][:, None] * sw[:, b][None, :] * P[b]
+    return y
+
+
+def _mut_blockscale_no_activation_scale(a_codes, a_scale, w_codes, w_scale):
+    P = bref.block_partials_ref(a_codes, w_codes, 128)
+    sw = np.repeat(np.asarray(w_scale, np.float64), 128, axis=0)
+    return sum(sw[:, b][None, :] * P[b] for b in range(P.shape[0]))
+
+
+def _mut_subchannel_first_group_scale(a_codes, a_scale, w_codes, w_scale, block=512):
+    P = bref.block_partials_ref(a_codes, w_codes, block)
+    sa = np.asarray(a_scale, np.float64)
+    y = P.sum(axis=0) * sa[:, 0][:, None]          # one group's scale for all
+    return y * np.asarray(w_scale, np.float64)[None, :]
+
+
+def _blockscale_pins():
+    block_pins.test_one_block_per_row_is_the_ptpc_quantiser()
+    for b in (128, 512):
+        block_pins.test_each_block_is_quantised_on_its_own(b)
+    block_pins.test_weight_block_is_a_per_tensor_quantiser()
+    block_pins.test_weight_blocks_slice_by_slice()
+    block_pins.test_blockscale_matmul_equals_dequantise_first()
+    block_pins.test_subchannel_matmul_equals_dequantise_first()
+    block_pins.test_equal_block_scales_reduce_to_ptpc()
+
+
 MUTANTS = {
     "silu_drops_g": (ref, "silu_ref", _mut_silu, _layer_pins),
     "gate_up_swapped": (ref, "expert_ffn_ref", _mut_expert_ffn_swap, _layer_pins),
@@ -169,6 +223,17 @@ MUTANTS = {
                                _norm_pins),
     "rsqrt_two_roundings": (nref, "rsqrt_f32_rn", _mut_rsqrt_two_roundings,
                             _norm_pins),
+    "activation_blocks_strided": (bref, "quant_blocks_ref", _mut_quant_blocks_strided,
+                                  _blockscale_pins),
+    "weight_blocks_as_strips": (bref, "quant_weight_blocks_ref",
+                                _mut_weight_blocks_row_strips, _blockscale_pins),
+    "blockscale_weight_scale_tiled": (bref, "blockscale_matmul_ref",
+                                      _mut_blockscale_tiled_weight_scale, _blockscale_pins),
+    "blockscale_no_activation_scale": (bref, "blockscale_matmul_ref",
+                                       _mut_blockscale_no_activation_scale,
+                                       _blockscale_pins),
+    "subchannel_one_group_scale": (bref, "subchannel_matmul_ref",
+                                   _mut_subchannel_first_group_scale, _blockscale_pins),
 }
 
 
