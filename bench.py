@@ -624,6 +624,76 @@ def run_ours(args, cfg, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_compare_scales(args, cfg, local_rank):
+    """The workload's two expert GEMMs (gate/up-shaped N = 2I, K = D and
+    down-shaped N = D, K = I, over the T k routed rows) with PTPC,
+    512-subchannel and BlockScale-128 scales on the one block-scaled engine,
+    and the production PTPC grouped GEMM beside them. Each launch is timed
+    with CUDA events on its stream, L2 flushed before every call; the median
+    of `steps` calls. One JSON line."""
+    import torch
+    from expert_layer_ptpc_gb300 import binding, build, scaled
+    build.build()
+    torch.cuda.set_device(local_rank)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def median_ms(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ts = sorted(a.elapsed_time(b) for a, b in ev)
+        return ts[len(ts) // 2]
+
+    sampler = ClockSampler(physical_gpu(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    result = {}
+    for which in ("gateup", "down"):
+        row = {}
+        for mode in ("ptpc", "sub512", "block128"):
+            prob = scaled.make_problem(mode, cfg, which)
+            row[mode + "_ms"] = median_ms(lambda: scaled.run(prob))
+            if mode == "ptpc":
+                row["ptpc_production_ms"] = median_ms(lambda: binding.moe_grouped_gemm(
+                    binding.MOE_GEMM_DOWN, prob["qa"], prob["sa"], prob["qw"], prob["sw"],
+                    prob["offsets"], out=prob["out"]))
+                R, K = prob["qa"].shape
+                N = prob["qw"].shape[1]
+                row["shape"] = {"rows": R, "N": N, "K": K, "groups": cfg.E}
+                row["flops"] = 2.0 * R * N * K
+            del prob
+            torch.cuda.empty_cache()
+        st, bits = binding.moe_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({bits:#x})")
+        for k in ("ptpc", "sub512", "block128", "ptpc_production"):
+            row[k + "_tflops"] = row["flops"] / (row[k + "_ms"] * 1e-3) / 1e12
+        row["block128_over_ptpc"] = row["block128_ms"] / row["ptpc_ms"]
+        row["sub512_over_ptpc"] = row["sub512_ms"] / row["ptpc_ms"]
+        result[which] = row
+    t1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    print(json.dumps({
+        "metric": "scale_granularity_gemm_ms", "unit": "ms", "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "e4m3",
+        "data": "synthetic", "config": {"workload": describe(cfg),
+                                        "l2": "flushed before every call"},
+        "engine": "one tcgen05 engine for all three modes (128 x 128 tiles); "
+                  "ptpc_production = moe_grouped_gemm (the layer's kernel)",
+        "gemms": result, "clocks": sampler.summary(t0, t1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -638,6 +708,9 @@ def main():
     ap.add_argument("--prenorm", action="store_true",
                     help="feed the layer from the residual stream: fused add + "
                          "RMSNorm + quant replaces the quantisation step")
+    ap.add_argument("--compare-scales", action="store_true",
+                    help="time the workload's expert GEMMs with PTPC, "
+                         "512-subchannel and BlockScale-128 scales (one JSON line)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the forward directly instead of replaying a "
                          "CUDA graph of it")
@@ -657,6 +730,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, cfg)
+        return
+    if args.compare_scales:
+        if rank == 0:
+            run_compare_scales(args, cfg, local_rank)
         return
 
     if world > 1:

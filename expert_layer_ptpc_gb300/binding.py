@@ -74,7 +74,12 @@ _SIGNATURES = {
                                    _I64, _P, _P, _P, _P, _P]),
     "moe_forward_prenorm": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  _SZ, _P, _I, _P]),
+    "moe_quant_blocks": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
+    "moe_quant_weight_blocks": (_I, [_P, _I64, _I, _P, _P, _P]),
+    "moe_grouped_gemm_scaled": (_I, [_I, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _P, _P]),
 }
+
+MOE_SCALE_PTPC, MOE_SCALE_SUB512, MOE_SCALE_BLOCK128 = 0, 1, 2
 
 MOE_FORWARD_EVENTS = 9
 
@@ -404,6 +409,56 @@ def moe_router_topk(x, w_r, k, renormalize=True, ids=None, weights=None,
         _ptr(x), _ptr(w_r), T, D, E, k, int(bool(renormalize)), _ptr(ids),
         _ptr(weights), _ptr(logits), _stream(stream)))
     return ids, weights
+
+
+def moe_quant_blocks(x, block, q=None, scales=None, stream=None):
+    """x [rows, K] bf16 -> (q [rows, K] e4m3, scales [rows, K / block] fp32),
+    one scale per 1 x block piece along K (block 128 or 512)."""
+    _need(x, torch.bfloat16, "x")
+    rows, K = x.shape
+    if q is None:
+        q = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, K // block), dtype=torch.float32, device=x.device)
+    _check("moe_quant_blocks", load_library().moe_quant_blocks(
+        _ptr(x), rows, K, block, _ptr(q), _ptr(scales), _stream(stream)))
+    return q, scales
+
+
+def moe_quant_weight_blocks(w, q=None, scales=None, stream=None):
+    """w [..., K] fp32 (rows a multiple of 128) -> (q same shape e4m3,
+    scales [rows / 128, K / 128] fp32), one scale per 128 x 128 block."""
+    _need(w, torch.float32, "w")
+    K = w.shape[-1]
+    rows = w.numel() // K
+    if q is None:
+        q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((rows // 128, K // 128), dtype=torch.float32, device=w.device)
+    _check("moe_quant_weight_blocks", load_library().moe_quant_weight_blocks(
+        _ptr(w), rows, K, _ptr(q), _ptr(scales), _stream(stream)))
+    return q, scales
+
+
+def moe_grouped_gemm_scaled(kind, A, a_scale, W, w_scale, group_offsets, out=None,
+                            stream=None):
+    """kind MOE_SCALE_PTPC / SUB512 / BLOCK128: W [G, N, K] -> out [rows, N]
+    fp32 with the scale layouts of include/moe_ptpc.h."""
+    _need(A, torch.uint8, "A")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(W, torch.uint8, "W")
+    _need(w_scale, torch.float32, "w_scale")
+    _need(group_offsets, torch.int32, "group_offsets")
+    a_rows, K = A.shape
+    G, N = W.shape[0], W.shape[1]
+    if W.shape[2] != K or group_offsets.numel() != G + 1:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((a_rows, N), dtype=torch.float32, device=A.device)
+    _check("moe_grouped_gemm_scaled", load_library().moe_grouped_gemm_scaled(
+        kind, _ptr(A), _ptr(a_scale), a_rows, _ptr(W), _ptr(w_scale), _ptr(group_offsets),
+        G, N, K, _ptr(out), _stream(stream)))
+    return out
 
 
 def moe_add_rmsnorm_quant(x, residual, gamma, eps=1e-6, dst_rows=None, copies=1,

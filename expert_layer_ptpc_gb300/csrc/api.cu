@@ -226,6 +226,48 @@ int moe_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                              stream, false);
 }
 
+int moe_quant_blocks(const uint16_t* in_bf16, int64_t rows, int K, int block, uint8_t* q,
+                     float* scales, moe_stream_t stream) {
+  if (rows < 0 || (block != 128 && block != 512) || K <= 0 || K % block != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!in_bf16 || !q || !scales) return MOE_ERR_INVALID_ARG;
+  const uintptr_t ain = reinterpret_cast<uintptr_t>(in_bf16);
+  const uintptr_t aq = reinterpret_cast<uintptr_t>(q);
+  if (block == 128 ? (ain % 8 != 0 || aq % 4 != 0) : (ain % 16 != 0 || aq % 16 != 0))
+    return MOE_ERR_INVALID_ARG;
+  return launch_quant_blocks(in_bf16, rows, K, block, q, scales, stream);
+}
+
+int moe_quant_weight_blocks(const float* w, int64_t rows, int K, uint8_t* q, float* scales,
+                            moe_stream_t stream) {
+  if (rows < 0 || rows % 128 != 0 || K <= 0 || K % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (rows / 128 > 65535) return MOE_ERR_UNSUPPORTED;
+  if (!w || !q || !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return launch_quant_weight_blocks(w, rows, K, q, scales, stream);
+}
+
+int moe_grouped_gemm_scaled(int scale_kind, const uint8_t* A, const float* a_scale,
+                            int64_t a_rows, const uint8_t* W, const float* w_scale,
+                            const int32_t* group_offsets, int groups, int N, int K,
+                            float* out, moe_stream_t stream) {
+  if (scale_kind != MOE_SCALE_PTPC && scale_kind != MOE_SCALE_SUB512 &&
+      scale_kind != MOE_SCALE_BLOCK128)
+    return MOE_ERR_INVALID_ARG;
+  if (a_rows < 0 || groups < 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (scale_kind == MOE_SCALE_SUB512 && K % 512 != 0) return MOE_ERR_UNSUPPORTED;
+  if (groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  if (a_rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (a_rows == 0 || groups == 0) return MOE_OK;
+  if (!A || !a_scale || !W || !w_scale || !group_offsets || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  return launch_grouped_gemm_scaled(scale_kind, A, a_scale, a_rows, W, w_scale,
+                                    group_offsets, groups, N, K, out, stream);
+}
+
 int moe_scale_max(const float* scale, int groups, int N, float* bound,
                   moe_stream_t stream) {
   if (groups < 0 || N <= 0) return MOE_ERR_INVALID_ARG;

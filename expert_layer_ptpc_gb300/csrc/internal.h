@@ -82,6 +82,17 @@ int launch_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int
                        int k, int renormalize, int32_t* ids, float* weights,
                        float* logits_out, cudaStream_t stream, bool pdl);
 
+// FP8 grouped GEMM with PTPC (0), 512-subchannel (1) or BlockScale-128 (2)
+// scales, and the block quantisers (gemm_scaled.cu). Return a moe_status.
+int launch_grouped_gemm_scaled(int mode, const uint8_t* A, const float* a_scale,
+                               int64_t a_rows, const uint8_t* W, const float* w_scale,
+                               const int32_t* offsets, int groups, int N, int K,
+                               float* out, cudaStream_t stream);
+int launch_quant_blocks(const uint16_t* in, int64_t rows, int K, int block, uint8_t* q,
+                        float* scales, cudaStream_t stream);
+int launch_quant_weight_blocks(const float* w, int64_t rows, int K, uint8_t* q,
+                               float* scales, cudaStream_t stream);
+
 // Largest row length launch_quant handles.
 constexpr int kMaxQuantCols = 32768;
 

@@ -416,6 +416,72 @@ MOE_API int moe_forward_prenorm(const moe_dims* dims, const moe_prenorm* pre,
  */
 MOE_API int moe_debug_expire_wait(int limit_us, moe_stream_t stream);
 
+/*
+ * FP8 with per-K-block scales: the alternatives to PTPC that the pages
+ * compare it with ("Ultimate Latency Optimization of Qwen3 and Qwen3-VL on
+ * AMD MI300X Series", section 2.1.1: BlockScale's fixed K block against
+ * PTPC's none, PTPC 15-30% faster on ROCm; the MI355X DeepSeek-R1 page,
+ * "MoRI Quantized All-to-All": one fp32 scale per 128 elements; "Optimizing
+ * Qwen 3.5 397B MoE on Ironwood TPU7x", GMM V2 paragraph: activations
+ * quantised per 512-wide subchannel). Every block uses the PTPC quantiser:
+ * s = fp32(max(amax_block, 1e-12) / 448), q = e4m3_rne_sat(fp32(v / s)).
+ */
+typedef enum moe_scale_kind {
+  MOE_SCALE_PTPC = 0,      /* a_scale [a_rows], w_scale [groups, N]            */
+  MOE_SCALE_SUB512 = 1,    /* a_scale [a_rows, K/512], w_scale [groups, N]     */
+  MOE_SCALE_BLOCK128 = 2   /* a_scale [a_rows, K/128],
+                              w_scale [groups, N/128, K/128]                   */
+} moe_scale_kind;
+
+/*
+ * moe_quant_blocks - per-row FP8 quantisation of in [rows, K] bf16 in
+ * 1 x block pieces along K (block 128 or 512): q [rows, K] e4m3 (written),
+ * scales [rows, K/block] fp32 (written), scales[r, b] for
+ * in[r, b*block .. (b+1)*block). Device pointers; in 8-byte aligned (block
+ * 128) or 16-byte aligned (512), q 4- or 16-byte aligned.
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned pointers, rows < 0, block
+ *         not 128 or 512, K not a positive multiple of block).
+ */
+MOE_API int moe_quant_blocks(const uint16_t* in_bf16, int64_t rows, int K, int block,
+                             uint8_t* q, float* scales, moe_stream_t stream);
+
+/*
+ * moe_quant_weight_blocks - BlockScale-128 weight quantisation of
+ * w [rows, K] fp32 (rows = groups * N, both multiples of 128) in 128 x 128
+ * blocks: q [rows, K] e4m3 (written), scales [rows/128, K/128] fp32
+ * (written). Device pointers, 16-byte aligned.
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned pointers, sizes not
+ *         positive multiples of 128), MOE_ERR_UNSUPPORTED (rows > 128 * 65535).
+ */
+MOE_API int moe_quant_weight_blocks(const float* w, int64_t rows, int K, uint8_t* q,
+                                    float* scales, moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_scaled - FP8 grouped GEMM with the scale granularity
+ * `scale_kind` (moe_scale_kind), all three on one tcgen05 engine: the tensor
+ * cores accumulate each scale group of K (all of K for PTPC, 512 for
+ * SUB512, 128 for BLOCK128) in TMEM, and the epilogue scales and sums the
+ * groups in fp32:
+ *   PTPC:     y[r, n] = w_scale[g, n] * fp32(P[r, n] * a_scale[r])
+ *   SUB512:   y[r, n] = w_scale[g, n] * sum_j fp32(P_j[r, n] * a_scale[r, j])
+ *   BLOCK128: y[r, n] = sum_b fp32(P_b[r, n] * fp32(a_scale[r, b] *
+ *                                                   w_scale[g, n/128, b]))
+ * (P_j: the FP8 dot product over scale group j, fp32 tensor-core
+ * accumulation.) Group g owns rows [group_offsets[g], group_offsets[g+1]) of
+ * A [a_rows, K] e4m3; W [groups, N, K] e4m3; out [a_rows, N] fp32 (rows
+ * outside every group not written). group_offsets is a DEVICE array of
+ * groups + 1 non-decreasing entries <= a_rows. A, W, out 16-byte aligned.
+ * Errors: MOE_ERR_INVALID_ARG (unknown kind, null or misaligned pointers,
+ *         negative sizes), MOE_ERR_UNSUPPORTED (N or K not multiples of 128,
+ *         K not a multiple of 512 for SUB512, K > 39168 for BLOCK128 (a
+ *         tile's scales are staged in shared memory), groups > 1025),
+ *         MOE_ERR_CUDA.
+ */
+MOE_API int moe_grouped_gemm_scaled(int scale_kind, const uint8_t* A, const float* a_scale,
+                                    int64_t a_rows, const uint8_t* W, const float* w_scale,
+                                    const int32_t* group_offsets, int groups, int N, int K,
+                                    float* out, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

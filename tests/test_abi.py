@@ -77,6 +77,21 @@ def test_argument_errors_need_no_gpu(lib):
                                None) == -2
     assert lib.moe_router_topk(None, None, 4, 4096, 8, 9, 1, None, None, None,
                                None) == -1                       # k > E
+    # block-scaled path: block sizes, kinds and shapes checked on the host
+    assert lib.moe_quant_blocks(None, 4, 256, 64, None, None, None) == -1     # block 64
+    assert lib.moe_quant_blocks(None, 4, 640, 512, None, None, None) == -1    # K % 512
+    assert lib.moe_quant_blocks(None, 0, 256, 128, None, None, None) == 0     # empty
+    assert lib.moe_quant_weight_blocks(None, 100, 256, None, None, None) == -1
+    assert lib.moe_quant_weight_blocks(None, 128 * 65536, 128, fake16, fake16,
+                                       None) == -2
+    assert lib.moe_grouped_gemm_scaled(3, None, None, 8, None, None, None, 2, 128,
+                                       256, None, None) == -1             # unknown kind
+    assert lib.moe_grouped_gemm_scaled(1, None, None, 8, None, None, None, 2, 128,
+                                       640, None, None) == -2             # K % 512
+    assert lib.moe_grouped_gemm_scaled(2, None, None, 8, None, None, None, 2, 100,
+                                       256, None, None) == -2             # N % 128
+    assert lib.moe_grouped_gemm_scaled(2, None, None, 0, None, None, None, 2, 128,
+                                       256, None, None) == 0              # no rows
     # the failure-detection check validates its limit before touching CUDA
     assert lib.moe_debug_expire_wait(0, None) == -1
     assert lib.moe_debug_expire_wait(2000000, None) == -1
