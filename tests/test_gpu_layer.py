@@ -228,6 +228,40 @@ def test_prenorm_layer_all_tokens(cfg):
     assert ok, f"{cfg.name}: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
 
 
+def test_prenorm_prefill_sampled():
+    """moe_forward_prenorm on the prefill workload at full size, in the
+    launch configuration and with the inputs `bench.py --prenorm` times
+    (residual N(0, 0.5^2) and gamma 1 + N(0, 0.1^2), bf16, seed 12345): the
+    new residual of every token bit for bit, the output of sampled tokens
+    against the oracle layer on the oracle's normalised activations."""
+    from expert_layer_ptpc_gb300 import binding
+    cfg = syn.CONFIGS["prefill"]
+    run = _Run(cfg)
+    x, logits = run.inputs(cfg)
+    g = torch.Generator(device="cpu").manual_seed(12345)
+    res = (torch.randn(cfg.T, cfg.D, generator=g) * 0.5).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn(cfg.D, generator=g)).to(torch.bfloat16)
+    res_out = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device="cuda")
+    out = run.layer.forward(x, logits, residual=res.cuda(), gamma=gamma.cuda(),
+                            eps=1e-6, residual_out=res_out)
+    st, bits = binding.moe_device_status()
+    assert st == 0, bits
+    ref = oracle.add_rmsnorm_ref(x.float().cpu().numpy(), res.float().numpy(),
+                                 gamma.float().numpy(), 1e-6)
+    assert np.array_equal(res_out.float().cpu().numpy(), ref[0])
+    ln = logits.cpu().numpy()
+    rid, _ = oracle.route_ref(ln, cfg.k, cfg.renormalize)
+    rng = np.random.default_rng(cfg.T + 3)
+    tokens = np.sort(rng.choice(cfg.T, 6, replace=False))
+    tokens[-1] = cfg.T - 1
+    touched = sorted(set(int(e) for e in rid[tokens].ravel()))
+    qmap = run.expert_weights(touched)
+    r = oracle.moe_forward_ref(ref[1], cfg.k, lambda e: qmap[e], cfg.E, logits=ln,
+                               renormalize=cfg.renormalize, tokens=tokens)
+    ok, max_rel, l1 = layer_tolerance_ok(out.float().cpu().numpy()[tokens], r["out64"])
+    assert ok, f"prefill prenorm: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
+
+
 def test_forward_is_deterministic():
     cfg = syn.LayerConfig("det", 2000, 512, 32, 4, 256, True, "normal")
     run = _Run(cfg)

@@ -169,6 +169,37 @@ def test_router_topk(T, D, E, k, renorm):
         assert exact[t, chosen].min() >= exact[t, ~chosen].max() - tol
 
 
+@pytest.mark.parametrize("name,T", [("prefill", None), ("sweep", 16384)])
+def test_router_topk_full_size(name, T):
+    """The fused router at the routing shapes `bench.py --router-gemm` times,
+    with the benchmark's own inputs: prefill (8192 tokens, 128 experts,
+    top-8) and the T = 16384 sweep point (512 experts, top-10). Logits of
+    sampled tokens within the fp32 bound of the exact products; ids of every
+    token bit-exact and weights within 1e-5 against route_ref on the
+    kernel's own logits."""
+    from dataclasses import replace
+    from expert_layer_ptpc_gb300 import synthetic as syn
+    cfg = syn.CONFIGS[name] if T is None else syn.sweep_config(T)
+    cfg = replace(cfg, router="weights")
+    x = syn.gen_x(cfg, "cuda")
+    w = syn.gen_router_weights(cfg, "cuda")
+    logits = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    ids, wts = B().moe_router_topk(x, w, cfg.k, cfg.renormalize, logits=logits)
+    assert B().moe_device_status() == (0, 0)
+    lg = logits.cpu().numpy()
+    rid, rw = oracle.route_ref(lg, cfg.k, cfg.renormalize)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    rng = np.random.default_rng(5)
+    rows = np.sort(rng.choice(cfg.T, 64, replace=False))
+    rows[-1] = cfg.T - 1
+    xd = x[torch.as_tensor(rows, device="cuda").long()].double().cpu().numpy()
+    wd = w.double().cpu().numpy()
+    exact = xd @ wd.T
+    bound = gemm_bound(np.abs(xd) @ np.abs(wd).T, cfg.D)
+    assert np.all(np.abs(lg[rows].astype(np.float64) - exact) <= bound)
+
+
 @pytest.mark.parametrize("T,D,k,shared,inplace,wide", [
     (1, 256, 1, False, False, False), (37, 512, 4, True, False, False),
     (300, 4096, 8, False, True, False), (64, 7168, 2, True, True, False),
