@@ -177,11 +177,12 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
   const int a_bytes = kRTile * 128;
   const int stage_bytes = a_bytes + n_pad * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + stages + s); };
   const uint32_t acc_bar = smem_u32(bars + 2 * stages);
+  const uint32_t xchg_bar = smem_u32(bars + 2 * stages + 1);   // upper-half lists ready
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = csplit > 1 ? cluster_rank() : 0;
   const int tile0 = (int)(blockIdx.x / csplit) * kRTile;
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(acc_bar, 1);
+    mbar_init(xchg_bar, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -275,7 +277,8 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
   // ---------------- epilogue ----------------
   __syncwarp();
   const bool epi = warp < 4;
-  const bool have = epi && warp_wait(acc_bar, 0, abort_flag, err, kErrTimeoutEpilogue);
+  // (every warp waits: without a K split, warps 4-7 scan half the columns)
+  const bool have = warp_wait(acc_bar, 0, abort_flag, err, kErrTimeoutEpilogue);
   tc_fence_after_sync();
   const int lrow = warp * 32 + lane;
   const int rows_t = min(T - tile0, kRTile);   // token rows of this tile
@@ -356,9 +359,16 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
     }
   } else if (have) {
     // thread = token: scan the logits straight out of TMEM with a running
-    // top-k and the softmax sums
-    const int t = tile0 + lrow;
-    const bool row_ok = lrow < rows_t;
+    // top-k and the softmax sums. Warps w and w + 4 read the same TMEM lanes:
+    // w scans the lower expert columns, w + 4 the upper ones, and hands its
+    // list and sums over through shared memory (the stages are free) for w
+    // to merge.
+    const int row = (warp & 3) * 32 + lane;
+    const int upper = warp >> 2;
+    const int c_split = (n_pad / 2 + 15) / 16 * 16;
+    const int c_begin = upper ? c_split : 0, c_end = upper ? n_pad : c_split;
+    const int t = tile0 + row;
+    const bool row_ok = row < rows_t;
     float vals[KT];
     int idx[KT];
 #pragma unroll
@@ -366,8 +376,8 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
       vals[i] = -INFINITY;
       idx[i] = 0x7fffffff;
     }
-    float m = -INFINITY, ssum = 0.f;   // online softmax over all experts
-    for (int c0 = 0; c0 < n_pad; c0 += 16) {
+    float m = -INFINITY, ssum = 0.f;   // online softmax over the scanned experts
+    for (int c0 = c_begin; c0 < c_end; c0 += 16) {
       float l[16];
       tmem_ld_x16(trow + (uint32_t)c0, l);
       tmem_ld_wait();
@@ -405,7 +415,54 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
           if (c0 + j < E) ssum += expf(l[j] - m);
       }
     }
-    if (row_ok) {
+    // the upper half's list and sums -> shared memory -> merged by the lower
+    float* xf = reinterpret_cast<float*>(smem) + row * (2 * KT + 2);
+    int* xi = reinterpret_cast<int*>(xf) + KT;
+    bool ok = true;
+    if (upper) {
+#pragma unroll
+      for (int i = 0; i < KT; ++i) {
+        xf[i] = vals[i];
+        xi[i] = idx[i];
+      }
+      xf[2 * KT] = m;
+      xf[2 * KT + 1] = ssum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xchg_bar);
+      ok = false;   // the lower warp writes this token
+    } else {
+      ok = warp_wait(xchg_bar, 0, abort_flag, err, kErrTimeoutEpilogue);
+      if (ok) {
+#pragma unroll
+        for (int i2 = 0; i2 < KT; ++i2) {   // every upper index is larger: ties stay
+          if (i2 < k) {
+            float cv = xf[i2];
+            int ci = xi[i2];
+#pragma unroll
+            for (int i = 0; i < KT; ++i) {
+              if (i < k && cv > vals[i]) {
+                const float tv = vals[i];
+                const int ti = idx[i];
+                vals[i] = cv;
+                idx[i] = ci;
+                cv = tv;
+                ci = ti;
+              }
+            }
+          }
+        }
+        const float m2 = xf[2 * KT], s2 = xf[2 * KT + 1];
+        if (!renormalize && m2 > -INFINITY) {
+          if (m2 > m) {
+            ssum = (m == -INFINITY ? 0.f : ssum * expf(m - m2)) + s2;
+            m = m2;
+          } else {
+            ssum += s2 * expf(m2 - m);
+          }
+        }
+      }
+    }
+    if (ok && row_ok) {
       float denom;
       if (renormalize) {
         denom = 0.f;
@@ -545,7 +602,7 @@ int launch_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int
   CUtensorMap tm_x, tm_w;
   if (!make_tmap_bf16(&tm_x, x, T, D, g.xbox)) return -3;
   if (!make_tmap_bf16(&tm_w, w_r, E, D, g.wbox)) return -3;
-  const int smem = 1024 + g.stages * stage_bytes + (2 * g.stages + 1) * 8 + 16;
+  const int smem = 1024 + g.stages * stage_bytes + (2 * g.stages + 2) * 8 + 16;
   auto kern = k <= 2 ? router_topk_kernel<2>
               : k <= 4 ? router_topk_kernel<4>
               : k <= 8 ? router_topk_kernel<8> : router_topk_kernel<16>;
