@@ -48,7 +48,8 @@ constexpr int kSCols = kSBN / 2;          // token columns per epilogue thread
 constexpr int kSATile = kSBM * kBK;       // 16 KB
 constexpr int kSStage = kSATile + kSBN * kBK;
 constexpr int kSMaxStages = 6;
-constexpr int kSBoxes = 4;                // per stage: 2 weight + 2 token boxes of 64 rows
+constexpr int kSBoxRows = 32;
+constexpr int kSBoxes = 8;                // per stage: 4 weight + 4 token boxes of 32 rows
 constexpr int kSAccBufs = 4;              // TMEM accumulators: 4 x 128 columns
 constexpr int kSNumBars = 2 * kSMaxStages + 2 * kSAccBufs + 1;
 constexpr int kSScaleLd = kSBN + 4;       // staged scales: [group][token], rows 16-byte aligned
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kSThreads, 1) grouped_gemm_scaled_kernel(
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(full_bar(s), kSProds);   // one arrival per producer
+      mbar_init(full_bar(s), kSBoxes);   // one arrival per box
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < kSAccBufs; ++b) {
@@ -149,11 +150,11 @@ __global__ void __launch_bounds__(kSThreads, 1) grouped_gemm_scaled_kernel(
   pdl_launch_dependents();
 
   if (warp >= kSProd0 && warp < kSProd0 + kSProds) {
-    // ---------------- TMA producers ----------------
-    if (lane == 0) {
-      const int p = warp - kSProd0;
-      uint32_t bytes = 0;
-      for (int b = p; b < kSBoxes; b += kSProds) bytes += 64 * kBK;
+    // ---------------- TMA producers: box lane * 3 + p, one per lane ----------------
+    const int p = warp - kSProd0;
+    const int b = lane * kSProds + p;
+    if (b < kSBoxes) {
+      const uint32_t bytes = kSBoxRows * kBK;
       const uint64_t pol_w = l2_policy_evict_normal();   // shared by the token tiles
       const uint64_t pol_a = l2_policy_evict_last();     // shared by the channel tiles
       int s = 0;
@@ -164,13 +165,12 @@ __global__ void __launch_bounds__(kSThreads, 1) grouped_gemm_scaled_kernel(
           break;
         mbar_arrive_expect_tx(full_bar(s), bytes);
         const uint32_t st = smem_u32(smem + s * kSStage);
-        for (int b = p; b < kSBoxes; b += kSProds) {
-          if (b < 2)
-            tma_load_2d(st + b * 64 * kBK, &tm_w, kb * kBK, wrow0 + b * 64, full_bar(s), pol_w);
-          else
-            tma_load_2d(st + kSATile + (b - 2) * 64 * kBK, &tm_a, kb * kBK,
-                        ti.row0 + (b - 2) * 64, full_bar(s), pol_a);
-        }
+        if (b < kSBoxes / 2)
+          tma_load_2d(st + b * kSBoxRows * kBK, &tm_w, kb * kBK, wrow0 + b * kSBoxRows,
+                      full_bar(s), pol_w);
+        else
+          tma_load_2d(st + kSATile + (b - kSBoxes / 2) * kSBoxRows * kBK, &tm_a, kb * kBK,
+                      ti.row0 + (b - kSBoxes / 2) * kSBoxRows, full_bar(s), pol_a);
         ++issued;
         if (++s == stages) {
           s = 0;
@@ -412,8 +412,8 @@ int launch_grouped_gemm_scaled(int mode, const uint8_t* A, const float* a_scale,
                                float* out, cudaStream_t stream) {
   if (a_rows == 0 || groups == 0) return 0;
   CUtensorMap tm_w, tm_a;
-  if (!make_tmap(&tm_w, W, (int64_t)groups * N, K, 64)) return -3;
-  if (!make_tmap(&tm_a, A, a_rows, K, 64)) return -3;
+  if (!make_tmap(&tm_w, W, (int64_t)groups * N, K, kSBoxRows)) return -3;
+  if (!make_tmap(&tm_a, A, a_rows, K, kSBoxRows)) return -3;
   auto kern = mode == kModeBlock128 ? grouped_gemm_scaled_kernel<kModeBlock128>
               : mode == kModeSub512 ? grouped_gemm_scaled_kernel<kModeSub512>
                                     : grouped_gemm_scaled_kernel<kModePtpc>;
