@@ -28,8 +28,9 @@
 //   warp 0      TMEM allocation and MMA issue (one lane)
 //   warps 1-3   TMA producers: two 64-row weight boxes and two 64-row token
 //               boxes per stage, shared out between them
-//   warps 4-11  epilogue: warp w reads TMEM lanes 32 (w % 4).. (channels) and
-//               one half of the 128 token columns
+//   warps 4-19  epilogue: warp w reads TMEM lanes 32 (w % 4).. (channels) and
+//               one quarter of the 128 token columns (four warps per
+//               scheduler hide the TMEM load latency of the promotion)
 // Every wait is bounded; a wait that runs out raises the device error word
 // and the roles stop after draining their copies and MMAs.
 #include "gemm_common.cuh"
@@ -42,9 +43,9 @@ using namespace gemm;
 constexpr int kSBM = 128;                 // channels per tile (MMA M)
 constexpr int kSBN = 128;                 // tokens per tile (MMA N)
 constexpr int kSProd0 = 1, kSProds = 3;   // producer warps
-constexpr int kSEpi0 = 4, kSEpis = 8;     // epilogue warps
+constexpr int kSEpi0 = 4, kSEpis = 16;    // epilogue warps
 constexpr int kSThreads = 32 * (kSEpi0 + kSEpis);
-constexpr int kSCols = kSBN / 2;          // token columns per epilogue thread
+constexpr int kSCols = kSBN / 4;          // token columns per epilogue thread
 constexpr int kSATile = kSBM * kBK;       // 16 KB
 constexpr int kSStage = kSATile + kSBN * kBK;
 constexpr int kSMaxStages = 6;
@@ -225,8 +226,8 @@ __global__ void __launch_bounds__(kSThreads, 1) grouped_gemm_scaled_kernel(
     // ---------------- epilogue: promote each group into registers ----------------
     const int e = warp - kSEpi0;
     const int q = warp & 3;            // TMEM lane quarter: channels 32q..32q+31
-    const int half = e >> 2;           // token columns half*64 .. half*64+63
-    const int col0 = half * kSCols;
+    const int quarter = e >> 2;        // token columns quarter*32 .. quarter*32+31
+    const int col0 = quarter * kSCols;
     // every group's multiplier of each of the tile's 128 token columns,
     // [group][token]: the activation scale, times the weight block's scale
     // for BlockScale-128 (read once, coalesced)
