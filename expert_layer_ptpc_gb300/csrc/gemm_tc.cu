@@ -32,6 +32,7 @@
 // the TMEM is freed before the kernel returns.
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -663,15 +664,16 @@ bool make_tmap_out(CUtensorMap* map, void* base, int64_t rows, int cols,
 }
 
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];   // 0: not asked yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
+    if (n <= 0) n = 1;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 int cta_pair_mode() {

@@ -37,6 +37,9 @@
 // warp per token.
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -493,16 +496,15 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_bf16() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q{};
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+  });
   return fn;
 }
 
@@ -557,9 +559,12 @@ int pick_split(Kern kern, RouterGeom& g, int T, int D, size_t smem, cudaLaunchCo
     if (cc == 0) continue;
     // how many clusters of c CTAs with this shared memory can be resident at
     // once (all tiles in one wave, or a smaller split)
-    static int known[2][kRMaxCluster + 1];   // -1 + count; 0: not asked yet
+    // per device (up to 64) and shared-memory class: 1 + the count, 0 when
+    // not asked yet (racing first askers store the same answer)
+    static std::atomic<int> known[64][2][kRMaxCluster + 1];
     const int slot = g.n_pad > 256 ? 1 : 0;
-    if (known[slot][c] == 0) {
+    std::atomic<int>& ans = known[dev >= 0 && dev < 64 ? dev : 0][slot][c];
+    if (ans.load(std::memory_order_relaxed) == 0) {
       if (c > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       attr[0].val.clusterDim.x = (unsigned)c;
       cfg.gridDim = dim3((unsigned)(tiles * c));
@@ -569,9 +574,9 @@ int pick_split(Kern kern, RouterGeom& g, int T, int D, size_t smem, cudaLaunchCo
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
       cudaGetLastError();   // a refused size is not an error of this call
-      known[slot][c] = 1 + n;
+      ans.store(1 + n, std::memory_order_relaxed);
     }
-    if (known[slot][c] - 1 < tiles) continue;
+    if (ans.load(std::memory_order_relaxed) - 1 < tiles) continue;
     g.chunk = cc;
     return c;
   }
