@@ -53,7 +53,10 @@ struct Cfg {
   // tile is 64 channels so twice as many tiles spread over the SMs; gate/up
   // packs 64 gate and the matching 64 up rows into one 128-row operand.
   static constexpr bool kPacked = BMW == 64;
-  static constexpr int kNumA = (GATEUP && !kPacked) ? 2 : 1;  // MMAs per K step
+  // MMAs per K step: gate and up tiles, or (down, BMW = 256) two 128-channel
+  // halves that share one token tile (its rows are read once per 256
+  // channels instead of once per 128)
+  static constexpr int kNumA = ((GATEUP && !kPacked) || BMW == 256) ? 2 : 1;
   static constexpr int kATile = kBM * kBK;                     // one 128-row operand
   static constexpr int kBTile = BN * kBK;
   static constexpr int kStage = kNumA * kATile + kBTile;
@@ -80,7 +83,8 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
                                     kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(BMW == 64 || BMW == 128, "tile width");
+  static_assert(BMW == 64 || BMW == 128 || (BMW == 256 && !GATEUP && BN == 128),
+                "tile width");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kStages >= 2, "pipeline depth");
 };
@@ -215,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           } else if (GATEUP) {           // packed: 64 gate rows, 64 up rows
             row = wrow + (box == 1 ? N : 0);
             off = box * 64 * kBK;
-          } else {                       // down: the two halves of the tile
+          } else {                       // down: 64-row quarters (halves) of the tile
             row = wrow + box * 64;
-            off = box * 64 * kBK;
+            off = (box >> 1) * C::kATile + (box & 1) * 64 * kBK;
           }
           tma_load_2d(stage_a(s, 0) + off, &tm_w, x, row, full_bar(s), pol);
         } else {
@@ -485,13 +489,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           emit(ti, n0, nvalid, ch0, v);
         }
       } else if (C::kStagedOut) {   // down projection, wide tiles
-        const int ch0 = ti.ctile * BMW + q * 32;
+       for (int which = 0; which < C::kNumA; ++which) {   // 128-channel halves
+        const int ch0 = ti.ctile * BMW + which * 128 + q * 32;
+        const uint32_t ta = taddr + (uint32_t)(which * BN);
         const float sw = w_scale[(int64_t)ti.group * N + ch0 + lane];
         const float swr = sw * rho;
         for (int n0 = 0; n0 < nvalid; n0 += 32) {
           float acc[32], v[32];
-          tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
-          tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
+          tmem_ld_x16(ta + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
+          tmem_ld_x16(ta + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
           tmem_ld_wait();
           if constexpr (OUT16) {
 #pragma unroll
@@ -504,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           }
           emit(ti, n0, nvalid, ch0, v);
         }
+       }
       } else if (GATEUP) {
         const int ch = ti.ctile * kBM + m;
         const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
@@ -717,6 +724,9 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   if (avg <= 16) return run<16, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   if (avg <= 32) return run<32, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   if (avg <= 64) return run<64, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  // 128-token tiles of 256 channels read each token tile once per 256
+  // channels: the SMs' operand feed, not HBM, bounded the 128-channel tiles
+  if (avg <= 128 && N % 256 == 0) return run<128, 256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   if (avg <= 128) return run<128, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   return run<256, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
 }
@@ -741,6 +751,9 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
   if (avg <= 16) MOE_DOWN16(16);
   if (avg <= 32) MOE_DOWN16(32);
   if (avg <= 64) MOE_DOWN16(64);
+  if (avg <= 128 && N % 256 == 0)
+    return run<128, 256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
+                                      nullptr, stream, pdl, o, row_scale, w_bound);
   if (avg <= 128) MOE_DOWN16(128);
   MOE_DOWN16(256);
 #undef MOE_DOWN16

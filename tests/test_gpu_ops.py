@@ -331,6 +331,7 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
     (2, [600, 301], 256, 512, 0),                    # BN 256 (wide tiles)
     (4, [130, 0, 300, 77], 512, 256, 0),             # CTA pairs, BN 128
     (6, [5, 9, 0, 300, 2, 3], 256, 256, 16),         # hint forces BN 16
+    (3, [400, 5, 90], 768, 384, 100),                # BN 128; down: 256-channel tiles
 ])
 def test_grouped_gemm(gateup, G, counts, N, K, hint):
     aq, sa, wq, sw, offs = _grouped_case(G, counts, N, K, gateup,
@@ -375,6 +376,7 @@ def test_scale_max():
     (3, [200, 129, 64], 128, 1024, 0),               # BN 128
     (5, [300, 0, 257, 511, 2], 384, 384, 0),         # BN 256, tails
     (2, [1000, 24], 256, 1536, 0),                   # long K
+    (4, [130, 0, 300, 77], 512, 512, 0),             # BN 128, 256-channel tiles
 ])
 def test_grouped_gemm_down_f16(G, counts, N, K, hint):
     """The fp16 encoding of y: row_scale * y16 against the oracle's y, within
