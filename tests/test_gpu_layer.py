@@ -262,6 +262,38 @@ def test_prenorm_prefill_sampled():
     assert ok, f"prefill prenorm: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
 
 
+def test_forward_on_two_streams_at_once():
+    """Two forwards in flight at once on two streams, each with its own
+    workspace (the ABI's contract: every call is asynchronous on the caller's
+    stream and allocates nothing). Each output equals, bit for bit, the same
+    forward run alone."""
+    import ctypes
+    from expert_layer_ptpc_gb300 import binding
+    cfg = syn.LayerConfig("conc", 2048, 1024, 32, 4, 512, True, "normal")
+    run = _Run(cfg)
+    L = run.layer
+    x1, lg1 = run.inputs(cfg)
+    x2, lg2 = syn.gen_x(cfg, "cuda", 1), syn.gen_logits(cfg, "cuda", 1)
+    ref1 = L.forward(x1, lg1).clone()
+    ref2 = L.forward(x2, lg2).clone()
+    torch.cuda.synchronize()
+    dims = L.dims(cfg.T)
+    need = max(binding.load_library().moe_forward_workspace_size(ctypes.byref(dims)), 1)
+    ws = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    outs = [torch.empty_like(ref1) for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for i, (x, lg) in enumerate(((x1, lg1), (x2, lg2))):
+            binding.moe_forward(dims, x, L.w_gu, L.s_gu, L.w_d, L.s_d, router_logits=lg,
+                                shared_gate_w=L.shared_gate_w, out=outs[i], ws=ws[i],
+                                stream=streams[i])
+    torch.cuda.synchronize()
+    st, bits = binding.moe_device_status()
+    assert st == 0, bits
+    assert torch.equal(outs[0].view(torch.int16), ref1.view(torch.int16))
+    assert torch.equal(outs[1].view(torch.int16), ref2.view(torch.int16))
+
+
 def test_forward_is_deterministic():
     cfg = syn.LayerConfig("det", 2000, 512, 32, 4, 256, True, "normal")
     run = _Run(cfg)
