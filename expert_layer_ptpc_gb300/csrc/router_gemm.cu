@@ -52,7 +52,8 @@ constexpr int kRProds = 4;               // producer warps
 constexpr int kRThreads = 32 * (kRProd0 + kRProds);
 constexpr int kRWarps = kRThreads / 32;
 constexpr int kRBoxRows = 64;            // rows per TMA box (tokens and router matrix)
-constexpr int kRBK = 64;                 // bf16 elements of K per stage (128 bytes)
+constexpr int kRBK = 64;                 // bf16 elements of K per stage (128 bytes),
+                                         // 32 (64 bytes) for the widest expert tiles
 constexpr int kRTile = 128;              // tokens per tile (MMA M)
 constexpr int kRMaxN = 512;              // expert columns (two N = 256 MMAs)
 constexpr int kRMaxK = 16;               // top-k kept in registers (KT <= 16)
@@ -80,6 +81,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand whose rows are `rowb` bytes:
+// 128 (128-byte swizzle) or 64 (64-byte swizzle); 8-row groups 8 * rowb
+// bytes apart. Bits as for smem_desc_k_sw128, swizzle mode 2 or 4.
+__device__ __forceinline__ uint64_t smem_desc_k_sw(uint32_t saddr, int rowb) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((8 * rowb) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(rowb == 128 ? 2 : 4) << 61;
+  return d;
 }
 
 // An unsigned key with the order of the fp32 values (-0 and +0 equal).
@@ -162,6 +175,8 @@ struct RouterGeom {
   int chunk;      // expert columns exchanged per round of the split reduction
   int xbox, nxb;  // token box rows and token boxes per stage
   int wbox, nwb;  // router-matrix box rows and boxes per stage
+  int kb;         // bf16 elements of K per stage: 64, or 32 for 512 expert rows
+                  // (40 KB stages instead of 80 KB: five in flight, not two)
 };
 
 // A stage: 128 token rows (the MMA's A; rows past those loaded are never
@@ -177,8 +192,9 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int n_pad = g.n_pad, stages = g.stages, csplit = g.csplit;
-  const int a_bytes = kRTile * 128;
-  const int stage_bytes = a_bytes + n_pad * 128;
+  const int rowb = 2 * g.kb;                     // bytes of a row's K step
+  const int a_bytes = kRTile * rowb;
+  const int stage_bytes = a_bytes + n_pad * rowb;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -189,7 +205,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = csplit > 1 ? cluster_rank() : 0;
   const int tile0 = (int)(blockIdx.x / csplit) * kRTile;
-  const int kpc = D / kRBK / csplit;            // K blocks of this CTA's slice
+  const int kpc = D / g.kb / csplit;            // K blocks of this CTA's slice
   const int kb0 = (int)rank * kpc;
   const int nbox = g.nxb + g.nwb;
   const int nprod = nbox < kRProds ? nbox : kRProds;
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
     const uint64_t pol = l2_policy_evict_last();
     uint32_t bytes = 0;
     for (int b = prod; b < nbox; b += nprod)
-      bytes += (uint32_t)((b < g.nxb ? g.xbox : g.wbox) * 128);
+      bytes += (uint32_t)((b < g.nxb ? g.xbox : g.wbox) * rowb);
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
@@ -233,10 +249,10 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
       for (int b = prod; b < nbox; b += nprod) {
         if (b < g.nxb) {
           const int r = b * g.xbox;
-          tma_load_2d(st + r * 128, &tm_x, kb * kRBK, tile0 + r, full_bar(s), pol);
+          tma_load_2d(st + r * rowb, &tm_x, kb * g.kb, tile0 + r, full_bar(s), pol);
         } else {
           const int r = (b - g.nxb) * g.wbox;
-          tma_load_2d(st + a_bytes + r * 128, &tm_w, kb * kRBK, r, full_bar(s), pol);
+          tma_load_2d(st + a_bytes + r * rowb, &tm_w, kb * g.kb, r, full_bar(s), pol);
         }
       }
       ++issued;
@@ -261,12 +277,15 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
       if (!mbar_wait_bounded(full_bar(s), ph, abort_flag, err, kErrTimeoutMma)) break;
       tc_fence_after_sync();
       const uint32_t a = smem_u32(smem + s * stage_bytes), b = a + a_bytes;
-#pragma unroll
-      for (int kk = 0; kk < kRBK / 16; ++kk) {   // K = 16 per instruction (32 bytes)
+      // descriptors of the stage; a K step of 32 bytes adds 2 to the
+      // address field (bytes >> 4), 256 expert rows add 16 * rowb
+      const uint64_t da = smem_desc_k_sw(a, rowb), db = smem_desc_k_sw(b, rowb);
+      const int ksteps = g.kb / 16;
+      for (int kk = 0; kk < ksteps; ++kk) {   // K = 16 per instruction (32 bytes)
         const uint32_t acc = (kb != kb0) || (kk != 0);
         for (int h = 0; h < n_pad; h += 256)
-          mma_bf16(tmem_base + (uint32_t)h, smem_desc_k_sw128(a + kk * 32),
-                   smem_desc_k_sw128(b + h * 128 + kk * 32), idesc, acc);
+          mma_bf16(tmem_base + (uint32_t)h, da + (uint64_t)(2 * kk),
+                   db + (uint64_t)((h * rowb) >> 4) + (uint64_t)(2 * kk), idesc, acc);
       }
       mma_commit(empty_bar(s));
       if (++s == stages) {
@@ -511,16 +530,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_bf16() {
 // [rows, D] bf16 as a 2D TMA map: boxes of 64 elements (128 bytes) of K x
 // box_rows rows, 128-byte swizzle; rows past the end read as zero.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int D,
-                    int box_rows) {
+                    int box_rows, int kb) {
   auto fn = encode_fn_bf16();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kRBK, (cuuint32_t)box_rows};
+  const cuuint32_t box[2] = {(cuuint32_t)kb, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            kb == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -542,8 +562,8 @@ int pick_split(Kern kern, RouterGeom& g, int T, int D, size_t smem, cudaLaunchCo
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = (T + kRTile - 1) / kRTile;
-  const int kblocks = D / kRBK;
-  const size_t avail = (size_t)g.stages * (kRTile * 128 + g.n_pad * 128);
+  const int kblocks = D / g.kb;
+  const size_t avail = (size_t)g.stages * (kRTile + g.n_pad) * 2 * g.kb;
   const int rows = T < kRTile ? T : kRTile;
   for (int c = kRMaxCluster; c >= 2; c /= 2) {
     if (kblocks % c != 0 || tiles * c > sms) continue;
@@ -593,7 +613,9 @@ int launch_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int
   if (!router_topk_supported(E, k, D)) return -2;
   RouterGeom g{};
   g.n_pad = E <= 256 ? (E + 15) / 16 * 16 : 512;
-  const int stage_bytes = kRTile * 128 + g.n_pad * 128;
+  // (a single tile's K slices are short: there the larger step wins)
+  g.kb = g.n_pad > 256 && T > kRTile ? 32 : kRBK;
+  const int stage_bytes = (kRTile + g.n_pad) * 2 * g.kb;
   g.stages = (200 * 1024) / stage_bytes;
   if (g.stages > 8) g.stages = 8;
   if (g.stages < 2) g.stages = 2;
@@ -605,8 +627,8 @@ int launch_router_topk(const uint16_t* x, const uint16_t* w_r, int T, int D, int
   while (g.n_pad % g.wbox != 0) g.wbox /= 2;
   g.nwb = g.n_pad / g.wbox;
   CUtensorMap tm_x, tm_w;
-  if (!make_tmap_bf16(&tm_x, x, T, D, g.xbox)) return -3;
-  if (!make_tmap_bf16(&tm_w, w_r, E, D, g.wbox)) return -3;
+  if (!make_tmap_bf16(&tm_x, x, T, D, g.xbox, g.kb)) return -3;
+  if (!make_tmap_bf16(&tm_w, w_r, E, D, g.wbox, g.kb)) return -3;
   const int smem = 1024 + g.stages * stage_bytes + (2 * g.stages + 2) * 8 + 16;
   auto kern = k <= 2 ? router_topk_kernel<2>
               : k <= 4 ? router_topk_kernel<4>
