@@ -139,7 +139,8 @@ def test_quant_scatter_with_extra_rows():
     (64, 256, 8, 2, True), (300, 4096, 128, 8, True), (1000, 2048, 256, 8, True),
     (129, 4096, 512, 10, False), (17, 1024, 40, 3, True), (5, 4096, 300, 16, True),
     (300, 192, 64, 6, False),       # 3 K blocks: no K split, one CTA per tile
-    (600, 192, 300, 8, False)])     # no K split, upper column half partly past E
+    (600, 192, 300, 8, False),      # no K split, upper column half partly past E
+    (33, 256, 8, 1, True), (200, 512, 20, 1, False)])   # k = 1
 def test_router_topk(T, D, E, k, renorm):
     """Router GEMM + top-k in one kernel. The logits (fp32 GEMM) lie within
     the fp32 accumulation bound of the exact dot products; the selection and

@@ -138,6 +138,27 @@ def test_grouped_gemm_scaled(mode, offsets, N, K):
     assert np.all(np.abs(got - y) <= bound)
 
 
+@pytest.mark.parametrize("mode", ["ptpc", "block128"])
+def test_grouped_gemm_scaled_odd_k_blocks(mode):
+    """K = 640: five 128-wide blocks, an odd number of scale groups for
+    BlockScale-128 (512-subchannel needs K a multiple of 512)."""
+    offsets, qa, sa, qw, sw = _problem(mode, [0, 70, 200], 256, 640, 41)
+    out = torch.full((200, 256), float("nan"), dtype=torch.float32, device="cuda")
+    B().moe_grouped_gemm_scaled(MODES[mode], cuda(qa), cuda(sa), cuda(qw), cuda(sw),
+                                cuda(offsets), out=out)
+    assert B().moe_device_status() == (0, 0)
+    y, bound = _expected(mode, offsets, qa, sa, qw, sw)
+    assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - y) <= bound)
+
+
+def test_sub512_rejects_k_off_its_blocks():
+    offsets, qa, sa, qw, sw = _problem("ptpc", [0, 8], 128, 640, 5)
+    with pytest.raises(B().MoeError) as e:
+        B().moe_grouped_gemm_scaled(MODES["sub512"], cuda(qa), cuda(np.ones((8, 1), np.float32)),
+                                    cuda(qw), cuda(sw), cuda(offsets))
+    assert e.value.status == -2          # MOE_ERR_UNSUPPORTED, before any launch
+
+
 def test_rows_outside_every_group_untouched():
     offsets, qa, sa, qw, sw = _problem("block128", [0, 100], 128, 256, 3)
     qa = np.concatenate([qa, qa[:28]])            # 28 rows owned by no group
