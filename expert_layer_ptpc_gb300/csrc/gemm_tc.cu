@@ -46,7 +46,7 @@ using namespace gemm;
 
 constexpr int kBM = 128;   // output channels per tile (MMA M)
 
-template <int BN, int BMW, bool GATEUP>
+template <int BN, int BMW, bool GATEUP, bool OUT16 = false>
 struct Cfg {
   // BMW = output channels per tile. 128: the MMA's 128 rows are 128 channels
   // (gate/up: a second MMA for the up rows). 64: for small token tiles, a
@@ -87,12 +87,18 @@ struct Cfg {
                 "tile width");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kStages >= 2, "pipeline depth");
+  // fp16 down output with staged stores: four more epilogue warps (12-15,
+  // the same TMEM lane quarters) take every other 32-token chunk; their
+  // fp16 boxes fit the same staging bytes
+  static constexpr bool kWideEpi = kStagedOut && OUT16;
+  static constexpr int kEpiSets = kWideEpi ? 2 : 1;
+  static constexpr int kThreadsT = kThreads + (kWideEpi ? 4 * 32 : 0);
 };
 
 // OUT16 (down projection only): y is written as fp16 codes with one fp32
 // factor per row instead of fp32 values (see the down epilogue).
 template <int BN, int BMW, bool GATEUP, bool OUT16>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
+__global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16>::kThreadsT, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     __half* __restrict__ out16, float* __restrict__ row_scale,
     const float* __restrict__ w_bound, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
-  using C = Cfg<BN, BMW, GATEUP>;
+  using C = Cfg<BN, BMW, GATEUP, OUT16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
-  __shared__ int warp_tot[kThreads / 32 + 1];
+  __shared__ int warp_tot[C::kThreadsT / 32 + 1];
   __shared__ Sched sched;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -141,13 +147,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);     // one per epilogue warp
+      mbar_init(acce_bar(b), 4 * C::kEpiSets);   // one per epilogue warp
     }
     mbar_init(drain_bar, 1);
     mbar_init(xfull_bar, 64);
     mbar_init(xempty_bar, 64);
     // ring consumers: each producer, the MMA issuer, each epilogue warp
-    sched_init(sched, C::kBoxes + 1 + 4);
+    sched_init(sched, C::kBoxes + 1 + 4 * C::kEpiSets);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
 
   // tile prefix: prefix[g] = sum_{g' < g} ceil(rows_g' / BN) * n_ctiles
   {
-    const int per = (groups + kThreads - 1) / kThreads;
+    const int per = (groups + C::kThreadsT - 1) / C::kThreadsT;
     const int g0 = threadIdx.x * per;
     int local = 0;
     for (int g = g0; g < g0 + per && g < groups; ++g)
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       prefix[g] = run;
       run += ((offsets[g + 1] - offsets[g] + BN - 1) / BN) * n_ctiles;
     }
-    if (threadIdx.x == kThreads - 1) prefix[groups] = base + incl;
+    if (threadIdx.x == C::kThreadsT - 1) prefix[groups] = base + incl;
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -367,7 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     // ch0 + lane. A full 32-token box inside the expert goes through shared
     // memory and one TMA store; a partial box at the expert's end is stored
     // directly, so rows of the next expert are never written.
-    float* obuf = outstage + (warp - kEpiWarp0) * 32 * 32;   // [token][channel]
+    // [token][channel]; epilogue warp index e = 0..3 (warps 1-4), 4..7 (12-15)
+    const int e_idx = warp < kSchedWarp ? warp - kEpiWarp0 : warp - kSchedWarp + 3;
+    const int eset = warp < kSchedWarp ? 0 : 1;
+    float* obuf = OUT16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(outstage) +
+                                                   e_idx * 32 * 32)
+                        : outstage + e_idx * 32 * 32;
     auto emit = [&](const TileInfo& ti, int n0, int nvalid, int ch0,
                     const float (&v)[32]) {
       if (n0 + 32 <= nvalid) {
@@ -494,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         const uint32_t ta = taddr + (uint32_t)(which * BN);
         const float sw = w_scale[(int64_t)ti.group * N + ch0 + lane];
         const float swr = sw * rho;
-        for (int n0 = 0; n0 < nvalid; n0 += 32) {
+        for (int n0 = 32 * eset; n0 < nvalid; n0 += 32 * C::kEpiSets) {
           float acc[32], v[32];
           tmem_ld_x16(ta + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
           tmem_ld_x16(ta + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
@@ -574,7 +585,7 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
         const float* w_scale, const int32_t* offsets, int groups, int N, int K,
         float* out, cudaStream_t stream, bool pdl, __half* out16 = nullptr,
         float* row_scale = nullptr, const float* w_bound = nullptr) {
-  using C = Cfg<BN, BMW, GATEUP>;
+  using C = Cfg<BN, BMW, GATEUP, OUT16>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;
@@ -603,7 +614,7 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)upper);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreadsT);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
