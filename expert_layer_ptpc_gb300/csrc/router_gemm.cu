@@ -39,6 +39,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "gemm_common.cuh"
 
@@ -280,13 +281,20 @@ __global__ void __launch_bounds__(kRThreads, 1) router_topk_kernel(
       // descriptors of the stage; a K step of 32 bytes adds 2 to the
       // address field (bytes >> 4), 256 expert rows add 16 * rowb
       const uint64_t da = smem_desc_k_sw(a, rowb), db = smem_desc_k_sw(b, rowb);
-      const int ksteps = g.kb / 16;
-      for (int kk = 0; kk < ksteps; ++kk) {   // K = 16 per instruction (32 bytes)
-        const uint32_t acc = (kb != kb0) || (kk != 0);
-        for (int h = 0; h < n_pad; h += 256)
-          mma_bf16(tmem_base + (uint32_t)h, da + (uint64_t)(2 * kk),
-                   db + (uint64_t)((h * rowb) >> 4) + (uint64_t)(2 * kk), idesc, acc);
-      }
+      // K = 16 per instruction (32 bytes): 4 or 2 per stage, fully unrolled
+      // (the issuing thread's instruction count is on the critical path)
+      auto issue = [&](auto ksteps) {
+#pragma unroll
+        for (int kk = 0; kk < decltype(ksteps)::value; ++kk) {
+          const uint32_t acc = (kb != kb0) || (kk != 0);
+          mma_bf16(tmem_base, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, acc);
+          if (n_pad > 256)
+            mma_bf16(tmem_base + 256u, da + (uint64_t)(2 * kk),
+                     db + (uint64_t)((256 * rowb) >> 4) + (uint64_t)(2 * kk), idesc, acc);
+        }
+      };
+      if (g.kb == 64) issue(std::integral_constant<int, 4>{});
+      else issue(std::integral_constant<int, 2>{});
       mma_commit(empty_bar(s));
       if (++s == stages) {
         s = 0;
