@@ -70,7 +70,11 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
 // The same reduction over the down projection's fp16 encoding: the row
 // factor folds into the slot weight, c_j = w[t, j] * row_scale[r_j], and
 // out = bf16_rne( sum_j c_j * y16[r_j] + (gate[t] * row_scale_shared[t]) *
-// y16_shared[t] ), in fp32 and slot order like combine_kernel.
+// y16_shared[t] ), in fp32 and slot order like combine_kernel. A thread
+// covers VEC columns (VEC / 8 16-byte loads per slot): 16 where D allows, so
+// that each block's dependent prologue (routing map, then row factors) is
+// paid once per 32 bytes of every slot row instead of once per 16.
+template <int VEC>
 __global__ void __launch_bounds__(kThreads) combine_f16_kernel(
     const __half* __restrict__ y16, const float* __restrict__ row_scale,
     const int32_t* __restrict__ f2s, const float* __restrict__ topk_w, int k, int D,
@@ -87,29 +91,39 @@ __global__ void __launch_bounds__(kThreads) combine_f16_kernel(
     coef[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x] * row_scale[r];
   }
   __syncthreads();
-  const int c = (blockIdx.y * kThreads + threadIdx.x) * kVec;
+  const int c = (blockIdx.y * kThreads + threadIdx.x) * VEC;
   if (c >= D) return;
-  float acc[kVec];
+  constexpr int kLd = VEC / 8;
+  float acc[VEC];
 #pragma unroll
-  for (int i = 0; i < kVec; ++i) acc[i] = 0.f;
+  for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
   auto add = [&](const __half* src, float w) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(src);
-    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+    uint4 raw[kLd];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __half22float2(h[i]);
-      acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
-      acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+    for (int l = 0; l < kLd; ++l) raw[l] = reinterpret_cast<const uint4*>(src)[l];
+#pragma unroll
+    for (int l = 0; l < kLd; ++l) {
+      const __half2* h = reinterpret_cast<const __half2*>(&raw[l]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h[i]);
+        acc[8 * l + 2 * i] = fmaf(w, f.x, acc[8 * l + 2 * i]);
+        acc[8 * l + 2 * i + 1] = fmaf(w, f.y, acc[8 * l + 2 * i + 1]);
+      }
     }
   };
   for (int j = 0; j < k; ++j) add(y16 + (int64_t)rows[j] * D + c, coef[j]);
   if (y16_shared != nullptr)
     add(y16_shared + (int64_t)t * D + c, gate[t] * row_scale_shared[t]);
-  uint4 packed;
-  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&packed);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-  *reinterpret_cast<uint4*>(out + (int64_t)t * D + c) = packed;
+  for (int l = 0; l < kLd; ++l) {
+    uint4 packed;
+    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      p[i] = __floats2bfloat162_rn(acc[8 * l + 2 * i], acc[8 * l + 2 * i + 1]);
+    *reinterpret_cast<uint4*>(out + (int64_t)t * D + c + 8 * l) = packed;
+  }
 }
 
 }  // namespace
@@ -121,12 +135,16 @@ cudaError_t launch_combine_f16(const uint16_t* y16, const float* row_scale,
                                const float* shared_gate, uint16_t* out,
                                cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid((unsigned)T, (unsigned)((D / kVec + kThreads - 1) / kThreads));
-  return launch_kernel(pdl, grid, dim3(kThreads), 0, stream, combine_f16_kernel,
-                       reinterpret_cast<const __half*>(y16), row_scale, f2s, topk_w,
-                       k, D, reinterpret_cast<const __half*>(y16_shared),
-                       row_scale_shared, shared_gate,
-                       reinterpret_cast<__nv_bfloat16*>(out));
+  auto go = [&](auto kern, int vec) {
+    const dim3 grid((unsigned)T, (unsigned)((D / vec + kThreads - 1) / kThreads));
+    return launch_kernel(pdl, grid, dim3(kThreads), 0, stream, kern,
+                         reinterpret_cast<const __half*>(y16), row_scale, f2s, topk_w,
+                         k, D, reinterpret_cast<const __half*>(y16_shared),
+                         row_scale_shared, shared_gate,
+                         reinterpret_cast<__nv_bfloat16*>(out));
+  };
+  if (D % 16 == 0) return go(combine_f16_kernel<16>, 16);
+  return go(combine_f16_kernel<8>, 8);
 }
 
 cudaError_t launch_combine(const float* y, const int32_t* f2s,

@@ -22,7 +22,7 @@ namespace {
 
 constexpr int kVec = 16;        // elements per thread per unit (16 bytes of codes)
 constexpr int kMaxThreads = 512;
-constexpr int kWarpsPerBlock = 8;   // shared-gate kernel
+constexpr int kWarpsPerBlock = 8;   // rows per block of the warp-per-row kernels
 
 __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&v)[kVec]) {
 #pragma unroll
@@ -97,10 +97,11 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
   // destination rows of this row
   const int nmain = dst_rows != nullptr ? copies : 1;
   const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
-  if (tid < ndst) {
-    dst[tid] = tid < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + tid] : r)
-                           : extra_row_base + r;
-  }
+  // strided: a block narrower than ndst (32 threads, 32 copies + the shared
+  // row) still fills every entry
+  for (int i = tid; i < ndst; i += blockDim.x)
+    dst[i] = i < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + i] : r)
+                       : extra_row_base + r;
   __syncthreads();
   if (warp == 0) {
     float a = lane < nwarps ? red_max[lane] : 0.f;
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
   }
   __syncthreads();
   const float s = __fdiv_rn(fmaxf(red_max[0], 1e-12f), 448.0f);
-  if (tid < ndst) out_scale[dst[tid]] = s;
+  for (int i = tid; i < ndst; i += blockDim.x) out_scale[dst[i]] = s;
   if (gate_w != nullptr && tid == 0) gate_out[r] = 1.0f / (1.0f + expf(-red_dot[0]));
 
 #pragma unroll
@@ -133,6 +134,85 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
       const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
       for (int d = 0; d < ndst; ++d)
         *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
+    }
+  }
+}
+
+// The same quantiser for rows of at most 64 vectors (1024 elements): one warp
+// per row and kWarpsPerBlock rows per block, so that narrow rows (h of a
+// 512-wide expert) are not one single-warp block each, and the reductions
+// stay in the warp. The row maximum is order-independent, so scales and
+// codes equal quant_rows_kernel's bit for bit; only the gate's dot product is
+// summed in another order (lane's units first, then across the warp).
+template <typename InT, int UNITS>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_warp_kernel(
+    const InT* __restrict__ in, int64_t rows, int cols,
+    const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
+    uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
+    const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out,
+    int release_early) {
+  if (release_early) pdl_launch_dependents();
+  pdl_wait();
+  if (!release_early) pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (r >= rows) return;   // whole warps: r is uniform within a warp
+  const int nunits = cols / kVec;
+  const InT* row = in + r * cols;
+
+  float v[UNITS][kVec];
+  float amax = 0.f, dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = lane + 32 * i;
+    if (u < nunits) {
+      load_vec(row + u * kVec, v[i]);
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+      if (gate_w != nullptr) {
+        float g[kVec];
+        load_vec(gate_w + u * kVec, g);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) dot = fmaf(v[i][j], g[j], dot);
+      }
+    }
+  }
+  // destination rows: lane d holds the d-th (the launcher sends rows with at
+  // most 32 destinations here)
+  const int nmain = dst_rows != nullptr ? copies : 1;
+  const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
+  int64_t my_dst = 0;
+  if (lane < ndst)
+    my_dst = lane < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + lane] : r)
+                          : extra_row_base + r;
+  amax = warp_max(amax);
+  const float s = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+  if (lane < ndst) out_scale[my_dst] = s;
+  if (gate_w != nullptr) {
+    dot = warp_sum(dot);
+    if (lane == 0) gate_out[r] = 1.0f / (1.0f + expf(-dot));
+  }
+
+#pragma unroll
+  for (int i = 0; i < UNITS; ++i) {
+    const int u = lane + 32 * i;
+    uint4 packed = make_uint4(0u, 0u, 0u, 0u);
+    if (u < nunits) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[i][4 * q], s),
+                                            __fdiv_rn(v[i][4 * q + 1], s));
+        const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[i][4 * q + 2], s),
+                                            __fdiv_rn(v[i][4 * q + 3], s));
+        w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      packed = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // every lane takes part in the shuffles; only lanes with a unit store
+    for (int d = 0; d < ndst; ++d) {
+      const int64_t dd = __shfl_sync(0xffffffffu, my_dst, d);
+      if (u < nunits) *reinterpret_cast<uint4*>(out_q + dd * cols + u * kVec) = packed;
     }
   }
 }
@@ -271,10 +351,11 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
   }
   const int nmain = dst_rows != nullptr ? copies : 1;
   const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
-  if (tid < ndst) {
-    dst[tid] = tid < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + tid] : r)
-                           : extra_row_base + r;
-  }
+  // strided: a block narrower than ndst (32 threads, 32 copies + the shared
+  // row) still fills every entry
+  for (int i = tid; i < ndst; i += blockDim.x)
+    dst[i] = i < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + i] : r)
+                       : extra_row_base + r;
   __syncthreads();
   if (warp == 0) {
     float a = lane < nwarps ? red_max[lane] : 0.f;
@@ -288,7 +369,7 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
   }
   __syncthreads();
   const float s = __fdiv_rn(fmaxf(red_max[0], 1e-12f), 448.0f);
-  if (tid < ndst) out_scale[dst[tid]] = s;
+  for (int i = tid; i < ndst; i += blockDim.x) out_scale[dst[i]] = s;
   if (gate_w != nullptr && tid == 0) gate_out[r] = 1.0f / (1.0f + expf(-red_dot[0]));
 #pragma unroll
   for (int i = 0; i < UNITS; ++i) {
@@ -337,6 +418,17 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
                         float* gate_out, cudaStream_t stream, bool pdl,
                         bool release_early) {
   const int nunits = cols / kVec;
+  const int ndst = (dst_rows != nullptr ? copies : 1) + (extra_row_base >= 0 ? 1 : 0);
+  if (nunits <= 64 && ndst <= 32) {
+    const dim3 grid((unsigned)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock));
+    auto go = [&](auto kern) {
+      return launch_kernel(pdl, grid, dim3(kWarpsPerBlock * 32), 0, stream, kern, in,
+                           rows, cols, dst_rows, copies, extra_row_base, out_q,
+                           out_scale, gate_w, gate_out, release_early ? 1 : 0);
+    };
+    if (nunits <= 32) return go(quant_rows_warp_kernel<InT, 1>);
+    return go(quant_rows_warp_kernel<InT, 2>);
+  }
   int threads = std::min(kMaxThreads, ((nunits + 31) / 32) * 32);
   const int units = (nunits + threads - 1) / threads;
   const dim3 grid((unsigned)rows), block(threads);

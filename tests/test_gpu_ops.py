@@ -97,6 +97,9 @@ def test_permute(T, E, k, skew):
 @pytest.mark.parametrize("dtype,rows,cols", [
     ("bf16", 64, 256), ("bf16", 33, 4096), ("f32", 130, 1536),
     ("f32", 7, 128), ("bf16", 5, 16), ("f32", 3, 8192),
+    # one warp per row up to 1024 columns: one or two vectors per lane, a
+    # ragged 17-vector row, rows not a multiple of the block's eight warps
+    ("f32", 1001, 512), ("f32", 77, 1024), ("bf16", 19, 272), ("f32", 5, 1040),
 ])
 def test_quant_exact(dtype, rows, cols):
     rng = np.random.default_rng(rows * cols)
@@ -116,9 +119,13 @@ def test_quant_exact(dtype, rows, cols):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
-def test_quant_scatter_with_extra_rows():
-    rng = np.random.default_rng(3)
-    T, D, k = 40, 512, 3
+@pytest.mark.parametrize("T,D,k", [
+    (40, 512, 3), (45, 2048, 3),
+    (21, 256, 31),    # 32 destinations: one lane each
+    (21, 256, 32),    # 33 destinations: the block-per-row kernel
+])
+def test_quant_scatter_with_extra_rows(T, D, k):
+    rng = np.random.default_rng(3 + k)
     x = torch.from_numpy(rng.standard_normal((T, D)).astype(np.float32)).to(
         torch.bfloat16)
     perm = rng.permutation(T * k).astype(np.int32)
@@ -205,7 +212,8 @@ def test_router_topk_full_size(name, T):
 @pytest.mark.parametrize("T,D,k,shared,inplace,wide", [
     (1, 256, 1, False, False, False), (37, 512, 4, True, False, False),
     (300, 4096, 8, False, True, False), (64, 7168, 2, True, True, False),
-    (200, 2048, 2, False, False, True)])
+    (200, 2048, 2, False, False, True),
+    (21, 256, 32, True, False, False)])   # 33 destinations, 32-thread blocks
 def test_add_rmsnorm_quant(T, D, k, shared, inplace, wide):
     """Fused add + RMSNorm + quant against the oracle: the new residual, the
     codes at every destination row and the scales bit for bit, the gate
@@ -436,7 +444,10 @@ def test_combine(T, k, D, shared):
 
 
 @pytest.mark.parametrize("T,k,D,shared", [(64, 2, 256, False), (17, 8, 4096, True),
-                                          (5, 10, 1024, True), (1, 1, 128, False)])
+                                          (5, 10, 1024, True), (1, 1, 128, False),
+                                          # 8 columns a thread (D not a multiple
+                                          # of 16); a ragged third block column
+                                          (9, 8, 2056, True), (3, 4, 4112, False)])
 def test_combine_f16(T, k, D, shared):
     rng = np.random.default_rng(T * k + D + 1)
     R = T * k
