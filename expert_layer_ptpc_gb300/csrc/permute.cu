@@ -20,8 +20,12 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunk = 8192;                 // flat entries per block
-constexpr int kSub = kChunk / kWarps;        // entries per warp
+// Flat entries per block: up to kSmallChunk entries are sorted by one block
+// (one launch); larger inputs take three launches over kChunk-entry chunks,
+// small enough that every chunk's serial work is short and the chunks
+// spread over many SMs.
+constexpr int kSmallChunk = 8192;
+constexpr int kChunk = 2048;
 
 // Exclusive prefix sum of vals[0..n) in shared memory (n <= 2 * kThreads),
 // in place; returns the total. All threads of the block must call it.
@@ -61,30 +65,31 @@ __device__ int block_exclusive_scan(int* vals, int n, int* warp_tot) {
   return total;
 }
 
-constexpr int kPerLane = kSub / 32;         // entries a lane holds
+// A chunk of PL * kThreads entries: warp w owns the sub-chunk of PL * 32
+// entries starting at PL * 32 w, lane l holds its entries 32 i + l.
 
 // Load this warp's sub-chunk: lane holds entries begin + 32 i + lane
-// (i < kPerLane); -1 past the end.
+// (i < PL); -1 past the end. All loads are issued before any is used.
+template <int PL>
 __device__ __forceinline__ void load_warp_ids(const int32_t* __restrict__ ids,
-                                              int64_t f0, int64_t R,
-                                              int (&e)[kPerLane]) {
+                                              int64_t f0, int64_t R, int (&e)[PL]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t begin = f0 + (int64_t)warp * kSub;
+  const int64_t begin = f0 + (int64_t)warp * (PL * 32);
 #pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
+  for (int i = 0; i < PL; ++i) {
     const int64_t f = begin + 32 * i + lane;
     e[i] = f < R ? ids[f] : -1;
   }
 }
 
 // Per-warp expert histograms of one chunk: whist[w * E + e].
-__device__ void chunk_warp_histograms(const int (&e)[kPerLane], int E,
-                                      int* whist) {
+template <int PL>
+__device__ void chunk_warp_histograms(const int (&e)[PL], int E, int* whist) {
   for (int i = threadIdx.x; i < kWarps * E; i += kThreads) whist[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int i = 0; i < kPerLane; ++i)
+  for (int i = 0; i < PL; ++i)
     if (e[i] >= 0) atomicAdd(&whist[warp * E + e[i]], 1);
   __syncthreads();
 }
@@ -105,14 +110,15 @@ __device__ void warp_bases(const int* base, int E, int* whist) {
 
 // Stable scatter of one chunk given per-warp starting rows. 32 consecutive
 // entries at a time: lanes with the same expert are ranked by lane order.
-__device__ void chunk_scatter(const int (&e)[kPerLane], int64_t f0, int64_t R,
-                              int E, int* whist, int32_t* __restrict__ s2f,
+template <int PL>
+__device__ void chunk_scatter(const int (&e)[PL], int64_t f0, int64_t R, int E,
+                              int* whist, int32_t* __restrict__ s2f,
                               int32_t* __restrict__ f2s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* base = whist + warp * E;
-  const int64_t begin = f0 + (int64_t)warp * kSub;
+  const int64_t begin = f0 + (int64_t)warp * (PL * 32);
 #pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
+  for (int i = 0; i < PL; ++i) {
     if (begin + 32 * i >= R) break;               // warp-uniform
     const int64_t f = begin + 32 * i + lane;
     const bool valid = e[i] >= 0;
@@ -138,7 +144,7 @@ __device__ void write_extra_group(int E, int total, int extra,
   }
 }
 
-// R <= kChunk: everything in one block.
+// R <= kSmallChunk: everything in one block.
 __global__ void __launch_bounds__(kThreads) permute_small_kernel(
     const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ s2f,
@@ -149,9 +155,10 @@ __global__ void __launch_bounds__(kThreads) permute_small_kernel(
   int* warp_tot = scan + E + 1;            // kWarps + 1
   pdl_wait();
   pdl_launch_dependents();
-  int mine[kPerLane];
-  load_warp_ids(ids, 0, R, mine);
-  chunk_warp_histograms(mine, E, whist);
+  constexpr int PL = kSmallChunk / kThreads;
+  int mine[PL];
+  load_warp_ids<PL>(ids, 0, R, mine);
+  chunk_warp_histograms<PL>(mine, E, whist);
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int c = 0;
     for (int w = 0; w < kWarps; ++w) c += whist[w * E + e];
@@ -164,10 +171,10 @@ __global__ void __launch_bounds__(kThreads) permute_small_kernel(
   if (threadIdx.x == 0) offsets[E] = total;
   write_extra_group(E, total, extra, counts, offsets);
   warp_bases(scan, E, whist);
-  chunk_scatter(mine, 0, R, E, whist, s2f, f2s);
+  chunk_scatter<PL>(mine, 0, R, E, whist, s2f, f2s);
 }
 
-// R > kChunk, pass 1: per-chunk expert counts -> hist[c * E + e].
+// R > kSmallChunk, pass 1: per-chunk expert counts -> hist[c * E + e].
 __global__ void __launch_bounds__(kThreads) permute_hist_kernel(
     const int32_t* __restrict__ ids, int64_t R, int E, int* __restrict__ hist) {
   extern __shared__ int smem[];
@@ -175,11 +182,18 @@ __global__ void __launch_bounds__(kThreads) permute_hist_kernel(
   pdl_launch_dependents();
   const int64_t f0 = (int64_t)blockIdx.x * kChunk;
   for (int i = threadIdx.x; i < E; i += kThreads) smem[i] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < kChunk; i += kThreads) {
-    const int64_t f = f0 + i;
-    if (f < R) atomicAdd(&smem[ids[f]], 1);
+  // every load in flight before the first atomic
+  constexpr int PL = kChunk / kThreads;
+  int e[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int64_t f = f0 + threadIdx.x + (int64_t)i * kThreads;
+    e[i] = f < R ? ids[f] : -1;
   }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < PL; ++i)
+    if (e[i] >= 0) atomicAdd(&smem[e[i]], 1);
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += kThreads)
     hist[(int64_t)blockIdx.x * E + i] = smem[i];
@@ -229,17 +243,18 @@ __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
   const int64_t f0 = (int64_t)blockIdx.x * kChunk;
   for (int e = threadIdx.x; e < E; e += kThreads)
     base[e] = hist[(int64_t)blockIdx.x * E + e];
-  int mine[kPerLane];
-  load_warp_ids(ids, f0, R, mine);
-  chunk_warp_histograms(mine, E, whist);
+  constexpr int PL = kChunk / kThreads;
+  int mine[PL];
+  load_warp_ids<PL>(ids, f0, R, mine);
+  chunk_warp_histograms<PL>(mine, E, whist);
   warp_bases(base, E, whist);
-  chunk_scatter(mine, f0, R, E, whist, s2f, f2s);
+  chunk_scatter<PL>(mine, f0, R, E, whist, s2f, f2s);
 }
 
 }  // namespace
 
 size_t permute_ws_bytes(int64_t R, int E) {
-  if (R <= kChunk) return 0;
+  if (R <= kSmallChunk) return 0;
   const int64_t nchunks = (R + kChunk - 1) / kChunk;
   return (size_t)(nchunks * E * sizeof(int));
 }
@@ -248,7 +263,7 @@ cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
                            int32_t* counts, int32_t* offsets, int32_t* s2f,
                            int32_t* f2s, int extra_group_rows, void* ws,
                            cudaStream_t stream, bool pdl) {
-  if (R <= kChunk) {
+  if (R <= kSmallChunk) {
     const size_t smem = (size_t)(kWarps * E + E + 1 + kWarps + 1) * sizeof(int);
     cudaError_t err = cudaFuncSetAttribute(
         permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

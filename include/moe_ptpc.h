@@ -137,8 +137,8 @@ MOE_API int moe_permute(const int32_t* topk_ids, int T, int E, int k,
  *   Inputs, outputs, results and errors are those of moe_permute; there is no
  *   workspace argument. Scratch: a fixed 1 MiB device array inside the
  *   library (held on every GPU that loads the library until the process
- *   exits), enough for T * k <= 8192 * floor(262144 / E) flat entries (for
- *   E = 128: 16,777,216; for E = 1024: 2,097,152). Larger calls return
+ *   exits), enough for T * k <= 2048 * floor(262144 / E) flat entries (for
+ *   E = 128: 4,194,304; for E = 1024: 524,288). Larger calls return
  *   MOE_ERR_UNSUPPORTED before launching anything.
  *   The first call on each device (with that device current) looks up the
  *   array's device address; make it before any stream capture on the device.

@@ -104,4 +104,7 @@ def test_argument_errors_need_no_gpu(lib):
 
 def test_permute_workspace_size(lib):
     assert lib.moe_permute_workspace_size(16, 128, 8) == 0          # one block
-    assert lib.moe_permute_workspace_size(8192, 128, 8) == 8 * 128 * 4
+    assert lib.moe_permute_workspace_size(1024, 128, 8) == 0        # 8192 entries
+    # one int histogram row per chunk of 2048 flat entries (ragged last chunk)
+    assert lib.moe_permute_workspace_size(8192, 128, 8) == 32 * 128 * 4
+    assert lib.moe_permute_workspace_size(1025, 128, 8) == 5 * 128 * 4

@@ -76,11 +76,15 @@ def test_route(T, E, k, renorm, ties):
     (64, 8, 2, False), (1, 512, 10, False), (16, 128, 8, False),
     (3000, 64, 6, True), (8192, 128, 8, False), (4096, 256, 8, True),
     (20000, 1024, 4, True), (5, 7, 7, False),
+    (2049, 16, 4, False),      # 8196 entries: four past the one-block path
+    (5000, 256, 8, "hot"),     # every token picks expert 3 (one counter)
 ])
 def test_permute(T, E, k, skew):
     rng = np.random.default_rng(T * 7 + E)
     logits = rng.standard_normal((T, E)).astype(np.float32)
-    if skew:   # many experts empty
+    if skew == "hot":
+        logits[:, 3] += 30.0
+    elif skew:   # many experts empty
         logits[:, : E // 2] -= 20.0
     ids, _ = oracle.route_ref(logits, k)
     counts, offsets, s2f, f2s = B().moe_permute(cuda(ids), E)

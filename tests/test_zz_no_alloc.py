@@ -67,9 +67,9 @@ def test_noalloc_permute_rejects_oversize():
     require_gpu()
     lib = ensure_library()
     # 1 MiB of scratch holds 256 histogram rows of E = 1024: at most 256
-    # chunks of 8192 flat entries
+    # chunks of 2048 flat entries; one token more is refused
     E, k = 1024, 8
-    T = 256 * 8192 // k + 1
+    T = 256 * 2048 // k + 1
     rc = lib.moe_permute_noalloc(ctypes.c_void_p(16), T, E, k,
                                  ctypes.c_void_p(16), ctypes.c_void_p(16),
                                  ctypes.c_void_p(16), ctypes.c_void_p(16), None)
