@@ -104,6 +104,7 @@ def test_permute(T, E, k, skew):
     # one warp per row up to 1024 columns: one or two vectors per lane, a
     # ragged 17-vector row, rows not a multiple of the block's eight warps
     ("f32", 1001, 512), ("f32", 77, 1024), ("bf16", 19, 272), ("f32", 5, 1040),
+    ("bf16", 41, 2048), ("f32", 9, 2064),
 ])
 def test_quant_exact(dtype, rows, cols):
     rng = np.random.default_rng(rows * cols)
