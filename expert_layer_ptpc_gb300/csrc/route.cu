@@ -7,6 +7,7 @@
 // fp32 logits (ties to the lower expert index).
 #include "common.cuh"
 #include "internal.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -50,11 +51,10 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_r, int T,
 }
 
 // ---------------------------------------------------------------------------
-// Top-k: one warp per token. Lane l holds logits l, l+32, ... (NPL of them) in
-// registers. Each of k rounds takes every lane's best untaken entry and
-// reduces (value, index) over the warp: larger value wins, equal values go to
-// the lower index. Lane j keeps the j-th winner, then the warp forms the
-// softmax weights.
+// Top-k: one warp per token, the warp selection of topk.cuh on the token's
+// row of logits (held as order keys in registers: k rounds of a max and a
+// min reduction over the warp; the chosen values and the softmax sum read
+// the row again, from L1).
 // ---------------------------------------------------------------------------
 template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(
@@ -63,67 +63,9 @@ __global__ void __launch_bounds__(256) route_kernel(
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (t >= T) return;
-  const int lane = (int)lane_id();
-  const float* row = logits + (int64_t)t * E;
-  float v[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? row[e] : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float my_val = -INFINITY;
-  int my_idx = 0;
-  for (int j = 0; j < k; ++j) {
-    // this lane's best untaken entry (scan in increasing index order, strict
-    // comparison keeps the lowest index among equal values)
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      const bool ok = e < E && !((taken >> i) & 1u);
-      if (ok && (v[i] > bv || bi == 0x7fffffff)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (j == lane) {
-      my_val = bv;
-      my_idx = bi;
-    }
-  }
-  // weights
-  const float top = __shfl_sync(0xffffffffu, my_val, 0);
-  float denom;
-  if (renormalize) {
-    const float p = lane < k ? expf(my_val - top) : 0.f;
-    denom = warp_sum(p);
-  } else {
-    // softmax over all E: the maximum of all logits is the top-1 logit
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) s += expf(v[i] - top);
-    }
-    denom = warp_sum(s);
-  }
-  if (lane < k) {
-    ids[(int64_t)t * k + lane] = my_idx;
-    weights[(int64_t)t * k + lane] = expf(my_val - top) / denom;
-  }
+  if (t >= T) return;   // whole warps
+  select_warp<NPL>(logits + (int64_t)t * E, E, k, renormalize, t, ids, weights,
+                   nullptr);
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k,
