@@ -46,7 +46,7 @@ using namespace gemm;
 
 constexpr int kBM = 128;   // output channels per tile (MMA M)
 
-template <int BN, int BMW, bool GATEUP, bool OUT16 = false>
+template <int BN, int BMW, bool GATEUP, bool OUT16 = false, int MINB = 1>
 struct Cfg {
   // BMW = output channels per tile. 128: the MMA's 128 rows are 128 channels
   // (gate/up: a second MMA for the up rows). 64: for small token tiles, a
@@ -68,7 +68,13 @@ struct Cfg {
   static constexpr int kTBoxes = BN / kTBoxRows;
   static constexpr int kBoxes = kWBoxes + kTBoxes;
   static_assert(kBoxes <= kMaxBoxes, "one producer warp per box");
-  static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
+  // MINB = 2: two CTAs share an SM, each with half the stage budget. For
+  // tiles of at most 16 tokens, which stream their weights once with almost
+  // no tensor work: one CTA's per-tile overhead (epilogue, tile hand-over)
+  // then overlaps the other's streaming, and an SM given a second tile of a
+  // launch with fewer tiles than two per SM streams both at once.
+  static constexpr int kBudget = MINB == 2 ? 96 * 1024 : kStageBudget;
+  static constexpr int kStages = (kBudget / kStage) > 10 ? 10 : (kBudget / kStage);
   static constexpr int kAccCols = kNumA * BN;                  // one buffer
   // two accumulator buffers (epilogue of one tile overlaps the next tile's
   // MMAs) when they fit in the 512 TMEM columns, else one
@@ -83,6 +89,9 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
                                     kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(MINB == 1 || (MINB == 2 && 2 * (kSmemBytes + 1024) <= 233472 &&
+                              2 * kTmemCols <= 512),
+                "two CTAs per SM");
   static_assert(BMW == 64 || BMW == 128 || (BMW == 256 && !GATEUP && BN == 128),
                 "tile width");
   static_assert(kTmemCols <= 512, "TMEM budget");
@@ -97,8 +106,9 @@ struct Cfg {
 
 // OUT16 (down projection only): y is written as fp16 codes with one fp32
 // factor per row instead of fp32 values (see the down epilogue).
-template <int BN, int BMW, bool GATEUP, bool OUT16>
-__global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16>::kThreadsT, 1) grouped_gemm_kernel(
+template <int BN, int BMW, bool GATEUP, bool OUT16, int MINB>
+__global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, MINB)
+    grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16>::kThreadsT, 1) gro
     __half* __restrict__ out16, float* __restrict__ row_scale,
     const float* __restrict__ w_bound, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
-  using C = Cfg<BN, BMW, GATEUP, OUT16>;
+  using C = Cfg<BN, BMW, GATEUP, OUT16, MINB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -580,12 +590,12 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16>::kThreadsT, 1) gro
 }
 
 // out (fp32) or, with OUT16, out16 + row_scale given w_bound (down only).
-template <int BN, int BMW, bool GATEUP, bool OUT16 = false>
+template <int BN, int BMW, bool GATEUP, bool OUT16 = false, int MINB = 1>
 int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
         const float* w_scale, const int32_t* offsets, int groups, int N, int K,
         float* out, cudaStream_t stream, bool pdl, __half* out16 = nullptr,
         float* row_scale = nullptr, const float* w_bound = nullptr) {
-  using C = Cfg<BN, BMW, GATEUP, OUT16>;
+  using C = Cfg<BN, BMW, GATEUP, OUT16, MINB>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;
@@ -596,7 +606,7 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
                             : make_tmap_out(&tm_out, out, a_rows, N, 32, 32, 4);
     if (!made) return -3;
   }
-  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP, OUT16>;
+  auto kern = grouped_gemm_kernel<BN, BMW, GATEUP, OUT16, MINB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
@@ -727,12 +737,19 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                                     groups, N, K, out, avg <= 128 ? 128 : 256,
                                     stream, pdl);
   if (kind == 0) {
-    if (avg <= 16) return run<16, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 16) {
+      // fewer tiles than two per SM: two CTAs an SM, so no SM streams a
+      // second tile alone after the others are done
+      if (token_tiles_upper(a_rows, groups, 16) * (N / 64) <= 2 * (int64_t)sm_count())
+        return run<16, 64, true, false, 2>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+      return run<16, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    }
     if (avg <= 32) return run<32, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
     if (avg <= 64) return run<64, 128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
     return run<128, 128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   }
-  if (avg <= 16) return run<16, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+  // 16-token down tiles (short K, per-tile overhead) always run two CTAs an SM
+  if (avg <= 16) return run<16, 128, false, false, 2>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   if (avg <= 32) return run<32, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   if (avg <= 64) return run<64, 128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   // 128-token tiles of 256 channels read each token tile once per 256
@@ -756,17 +773,17 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
                                              offsets, groups, N, K, y16, row_scale,
                                              avg <= 128 ? 128 : 256, stream, pdl);
   __half* o = reinterpret_cast<__half*>(y16);
-#define MOE_DOWN16(bn)                                                             \
-  return run<bn, 128, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, \
-                                   N, K, nullptr, stream, pdl, o, row_scale, w_bound)
-  if (avg <= 16) MOE_DOWN16(16);
-  if (avg <= 32) MOE_DOWN16(32);
-  if (avg <= 64) MOE_DOWN16(64);
+#define MOE_DOWN16(bn, minb)                                                             \
+  return run<bn, 128, false, true, minb>(A, a_scale, a_rows, W, w_scale, offsets, groups, \
+                                         N, K, nullptr, stream, pdl, o, row_scale, w_bound)
+  if (avg <= 16) MOE_DOWN16(16, 2);
+  if (avg <= 32) MOE_DOWN16(32, 1);
+  if (avg <= 64) MOE_DOWN16(64, 1);
   if (avg <= 128 && N % 256 == 0)
     return run<128, 256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
                                       nullptr, stream, pdl, o, row_scale, w_bound);
-  if (avg <= 128) MOE_DOWN16(128);
-  MOE_DOWN16(256);
+  if (avg <= 128) MOE_DOWN16(128, 1);
+  MOE_DOWN16(256, 1);
 #undef MOE_DOWN16
 }
 

@@ -346,6 +346,8 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
     (4, [130, 0, 300, 77], 512, 256, 0),             # CTA pairs, BN 128
     (6, [5, 9, 0, 300, 2, 3], 256, 256, 16),         # hint forces BN 16
     (3, [400, 5, 90], 768, 384, 100),                # BN 128; down: 256-channel tiles
+    # BN 16 with more possible tiles than two per SM: gate/up one CTA an SM
+    (40, [3, 1, 4, 1, 5, 9, 2, 6, 5, 3] * 4, 512, 256, 0),
 ])
 def test_grouped_gemm(gateup, G, counts, N, K, hint):
     aq, sa, wq, sw, offs = _grouped_case(G, counts, N, K, gateup,
