@@ -212,6 +212,42 @@ def gateup_bytes(cfg, touched):
         rows * cfg.I * 4
 
 
+def implementation_bytes(cfg, touched, pre=False):
+    """Bytes the forward's launches move, intermediates included (reported
+    beside the algorithmic bytes for diagnosis): every launch's reads and
+    writes counted once, as if nothing stayed in L2 between launches."""
+    T, D, E, k, I = cfg.T, cfg.D, cfg.E, cfg.k, cfg.I
+    R, rows = T * k, cfg.rows
+    y16 = rows * D * 4 >= (32 << 20)      # the forward's fp16 encoding of y
+    ybytes = rows * D * 2 + rows * 4 if y16 else rows * D * 4
+    b = 0
+    # routing: logits in (or x and the router matrix), ids and weights out
+    if cfg.router == "weights":
+        fused = (E <= 512 and k <= 16 and D % 64 == 0 and T * E * D >= (1 << 20))
+        b += 2 * T * D + 2 * E * D + (0 if fused else 2 * 4 * T * E)
+    else:
+        b += 4 * T * E
+    b += 8 * T * k
+    # permutation: ids in; counts, offsets and both row maps out
+    b += 4 * R + 8 * (cfg.groups + 1) + 8 * R
+    # quantiser: x in (and the residual and gamma, the new residual out, for
+    # the pre-norm forward), codes and scales of every destination row out,
+    # the shared gate's weights in and gate out
+    b += 2 * T * D + (2 * T * D * 2 + 2 * D if pre else 0) + rows * (D + 4)
+    b += (2 * D + 4 * T) if cfg.shared else 0
+    # gate/up GEMM: weights, codes and scales in, fp32 h out
+    b += gateup_bytes(cfg, touched)
+    # requantisation: h in, codes and scales out
+    b += rows * I * 4 + rows * (I + 4)
+    # down GEMM: weights, scales and codes in, y out; the fp16 encoding's
+    # bound reads every group's down scales first
+    b += touched * (D * I + 4 * D) + rows * (I + 4) + ybytes
+    b += cfg.groups * D * 4 + 4 * cfg.groups if y16 else 0
+    # combine: y, the row map and the weights in, bf16 out
+    b += ybytes + 8 * T * k + 2 * T * D + (4 * T if cfg.shared else 0)
+    return b
+
+
 def layer_flops(cfg):
     router = 2.0 * cfg.T * cfg.D * cfg.E if cfg.router == "weights" else 0.0
     return 2.0 * cfg.rows * cfg.D * 2 * cfg.I + 2.0 * cfg.rows * cfg.I * cfg.D + router
@@ -572,11 +608,15 @@ def run_ours(args, cfg, rank, world, local_rank):
         "algorithmic_bytes_per_launch": gu_bytes,
         "flops_per_launch": gu_flops, "ms_per_launch": gemm_ms})
     t_roof = max(F / (fp8_peak * 1e12), B / (hbm * 1e9))
+    B_impl = implementation_bytes(cfg, touched, bool(pre))
     layer_roofline = {
         "bound": "tensor" if F / (fp8_peak * 1e12) > B / (hbm * 1e9) else "hbm",
         "algorithmic_bytes": B, "flops": F, "achieved_gbs": layer_gbs,
         "achieved_fp8_tflops": F / (max_ms * 1e-3) / 1e12,
-        "t_roof_ms": t_roof * 1e3, "frac": t_roof / (max_ms * 1e-3)}
+        "t_roof_ms": t_roof * 1e3, "frac": t_roof / (max_ms * 1e-3),
+        # diagnosis: the bytes the launches move with the intermediates
+        "implementation_bytes": B_impl,
+        "implementation_gbs": B_impl / (max_ms * 1e-3) / 1e9}
     clocks = sampler.summary(t_wall0, t_wall1)
     prenorm = None
     if pre:
