@@ -66,3 +66,49 @@ def quantize_experts(raw_pairs):
     if len(raw_pairs) <= 1:
         return [_quantize_expert(p) for p in raw_pairs]
     return oracle_pool().map(_quantize_expert, raw_pairs, chunksize=1)
+
+
+def parity_tokens(ids, E, shared, n_min=256, seed=0):
+    """Tokens whose outputs the full-size layer tests compare with the oracle.
+
+    Every output row depends only on its own token once the routing is fixed,
+    so a large batch is checked on a sample of tokens. The sample is aimed at
+    the rows where the GEMM tiles change, taken from the layer's own
+    permutation (counting sort of the routed ids, expert-contiguous rows):
+
+    * the first and the last row of every expert that has rows;
+    * both rows on either side of every tile boundary inside an expert's
+      slice: every 64 rows (which covers the 64-, 128- and 256-row token
+      tiles and the 256-token CTA-pair tiles), or every 16 rows when the
+      experts average at most 32 rows (the 16- and 32-row tiles);
+    * for the shared expert (one row per token, group E after the routed
+      rows): the first and last token, and the tokens on either side of its
+      first four and last four tile boundaries;
+
+    then seeded random tokens until there are at least n_min (or all T).
+    Returns the sorted token indices."""
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    _, offsets, s2f, _ = oracle.permute_ref(ids, E)
+    R = T * k
+    step = 16 if R <= 32 * E else 64
+    rows = set()
+    for g in range(E):
+        a, b = int(offsets[g]), int(offsets[g + 1])
+        if b <= a:
+            continue
+        rows.update((a, b - 1))
+        for m in range(a + step, b, step):
+            rows.update((m - 1, m))
+    toks = {int(s2f[s]) // k for s in rows}
+    if shared and T > 0:
+        toks.update((0, T - 1))
+        bounds = list(range(step, T, step))
+        for m in bounds[:4] + bounds[-4:]:
+            toks.update((m - 1, m))
+    want = min(T, n_min)
+    if len(toks) < want:
+        rng = np.random.default_rng(seed)
+        rest = np.setdiff1d(np.arange(T), np.fromiter(toks, np.int64))
+        toks.update(int(t) for t in rng.choice(rest, want - len(toks), replace=False))
+    return np.array(sorted(toks), dtype=np.int64)

@@ -1,11 +1,14 @@
 """End-to-end parity of moe_forward (through the C ABI) against the oracle.
 
 Small layers are checked on every token. The five workloads run at their full
-sizes, in the launch configuration the benchmark uses; there the oracle
-evaluates a seeded sample of tokens (every output row depends only on its own
-token once the routing is fixed) while the routing and the permutation are
-compared bit for bit on all tokens. The GPU-quantised weights of every expert
-the sample touches are compared byte for byte with the oracle's.
+sizes, in the launch configuration the benchmark uses; there the routing and
+the permutation are compared bit for bit on all tokens, and the outputs on a
+sample of at least 256 tokens (every output row depends only on its own token
+once the routing is fixed) aimed at the rows where the GEMM tiles change:
+every expert's first and last row and the rows on either side of each tile
+boundary inside its slice (`parity_tokens`). The GPU-quantised weights of
+every expert the sample touches are compared byte for byte with the
+oracle's.
 
 Accuracy contract on bf16 outputs: max|gpu - oracle| <= 2e-2 * rms(oracle) and
 sum|gpu - oracle| / sum|oracle| <= 5e-3."""
@@ -17,7 +20,8 @@ import torch
 import oracle
 from expert_layer_ptpc_gb300 import synthetic as syn
 from tests.gpu_helpers import (U32, ensure_library, gemm_bound,
-                               layer_tolerance_ok, quantize_experts, require_gpu)
+                               layer_tolerance_ok, parity_tokens,
+                               quantize_experts, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,25 +48,30 @@ class _Run:
                   else syn.gen_logits(cfg, "cuda", self.seed))
         return x, logits
 
-    def expert_weights(self, es):
+    def expert_weights(self, es, batch=32):
+        """The oracle's quantisation of experts `es` (from the same seeded raw
+        weights, drawn on the GPU and copied back), each compared byte for
+        byte with the GPU's own quantisation. Experts go through the process
+        pool in batches, so host memory holds at most `batch` raw experts."""
         missing = [e for e in es if e not in self.qcache]
-        raw = []
-        for e in missing:
-            gu, d = syn.gen_expert_weights(self.cfg, e, "cuda", self.seed)
-            raw.append((gu.cpu().numpy(), d.cpu().numpy()))
-        for e, q in zip(missing, quantize_experts(raw)):
-            self.qcache[e] = q
-            # the GPU's own quantisation of this expert, byte for byte
-            L = self.layer
-            assert np.array_equal(L.w_gu[e].cpu().numpy(), q[0]), e
-            assert np.array_equal(L.s_gu[e].cpu().numpy().view(np.uint32),
-                                  q[1].view(np.uint32)), e
-            assert np.array_equal(L.w_d[e].cpu().numpy(), q[2]), e
-            assert np.array_equal(L.s_d[e].cpu().numpy().view(np.uint32),
-                                  q[3].view(np.uint32)), e
+        L = self.layer
+        for i in range(0, len(missing), batch):
+            part = missing[i:i + batch]
+            raw = []
+            for e in part:
+                gu, d = syn.gen_expert_weights(self.cfg, e, "cuda", self.seed)
+                raw.append((gu.cpu().numpy(), d.cpu().numpy()))
+            for e, q in zip(part, quantize_experts(raw)):
+                self.qcache[e] = q
+                assert np.array_equal(L.w_gu[e].cpu().numpy(), q[0]), e
+                assert np.array_equal(L.s_gu[e].cpu().numpy().view(np.uint32),
+                                      q[1].view(np.uint32)), e
+                assert np.array_equal(L.w_d[e].cpu().numpy(), q[2]), e
+                assert np.array_equal(L.s_d[e].cpu().numpy().view(np.uint32),
+                                      q[3].view(np.uint32)), e
         return {e: self.qcache[e] for e in es}
 
-    def check(self, cfg, n_sample=None):
+    def check(self, cfg, sample=False):
         from expert_layer_ptpc_gb300 import binding
         T, k, E = cfg.T, cfg.k, cfg.E
         x, logits = self.inputs(cfg)
@@ -115,13 +124,11 @@ class _Run:
             assert np.array_equal(s2f.cpu().numpy(), rs)
             assert np.array_equal(f2s.cpu().numpy(), rf)
 
-        if n_sample is None or n_sample >= T:
-            tokens = np.arange(T)
+        if sample:
+            # the GPU's own ids give the row layout its GEMM tiles saw
+            tokens = parity_tokens(ids.cpu().numpy(), E, cfg.shared, seed=T + 17)
         else:
-            rng = np.random.default_rng(T + 17)
-            tokens = np.sort(rng.choice(T, n_sample, replace=False))
-            tokens[0] = 0
-            tokens[-1] = T - 1            # first and last token always
+            tokens = np.arange(T)
         tokens = tokens[ok_t[tokens]]     # unique routing only
         touched = sorted(set(int(e) for e in rid[tokens].ravel()))
         if cfg.shared:
@@ -172,12 +179,12 @@ def test_decode_layer():
 
 def test_prefill_layer():
     cfg = syn.CONFIGS["prefill"]
-    _Run(cfg).check(cfg, n_sample=6)
+    _Run(cfg).check(cfg, sample=True)
 
 
 def test_skewed_layer():
     cfg = syn.CONFIGS["skewed"]
-    _Run(cfg).check(cfg, n_sample=24)
+    _Run(cfg).check(cfg, sample=True)
 
 
 @pytest.fixture(scope="module")
@@ -188,7 +195,7 @@ def sweep_run():
 @pytest.mark.parametrize("T", syn.SWEEP_T)
 def test_sweep_layer(sweep_run, T):
     cfg = syn.sweep_config(T)
-    sweep_run.check(cfg, n_sample=4)
+    sweep_run.check(cfg, sample=T > 256)
 
 
 @pytest.mark.parametrize("cfg", [
@@ -232,8 +239,9 @@ def test_prenorm_prefill_sampled():
     """moe_forward_prenorm on the prefill workload at full size, in the
     launch configuration and with the inputs `bench.py --prenorm` times
     (residual N(0, 0.5^2) and gamma 1 + N(0, 0.1^2), bf16, seed 12345): the
-    new residual of every token bit for bit, the output of sampled tokens
-    against the oracle layer on the oracle's normalised activations."""
+    new residual of every token bit for bit, the output of the tile-boundary
+    sample of tokens against the oracle layer on the oracle's normalised
+    activations."""
     from expert_layer_ptpc_gb300 import binding
     cfg = syn.CONFIGS["prefill"]
     run = _Run(cfg)
@@ -251,9 +259,7 @@ def test_prenorm_prefill_sampled():
     assert np.array_equal(res_out.float().cpu().numpy(), ref[0])
     ln = logits.cpu().numpy()
     rid, _ = oracle.route_ref(ln, cfg.k, cfg.renormalize)
-    rng = np.random.default_rng(cfg.T + 3)
-    tokens = np.sort(rng.choice(cfg.T, 6, replace=False))
-    tokens[-1] = cfg.T - 1
+    tokens = parity_tokens(rid, cfg.E, cfg.shared, seed=cfg.T + 3)
     touched = sorted(set(int(e) for e in rid[tokens].ravel()))
     qmap = run.expert_weights(touched)
     r = oracle.moe_forward_ref(ref[1], cfg.k, lambda e: qmap[e], cfg.E, logits=ln,

@@ -99,3 +99,46 @@ def test_bf16_round_ties_to_even():
     # 1 + 2^-8 lies half way between bf16 1.0 and 1 + 2^-7: even is 1.0.
     assert bf16_round(np.array([1.0 + 2 ** -8]))[0] == 1.0
     assert bf16_round(np.array([1.0 + 3 * 2 ** -8]))[0] == 1.0 + 2 ** -6
+
+
+# ---------------------------------------------------------------------------
+# exhaustive: every fp32 bit pattern
+# ---------------------------------------------------------------------------
+_EXH_CHUNK_BITS = 24
+
+
+def _exhaustive_chunk(c):
+    """Mismatches between the oracle's encoder and torch's float8_e4m3fn cast
+    over the 2^24 fp32 bit patterns of chunk c. torch's cast rounds to
+    nearest even inside the finite range but is not saturating (it gives NaN
+    beyond it), so its input is first clipped to +-448, which the OCP
+    saturating rule maps every larger magnitude to. NaN inputs must give a
+    NaN code (exponent and mantissa all ones) on both sides."""
+    import numpy as np
+    import torch
+    torch.set_num_threads(1)
+    from oracle import e4m3_encode
+    bits = np.arange(c << _EXH_CHUNK_BITS, (c + 1) << _EXH_CHUNK_BITS,
+                     dtype=np.uint64).astype(np.uint32)
+    v = bits.view(np.float32)
+    got = e4m3_encode(v)
+    ref = torch.from_numpy(np.clip(v, -448.0, 448.0)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    nan = np.isnan(v)
+    bad = (got != ref) & ~nan
+    bad |= nan & ((got & 0x7F) != 0x7F)
+    first = int(bits[np.flatnonzero(bad)[0]]) if bad.any() else -1
+    return int(bad.sum()), first
+
+
+def test_encode_exhaustive_all_fp32():
+    """The encoder on all 2^32 fp32 bit patterns (both zeros, every
+    subnormal and normal, both infinities, every NaN) against torch's cast
+    with saturation, in 256 chunks over a spawn-started process pool."""
+    import multiprocessing as mp
+    n_chunks = 1 << (32 - _EXH_CHUNK_BITS)
+    workers = max(1, min(16, os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(workers) as pool:
+        res = pool.map(_exhaustive_chunk, range(n_chunks), chunksize=1)
+    bad = [(c, n, f) for c, (n, f) in enumerate(res) if n]
+    assert not bad, f"mismatching chunks (chunk, count, first bits): {bad[:5]}"
