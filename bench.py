@@ -6,8 +6,12 @@
 A step is one full layer forward (routing, permutation, quantisation, gate/up
 GEMM with SwiGLU, requantisation, down GEMM, combine) over one batch of
 seeded synthetic inputs, already resident in HBM. The default workload is the
-decode-shaped layer (T=16, D=4096, E=128, top-8, I=1536): it streams the
-touched experts' FP8 weights from HBM, so the roofline is HBM bandwidth.
+largest one, the Qwen3.5-like layer at T=16384 tokens (D=4096, 512 experts
+of I=1024, top-10 plus a shared expert): 4.5 TFLOP over 6.5 GB of touched
+FP8 weights, close to the ridge between the FP8 tensor roof and HBM. At N=1
+the same run then times every other workload (tiny, decode, prefill, skewed,
+T in {1, 64, 512, 4096}) the same way and reports them under
+`all_workloads`.
 
 Timing: W untimed warm-up steps, then K timed steps; before every step a
 256 MiB buffer is written so no weight stays in the 129 MB L2. Each step is
@@ -35,6 +39,13 @@ if ROOT not in sys.path:
 
 METRIC = "fused-MoE layer tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+# the largest workload (16384 tokens, 512 experts, top-10 + shared): the line's
+# headline; every other workload is timed in the same run under all_workloads
+DEFAULT_WORKLOAD = "sweep@16384"
+ALL_WORKLOADS = ("tiny", "decode", "prefill", "skewed", "sweep@1", "sweep@64",
+                 "sweep@512", "sweep@4096", "sweep@16384")
+# GB300 dense FP8 tensor throughput as NVIDIA states it (without sparsity)
+NOMINAL_FP8_TFLOPS = 4500.0
 
 
 # ---------------------------------------------------------------------------
@@ -153,23 +164,34 @@ def replica_tokens_per_s(T, world, max_ms):
     return world * T / (max_ms * 1e-3)
 
 
-def captured_traffic(algorithmic_bytes, bn_decode):
-    """DRAM traffic of the gate/up launch from the committed ncu record
-    (profiles/traffic_gateup_decode.json), scaled to this launch by its
-    algorithmic bytes; None when the record is missing, was taken on another
-    tile shape, or the kernel sources changed since the capture."""
+def captured_traffic(cfg, algorithmic_bytes):
+    """DRAM traffic of the gate/up launch from a committed ncu record of the
+    same kernel instantiation on a smaller case (profiles/traffic_*.json),
+    scaled to this launch by its algorithmic bytes. Returns (traffic,
+    source), or (None, None) when no record covers this launch's kernel or
+    the kernel sources changed since the capture."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic_gateup_decode.json")
-    if not bn_decode or not os.path.exists(path):
-        return None
+    per_expert = cfg.T * cfg.k / max(1, cfg.E)
+    # the instantiation the gate/up dispatch picks from the rows per expert
+    if per_expert <= 16:
+        name = "traffic_gateup_decode.json"
+    elif per_expert >= 256:
+        name = "traffic_gateup_pair.json"
+    else:
+        return None, None
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None, None
     rec = json.load(open(path))
     h = hashlib.sha256()
     for f in rec["sources"]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     if h.hexdigest() != rec["sources_sha256"]:
-        return None
-    return rec["traffic_per_algorithmic_byte"] * algorithmic_bytes
+        return None, None
+    return (rec["traffic_per_algorithmic_byte"] * algorithmic_bytes,
+            f"ncu capture of {rec['kernel']} scaled by algorithmic bytes "
+            f"(profiles/{name})")
 
 
 def physical_gpu(local_rank):
@@ -288,11 +310,13 @@ def _oracle_inputs(cfg_name, seed):
 _W = {}
 
 
-def _worker_init(cfg_name, seed):
-    """Timing worker: holds the workload's inputs and quantised weights."""
+def _worker_init(cfg_name, inputs):
+    """Timing worker: holds the workload's inputs (x, router matrix, logits,
+    shared gate) and quantised weights."""
     _limit_threads()
-    cfg, x, wr, logits, wg = _oracle_inputs(cfg_name, seed)
-    _W.update(cfg=cfg, x=x, wr=wr, logits=logits, wg=wg, quant={})
+    x, wr, logits, wg = inputs
+    _W.update(cfg=workload_config(cfg_name), x=x, wr=wr, logits=logits, wg=wg,
+              quant={})
 
 
 def _worker_add(quant):
@@ -314,19 +338,38 @@ def _worker_timed(tokens):
     return time.perf_counter() - t0
 
 
-class OracleRunner:
-    """A spawn-started pool quantises expert weights in parallel (untimed);
-    one single-threaded worker runs the timed oracle."""
+_POOL = None
 
-    def __init__(self, cfg_name, seed=0):
+
+def oracle_pool():
+    """One spawn-started process pool for the oracle's weight quantisation
+    (started before it is needed; never forked from a process holding a CUDA
+    context)."""
+    global _POOL
+    if _POOL is None:
+        import multiprocessing as mp
+        _limit_threads()
+        _POOL = mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 2)))
+    return _POOL
+
+
+class OracleRunner:
+    """The shared pool quantises expert weights in parallel (untimed); one
+    single-threaded worker runs the timed oracle."""
+
+    def __init__(self, cfg_name, seed=0, inputs=None, pool=None):
         import multiprocessing as mp
         _limit_threads()
         ctx = mp.get_context("spawn")
         self.cfg_name, self.seed = cfg_name, seed
-        self.cfg, _, _, self.logits, _ = _oracle_inputs(cfg_name, seed)
-        self.quant_pool = ctx.Pool(max(1, min(16, os.cpu_count() or 2)))
+        self.cfg = workload_config(cfg_name)
+        if inputs is None:
+            _, x, wr, logits, wg = _oracle_inputs(cfg_name, seed)
+            inputs = (x, wr, logits, wg)
+        self.logits = inputs[2]
+        self.quant_pool = pool if pool is not None else oracle_pool()
         self.timer = ctx.Pool(1, initializer=_worker_init,
-                              initargs=(cfg_name, seed))
+                              initargs=(cfg_name, inputs))
         self.have = set()
 
     def prepare(self, tokens):
@@ -347,16 +390,15 @@ class OracleRunner:
         return self.timer.apply(_worker_timed, (list(tokens),))
 
     def close(self):
-        self.quant_pool.terminate()
         self.timer.terminate()
 
 
-def cpu_baseline(cfg_name, seed=0, budget_s=20.0):
+def cpu_baseline(cfg_name, seed=0, budget_s=20.0, pool=None):
     """The oracle, as it stands, timed on this host on a bounded sample of the
     workload's tokens. Weight quantisation (done once per model on both
     sides) is outside the timing."""
     cfg = workload_config(cfg_name)
-    run = OracleRunner(cfg_name, seed)
+    run = OracleRunner(cfg_name, seed, pool=pool)
     try:
         run.prepare([0])
         dt1 = run.time([0])
@@ -374,15 +416,52 @@ def cpu_baseline(cfg_name, seed=0, budget_s=20.0):
                        f"{dt:.1f} s; weights quantised outside the timing")}
 
 
-def run_reference(args, cfg):
-    """The reference arm: the CPU oracle. Each step evaluates one token of the
-    batch (rotating), routing over the whole batch included."""
-    run = OracleRunner(args.workload, 0)
+def bench_config(cfg, touched, world):
+    """The `config` object of a JSON line, the same for both arms."""
+    return {"workload": describe(cfg), "T": cfg.T, "D": cfg.D, "E": cfg.E,
+            "k": cfg.k, "I": cfg.I, "shared": cfg.shared,
+            "touched_experts": int(touched),
+            "l2": "flushed before every step (256 MiB write)",
+            "parallelism": f"replicas x{world}"}
+
+
+def _reference_inputs(cfg, seed=0):
+    """x, router input and shared gate of the workload as the GPU arm draws
+    them (on the GPU when there is one, so both arms route the same tokens),
+    as numpy arrays."""
+    import torch
+    import oracle
+    from expert_layer_ptpc_gb300 import synthetic as syn
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = syn.gen_x(cfg, dev, seed).float().cpu().numpy()
+    if cfg.router == "weights":
+        wr = syn.gen_router_weights(cfg, dev, seed).float().cpu().numpy()
+        logits = oracle.router_logits_ref(x, wr)
+    else:
+        wr, logits = None, syn.gen_logits(cfg, dev, seed).cpu().numpy()
+    wg = (syn.gen_shared_gate(cfg, dev, seed).float().cpu().numpy()
+          if cfg.shared else None)
+    return x, wr, logits, wg
+
+
+def run_reference(args, cfg, world):
+    """The reference arm: the CPU oracle, on the GPU arm's tokens. Each step
+    evaluates one token of the batch (rotating), routing and permutation over
+    the whole batch included. Expert weights come from the same seeded
+    recipe, drawn on the host (their values do not change the oracle's
+    time)."""
+    import numpy as np
+    import oracle
+    x, wr, logits, wg = _reference_inputs(cfg)
+    ids, _ = oracle.route_ref(logits, cfg.k, cfg.renormalize)
+    touched = int((np.bincount(ids.ravel(), minlength=cfg.E) > 0).sum())
+    run = OracleRunner(args.workload, 0, inputs=(x, wr, logits, wg))
     try:
-        run.prepare(list(range(cfg.T)))
-        for i in range(args.warmup):
-            run.time([i % cfg.T])
-        times = [run.time([i % cfg.T]) for i in range(args.steps)]
+        steps = [i % cfg.T for i in range(args.warmup + args.steps)]
+        run.prepare(sorted(set(steps)))
+        for t in steps[:args.warmup]:
+            run.time([t])
+        times = [run.time([t]) for t in steps[args.warmup:]]
     finally:
         run.close()
     total = sum(times)
@@ -393,12 +472,11 @@ def run_reference(args, cfg):
         "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(cfg), "T": cfg.T, "D": cfg.D,
-                   "E": cfg.E, "k": cfg.k, "I": cfg.I, "shared": cfg.shared},
+        "config": bench_config(cfg, touched, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1,
                          "kind": "oracle",
                          "sample": "one token of the batch per step (expert "
-                                   "FFNs of its k experts; routing and "
+                                   "FFNs of its experts; routing and "
                                    "permutation over the batch), fp64 numpy, "
                                    "1 BLAS thread"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -410,34 +488,46 @@ def run_reference(args, cfg):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def run_ours(args, cfg, rank, world, local_rank):
+class Workload:
+    """A layer with its seeded inputs on the device, ready to time."""
+
+    def __init__(self, cfg, dev, layer=None, prenorm=False):
+        import torch
+        from expert_layer_ptpc_gb300 import synthetic as syn
+        from expert_layer_ptpc_gb300.layer import MoELayer
+        self.cfg = cfg
+        self.layer = layer if layer is not None else MoELayer.synthetic(cfg, dev, seed=0)
+        self.x = syn.gen_x(cfg, dev, 0)
+        self.logits = None if cfg.router == "weights" else syn.gen_logits(cfg, dev, 0)
+        self.out = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=dev)
+        self.ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+        self.tw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+        self.pre = {}
+        if prenorm:   # layer input = RMSNorm(x + residual) * gamma
+            if self.logits is None:
+                raise SystemExit("--prenorm needs a workload with router logits")
+            g = torch.Generator(device="cpu").manual_seed(12345)
+            res = (torch.randn(cfg.T, cfg.D, generator=g) * 0.5).to(torch.bfloat16).to(dev)
+            gamma = (1.0 + 0.1 * torch.randn(cfg.D, generator=g)).to(torch.bfloat16).to(dev)
+            self.pre = {"residual": res, "gamma": gamma, "eps": 1e-6,
+                        "residual_out": torch.empty_like(res)}
+
+    def step(self, evs=None):
+        self.layer.forward(self.x, self.logits, out=self.out, topk_ids=self.ids,
+                           topk_w=self.tw, events=evs, **self.pre)
+
+    def check_status(self, where):
+        st, bits = self.layer.status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({bits:#x}) {where}")
+
+
+def measure(args, w, stream, flush, sampler=None, graph=True):
+    """W warm-up steps, K timed graph replays (L2 flushed before each), then
+    K steps with the library's per-kernel marks. Returns step times (ms),
+    per-kernel times (ms) and the wall-clock window of the timed steps."""
     import torch
-    import torch.distributed as dist
-
-    from expert_layer_ptpc_gb300 import binding, build
-    from expert_layer_ptpc_gb300 import synthetic as syn
-    from expert_layer_ptpc_gb300.layer import MoELayer
-
-    build.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    layer = MoELayer.synthetic(cfg, dev, seed=0)
-    x = syn.gen_x(cfg, dev, 0)
-    logits = None if cfg.router == "weights" else syn.gen_logits(cfg, dev, 0)
-    out = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device=dev)
-    pre = {}
-    if args.prenorm:   # layer input = RMSNorm(x + residual) * gamma
-        if logits is None:
-            raise SystemExit("--prenorm needs a workload with router logits")
-        g = torch.Generator(device="cpu").manual_seed(12345)
-        res = (torch.randn(cfg.T, cfg.D, generator=g) * 0.5).to(torch.bfloat16).to(dev)
-        gamma = (1.0 + 0.1 * torch.randn(cfg.D, generator=g)).to(torch.bfloat16).to(dev)
-        pre = {"residual": res, "gamma": gamma, "eps": 1e-6,
-               "residual_out": torch.empty_like(res)}
-    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
-    tw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    from expert_layer_ptpc_gb300 import binding
     nev = binding.MOE_FORWARD_EVENTS
 
     def make_events(n):
@@ -448,79 +538,177 @@ def run_ours(args, cfg, rank, world, local_rank):
                 e.record(stream)
         return evs
 
-    def step(evs=None):
-        layer.forward(x, logits, out=out, topk_ids=ids, topk_w=tw, events=evs, **pre)
-
-    # warm-up (also validates the run)
     warm = make_events(1)[0]
     for _ in range(max(args.warmup, 1)):
         flush.fill_(1)
-        step(warm)
+        w.step(warm)
     torch.cuda.synchronize()
-    st, bits = binding.moe_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({bits:#x}) after warm-up")
+    w.check_status("after warm-up")
 
     # The step a serving loop runs: one CUDA graph holding the whole forward
     # (kernels chained with programmatic dependent launch).
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        graph.replay()
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            w.step()
+        g.replay()
         torch.cuda.synchronize()
 
-    def run_step():
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
-
-    # timed region 1: whole steps
-    sampler = ClockSampler(physical_gpu(local_rank))
-    sampler.start()
-    time.sleep(0.3)
     marks = [(torch.cuda.Event(enable_timing=True),
               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
+    if sampler is not None:
+        sampler.barrier()
     torch.cuda.synchronize()
-    t_wall0 = time.time()
+    t0 = time.time()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         marks[i][0].record(stream)
-        run_step()
+        if g is not None:
+            g.replay()
+        else:
+            w.step()
         marks[i][1].record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    t_wall1 = time.time()
-    time.sleep(0.3)
-    sampler.stop()
-    st, bits = binding.moe_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({bits:#x}) in the timed region")
+    if sampler is not None:
+        sampler.barrier()
+    t1 = time.time()
+    w.check_status("in the timed region")
     step_ms = [a.elapsed_time(b) for a, b in marks]
 
-    # timed region 2: the same forward with the library's step marks, to time
-    # each kernel on its launching stream (the marks serialise the kernels)
+    # the same forward with the library's step marks, to time each kernel on
+    # its launching stream (the marks serialise the kernels)
     evs = make_events(args.steps)
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        step(evs[i])
+        w.step(evs[i])
     torch.cuda.synchronize()
-    st, bits = binding.moe_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({bits:#x}) in the profiled run")
+    w.check_status("in the profiled run")
     phase_ms = [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(nev - 1)]
     profiled_ms = sum(e[0].elapsed_time(e[nev - 1]) for e in evs) / len(evs)
+    del g
+    return step_ms, phase_ms, profiled_ms, (t0, t1)
+
+
+def rooflines(cfg, counts, step_ms, phase_ms, pre=False):
+    """Roofline of the gate/up GEMM launch and of the whole layer step."""
+    B, touched = algorithmic_bytes(cfg, counts)
+    if pre:   # the residual read and the new residual written, gamma
+        B += 2 * cfg.T * cfg.D * 2 + 2 * cfg.D
+    F = layer_flops(cfg)
+    hbm, bf16, peak_src = peaks()
+    fp8_peak = 2.0 * bf16     # measured bf16 x the nominal fp8/bf16 ratio of 2
+    gemm_ms = sum(phase_ms[4]) / len(phase_ms[4])
+    gu_bytes = gateup_bytes(cfg, touched)
+    # the gate/up GEMM: bound by whichever roof is lower for its bytes/flops
+    gu_flops = 2.0 * cfg.rows * cfg.D * 2 * cfg.I
+    tensor_bound = gu_flops / (fp8_peak * 1e12) > gu_bytes / (hbm * 1e9)
+    if tensor_bound:
+        ach = gu_flops / (gemm_ms * 1e-3) / 1e12
+        gemm = {"bound": "tensor", "achieved": ach, "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": ach / fp8_peak,
+                "peak_source": peak_src + ", fp8 = 2 x bf16 burst",
+                "frac_of_nominal_fp8": ach / NOMINAL_FP8_TFLOPS}
+    else:
+        ach = gu_bytes / (gemm_ms * 1e-3) / 1e9
+        gemm = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": peak_src}
+    traffic, tsrc = captured_traffic(cfg, gu_bytes)
+    gemm.update({
+        "kernel": "gate/up grouped GEMM (tcgen05, SwiGLU epilogue)",
+        "traffic": traffic, "traffic_source": tsrc,
+        "algorithmic_bytes_per_launch": gu_bytes,
+        "flops_per_launch": gu_flops, "ms_per_launch": gemm_ms})
+    ms = statistics.mean(step_ms)
+    t_roof = max(F / (fp8_peak * 1e12), B / (hbm * 1e9))
+    B_impl = implementation_bytes(cfg, touched, pre)
+    layer = {
+        "bound": "tensor" if F / (fp8_peak * 1e12) > B / (hbm * 1e9) else "hbm",
+        "algorithmic_bytes": B, "flops": F,
+        "achieved_gbs": B / (ms * 1e-3) / 1e9,
+        "achieved_fp8_tflops": F / (ms * 1e-3) / 1e12,
+        "t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms * 1e-3),
+        "frac_tensor_of_nominal_fp8": F / (ms * 1e-3) / 1e12 / NOMINAL_FP8_TFLOPS,
+        # diagnosis: the bytes the launches move with the intermediates
+        "implementation_bytes": B_impl,
+        "implementation_gbs": B_impl / (ms * 1e-3) / 1e9}
+    return gemm, layer, touched
+
+
+KERNEL_NAMES = ["router", "route", "permute", "quant_x", "gateup_gemm", "requant",
+                "down_gemm", "combine"]
+
+
+def kernel_times(phase_ms, pre=False):
+    names = list(KERNEL_NAMES)
+    if pre:
+        names[3] = "addnorm_quant_x"
+    return {n: round(sum(p) / len(p), 5) for n, p in zip(names, phase_ms)}
+
+
+def run_all_workloads(args, dev, stream, flush, sweep_layer, pool):
+    """Every workload but the headline one, each timed the same way (graph
+    replays, L2 flushed before each step) with its roofline fractions and the
+    oracle's speed on a few of its tokens."""
+    import torch
+    from expert_layer_ptpc_gb300 import synthetic as syn
+    res = {}
+    for name in ALL_WORKLOADS:
+        if name == args.workload:
+            continue
+        cfg = workload_config(name)
+        layer = sweep_layer if name.startswith("sweep@") else None
+        w = Workload(cfg, dev, layer=layer)
+        step_ms, phase_ms, _, _ = measure(args, w, stream, flush)
+        counts = torch.bincount(w.ids.view(-1).long(), minlength=cfg.E).cpu().numpy()
+        gemm, layer_rf, touched = rooflines(cfg, counts, step_ms, phase_ms)
+        ms = statistics.mean(step_ms)
+        res[name] = {
+            "workload": describe(cfg), "tokens_per_s": cfg.T / (ms * 1e-3),
+            "ms_per_step": ms, "touched_experts": touched,
+            "layer_roofline": {k: layer_rf[k] for k in (
+                "bound", "frac", "t_roof_ms", "achieved_gbs", "achieved_fp8_tflops",
+                "implementation_bytes")},
+            "gateup_gemm_roofline": {k: gemm[k] for k in (
+                "bound", "frac", "achieved", "unit", "ms_per_launch")},
+            "kernel_ms": kernel_times(phase_ms),
+            "cpu_baseline": (None if args.no_cpu_baseline else
+                             cpu_baseline(name, budget_s=3.0, pool=pool)),
+        }
+        del w
+        if layer is None:
+            torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from expert_layer_ptpc_gb300 import build
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = Workload(cfg, dev, prenorm=args.prenorm)
+    pre = w.pre
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    sampler = ClockSampler(physical_gpu(local_rank))
+    sampler.barrier = (lambda: dist.barrier()) if world > 1 else (lambda: None)
+    sampler.start()
+    time.sleep(0.3)
+    step_ms, phase_ms, profiled_ms, (t_wall0, t_wall1) = measure(
+        args, w, stream, flush, sampler, graph=not args.no_graph)
+    time.sleep(0.3)
+    sampler.stop()
     mean_ms = sum(step_ms) / len(step_ms)
     max_ms = max_over_ranks(mean_ms, dev)
 
     # e2e: the same forward through the public API from pinned host buffers,
     # copies in and out inside the timed region
+    x, logits, out, layer = w.x, w.logits, w.out, w.layer
     x_h = x.cpu().pin_memory()
     lg_h = logits.cpu().pin_memory() if logits is not None else None
     out_h = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16).pin_memory()
@@ -557,6 +745,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         b.record(stream)
         e_ms.append((a, b))
     torch.cuda.synchronize()
+    w.check_status("in the end-to-end run")
     e2e_mean = sum(a.elapsed_time(b) for a, b in e_ms) / len(e_ms)
     e2e_max = max_over_ranks(e2e_mean, dev)
     h2d = x.numel() * 2 + (logits.numel() * 4 if logits is not None else 0)
@@ -567,56 +756,11 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     if rank != 0:
         return
-    counts = torch.bincount(ids.view(-1).long(), minlength=cfg.E).cpu().numpy()
-    B, touched = algorithmic_bytes(cfg, counts)
-    if pre:   # the residual read and the new residual written, gamma
-        B += 2 * cfg.T * cfg.D * 2 + 2 * cfg.D
-    F = layer_flops(cfg)
-    hbm, bf16, peak_src = peaks()
-    gemm_ms = sum(phase_ms[4]) / len(phase_ms[4])
-    gu_bytes = gateup_bytes(cfg, touched)
-    names = ["router", "route", "permute",
-             "addnorm_quant_x" if pre else "quant_x", "gateup_gemm", "requant",
-             "down_gemm", "combine"]
-    kernel_ms = {n: round(sum(p) / len(p), 5) for n, p in zip(names, phase_ms)}
+    counts = torch.bincount(w.ids.view(-1).long(), minlength=cfg.E).cpu().numpy()
+    gemm_roofline, layer_roofline, touched = rooflines(
+        cfg, counts, [max_ms], phase_ms, bool(pre))
+    kernel_ms = kernel_times(phase_ms, bool(pre))
     dominant = max(kernel_ms, key=kernel_ms.get)
-    layer_gbs = B / (max_ms * 1e-3) / 1e9
-    fp8_peak = 2.0 * bf16     # measured bf16 x the nominal fp8/bf16 ratio of 2
-    # the gate/up GEMM: bound by whichever roof is lower for its bytes/flops
-    gu_flops = 2.0 * cfg.rows * cfg.D * 2 * cfg.I
-    tensor_bound = gu_flops / (fp8_peak * 1e12) > gu_bytes / (hbm * 1e9)
-    if tensor_bound:
-        ach = gu_flops / (gemm_ms * 1e-3) / 1e12
-        gemm_roofline = {"bound": "tensor", "achieved": ach, "peak": fp8_peak,
-                         "unit": "TFLOP/s", "frac": ach / fp8_peak,
-                         "peak_source": peak_src + ", fp8 = 2 x bf16 burst"}
-    else:
-        ach = gu_bytes / (gemm_ms * 1e-3) / 1e9
-        gemm_roofline = {"bound": "hbm", "achieved": ach, "peak": hbm,
-                         "unit": "GB/s", "frac": ach / hbm,
-                         "peak_source": peak_src}
-    # decode-sized token tiles (<= 16 rows per expert on average) run the
-    # instantiation the traffic record was captured on
-    decode_tiles = cfg.rows / max(1, cfg.groups) <= 16
-    traffic = captured_traffic(gu_bytes, decode_tiles)
-    gemm_roofline.update({
-        "kernel": "gate/up grouped GEMM (tcgen05, SwiGLU epilogue)",
-        "traffic": traffic,
-        "traffic_source": ("ncu capture scaled by algorithmic bytes "
-                           "(profiles/traffic_gateup_decode.json)"
-                           if traffic is not None else None),
-        "algorithmic_bytes_per_launch": gu_bytes,
-        "flops_per_launch": gu_flops, "ms_per_launch": gemm_ms})
-    t_roof = max(F / (fp8_peak * 1e12), B / (hbm * 1e9))
-    B_impl = implementation_bytes(cfg, touched, bool(pre))
-    layer_roofline = {
-        "bound": "tensor" if F / (fp8_peak * 1e12) > B / (hbm * 1e9) else "hbm",
-        "algorithmic_bytes": B, "flops": F, "achieved_gbs": layer_gbs,
-        "achieved_fp8_tflops": F / (max_ms * 1e-3) / 1e12,
-        "t_roof_ms": t_roof * 1e3, "frac": t_roof / (max_ms * 1e-3),
-        # diagnosis: the bytes the launches move with the intermediates
-        "implementation_bytes": B_impl,
-        "implementation_gbs": B_impl / (max_ms * 1e-3) / 1e9}
     clocks = sampler.summary(t_wall0, t_wall1)
     prenorm = None
     if pre:
@@ -624,6 +768,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         # the new residual, the codes of every destination row (k + shared)
         # and their scales (and the gate) out. Unfused, the normalised bf16
         # activations would be written and read once more.
+        hbm = peaks()[0]
         q_ms = sum(phase_ms[3]) / len(phase_ms[3])
         qb = 3 * cfg.T * cfg.D * 2 + 2 * cfg.D + cfg.rows * (cfg.D + 4) + \
             (4 * cfg.T + 2 * cfg.D if cfg.shared else 0)
@@ -639,12 +784,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": describe(cfg), "T": cfg.T, "D": cfg.D,
-                   "E": cfg.E, "k": cfg.k, "I": cfg.I, "shared": cfg.shared,
-                   "touched_experts": touched,
-                   "l2": "flushed before every step (256 MiB write)",
-                   "cuda_graph": graph is not None,
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(cfg, touched, world),
+        "cuda_graph": not args.no_graph,
         "roofline": gemm_roofline,
         "layer_roofline": layer_roofline,
         "kernel_ms": kernel_ms, "dominant_kernel": dominant,
@@ -659,8 +800,15 @@ def run_ours(args, cfg, rank, world, local_rank):
     if prenorm is not None:
         line["config"]["prenorm"] = {"eps": pre["eps"], "input": "RMSNorm(x + residual) * gamma"}
         line["prenorm"] = prenorm
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload)
+    if world == 1:
+        pool = None if args.no_cpu_baseline else oracle_pool()
+        if pool is not None:
+            line["cpu_baseline"] = cpu_baseline(args.workload, pool=pool)
+        if not args.no_all_workloads and not args.prenorm:
+            sweep_layer = layer if cfg.name.startswith("sweep") else None
+            del w
+            line["all_workloads"] = run_all_workloads(args, dev, stream, flush,
+                                                      sweep_layer, pool)
     print(json.dumps(line), flush=True)
 
 
@@ -704,9 +852,20 @@ def run_compare_scales(args, cfg, local_rank):
             prob = scaled.make_problem(mode, cfg, which)
             row[mode + "_ms"] = median_ms(lambda: scaled.run(prob))
             if mode == "ptpc":
+                # the layer's own kernel for this projection: gate/up with its
+                # SwiGLU epilogue (N = 2I weight rows in, I columns out), down
+                # as a plain PTPC GEMM
+                kind = (binding.MOE_GEMM_GATEUP_SWIGLU if which == "gateup"
+                        else binding.MOE_GEMM_DOWN)
+                R0 = prob["qa"].shape[0]
+                n_out = prob["qw"].shape[1] // (2 if which == "gateup" else 1)
+                prod_out = torch.empty((R0, n_out), dtype=torch.float32, device="cuda")
                 row["ptpc_production_ms"] = median_ms(lambda: binding.moe_grouped_gemm(
-                    binding.MOE_GEMM_DOWN, prob["qa"], prob["sa"], prob["qw"], prob["sw"],
-                    prob["offsets"], out=prob["out"]))
+                    kind, prob["qa"], prob["sa"], prob["qw"], prob["sw"],
+                    prob["offsets"], out=prod_out))
+                row["ptpc_production_kernel"] = (
+                    "gate/up with SwiGLU" if which == "gateup" else "down")
+                del prod_out
                 R, K = prob["qa"].shape
                 N = prob["qw"].shape[1]
                 row["shape"] = {"rows": R, "N": N, "K": K, "groups": cfg.E}
@@ -730,7 +889,8 @@ def run_compare_scales(args, cfg, local_rank):
         "data": "synthetic", "config": {"workload": describe(cfg),
                                         "l2": "flushed before every call"},
         "engine": "one tcgen05 engine for all three modes (128 x 128 tiles); "
-                  "ptpc_production = moe_grouped_gemm (the layer's kernel)",
+                  "ptpc_production = moe_grouped_gemm, the layer's own kernel "
+                  "(gate/up: with its SwiGLU epilogue)",
         "gemms": result, "clocks": sampler.summary(t0, t1)}), flush=True)
 
 
@@ -740,8 +900,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-workloads", action="store_true",
+                    help="time only the named workload (the others are "
+                         "otherwise timed after it, N=1 only)")
     ap.add_argument("--router-gemm", action="store_true",
                     help="route every workload from a bf16 router matrix: the "
                          "fused tensor-core router GEMM + top-k is in the step")
@@ -769,7 +932,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            run_reference(args, cfg)
+            run_reference(args, cfg, world)
         return
     if args.compare_scales:
         if rank == 0:

@@ -68,7 +68,8 @@ _SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P, _P, _SZ,
                                   ctypes.POINTER(ctypes.c_void_p), _I, _P]),
     "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
-    "moe_debug_expire_wait": (_I, [_I, _P]),
+    "moe_workspace_status": (_I, [_P, _SZ, _P, ctypes.POINTER(ctypes.c_uint)]),
+    "moe_debug_expire_wait": (_I, [_I, _P, _SZ, _P]),
     "moe_router_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_add_rmsnorm_quant": (_I, [_P, _P, _P, ctypes.c_float, _I64, _I, _P, _P, _I,
                                    _I64, _P, _P, _P, _P, _P]),
@@ -489,15 +490,27 @@ def moe_add_rmsnorm_quant(x, residual, gamma, eps=1e-6, dst_rows=None, copies=1,
     return residual_out, out_q, out_scale, gate_out
 
 
-def moe_debug_expire_wait(limit_us, stream=None):
+def moe_debug_expire_wait(limit_us, ws=None, stream=None):
     """Launch a bounded wait that nothing completes (expires after limit_us);
-    the next moe_device_status() reports it. Raises MoeError on bad input."""
-    _check("moe_debug_expire_wait",
-           load_library().moe_debug_expire_wait(int(limit_us), _stream(stream)))
+    the next moe_workspace_status(ws) (moe_device_status() without a
+    workspace) reports it. Raises MoeError on bad input."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("moe_debug_expire_wait", load_library().moe_debug_expire_wait(
+        int(limit_us), _ptr(ws), nbytes, _stream(stream)))
 
 
 def moe_device_status(stream=None):
-    """Synchronise the stream and return (status, error bits)."""
+    """Errors of the standalone steps: read and clear the device error word
+    on the stream, synchronise it, and return (status, error bits)."""
     detail = ctypes.c_uint(0)
     st = load_library().moe_device_status(_stream(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def moe_workspace_status(ws, stream=None):
+    """Errors of the most recent forward on workspace `ws`: read and clear its
+    error word on the stream, synchronise it, return (status, error bits)."""
+    detail = ctypes.c_uint(0)
+    st = load_library().moe_workspace_status(
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream), ctypes.byref(detail))
     return st, detail.value

@@ -9,22 +9,57 @@
 
 namespace moe {
 
-// Set by kernels whose bounded wait ran out; read and cleared by
-// moe_device_status().
+// Set by kernels of the standalone entry points whose bounded wait ran out;
+// read and cleared by moe_device_status(). moe_forward's kernels report into
+// a word inside the forward's own workspace instead (moe_workspace_status).
 __device__ unsigned g_error_word;
+// Where moe_device_status's read-and-clear leaves the old value.
+__device__ unsigned g_error_taken;
 
-unsigned* device_error_word() {
+namespace {
+
+// The error word of the launches the calling thread is making, when a
+// forward has set one (ErrorWordScope).
+thread_local unsigned* t_error_word = nullptr;
+
+unsigned* symbol_address(const void* symbol) {
+  void* p = nullptr;
+  return cudaGetSymbolAddress(&p, symbol) == cudaSuccess ? static_cast<unsigned*>(p)
+                                                         : nullptr;
+}
+
+// Per-device addresses of g_error_word (slot 0) and g_error_taken (slot 1).
+unsigned* global_word(int which) {
   static std::mutex mu;
-  static unsigned* addr[64] = {};
+  static unsigned* addr[64][2] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess)
-      addr[dev] = static_cast<unsigned*>(p);
-  }
-  return addr[dev];
+  if (addr[dev][which] == nullptr)
+    addr[dev][which] = symbol_address(which == 0 ? static_cast<const void*>(&g_error_word)
+                                                 : static_cast<const void*>(&g_error_taken));
+  return addr[dev][which];
+}
+
+}  // namespace
+
+unsigned* device_error_word() {
+  return t_error_word != nullptr ? t_error_word : global_word(0);
+}
+
+// While alive, the kernels the calling thread launches report into `word`.
+struct ErrorWordScope {
+  unsigned* prev;
+  explicit ErrorWordScope(unsigned* word) : prev(t_error_word) { t_error_word = word; }
+  ~ErrorWordScope() { t_error_word = prev; }
+  ErrorWordScope(const ErrorWordScope&) = delete;
+  ErrorWordScope& operator=(const ErrorWordScope&) = delete;
+};
+
+// taken = the word's bits; the word = 0, in one atomic step, so that a bit a
+// kernel sets concurrently is either taken now or left for the next read.
+__global__ void take_error_word_kernel(unsigned* word, unsigned* taken) {
+  *taken = atomicExch(word, 0u);
 }
 
 // One thread waits, with a bounded wait like every wait of the layer's
@@ -56,10 +91,14 @@ inline int cuda_status(cudaError_t e) {
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Byte offsets of the intermediates inside the moe_forward workspace.
+// Byte offsets of the intermediates inside the moe_forward workspace. The
+// first kForwardStatusBytes hold the forward's error word and the slot its
+// read-and-clear copies from (moe_workspace_status).
+constexpr size_t kForwardStatusBytes = 256;
+
 struct ForwardLayout {
-  size_t ids, w, logits, counts, offsets, s2f, f2s, perm, xq, sx, gate, h, hq,
-      sh, y, row_scale, w_bound, total;
+  size_t status, ids, w, logits, counts, offsets, s2f, f2s, perm, xq, sx, gate, h,
+      hq, sh, y, row_scale, w_bound, total;
 };
 
 // The expert output y goes through HBM in fp32 while it is small, and in the
@@ -81,6 +120,7 @@ ForwardLayout forward_layout(const moe_dims& d) {
     off = align256(off + bytes);
     return o;
   };
+  L.status = take(kForwardStatusBytes);
   L.ids = take(R * 4);
   L.w = take(R * 4);
   L.logits = take((size_t)d.T * d.E * 4);
@@ -349,7 +389,11 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
   int st = check_dims(dims);
   if (st != MOE_OK) return st;
   const moe_dims d = *dims;
-  if (d.T == 0) return MOE_OK;   // empty batch: nothing to read or write
+  if (d.T == 0) {   // empty batch: nothing to read or write but the error word
+    if (ws != nullptr && ws_bytes >= kForwardStatusBytes && aligned16(ws))
+      return cuda_status(cudaMemsetAsync(ws, 0, sizeof(unsigned), stream));
+    return MOE_OK;
+  }
   if ((router_logits == nullptr) == (router_w == nullptr)) return MOE_ERR_INVALID_ARG;
   if (d.shared && shared_gate_w == nullptr) return MOE_ERR_INVALID_ARG;
   if (!d.shared && shared_gate_w != nullptr) return MOE_ERR_INVALID_ARG;
@@ -370,6 +414,13 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
 
   uint8_t* base = static_cast<uint8_t*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+  // This forward's kernels report expired waits into the workspace's own
+  // error word, cleared first (in stream order), so that forwards on other
+  // streams and workspaces never see each other's errors.
+  auto* err_word = static_cast<unsigned*>(at(L.status));
+  if (cudaMemsetAsync(err_word, 0, sizeof(unsigned), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  ErrorWordScope err_scope(err_word);
   const int64_t R = (int64_t)d.T * d.k;
   const int64_t rows = R + (d.shared ? d.T : 0);
   const int G = d.E + (d.shared ? 1 : 0);
@@ -482,6 +533,31 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
 
 }  // namespace
 
+namespace {
+
+// Read and clear an error word on `stream` (after everything queued before),
+// then map its bits to a status.
+int take_status(unsigned* word, unsigned* taken, moe_stream_t stream, unsigned* detail) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  take_error_word_kernel<<<1, 1, 0, s>>>(word, taken);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpyAsync(&bits, taken, sizeof(bits), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = bits;
+  if (bits == 0) return MOE_OK;
+  // a tile map larger than the launch alone: group offsets past a_rows
+  return bits == moe::kErrBadIndex ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
+}
+
+bool forward_status_ok(const void* ws, size_t ws_bytes) {
+  return ws != nullptr && ws_bytes >= kForwardStatusBytes && aligned16(ws);
+}
+
+}  // namespace
+
 extern "C" {
 
 int moe_forward(const moe_dims* dims, const uint16_t* x,
@@ -564,9 +640,11 @@ int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
                       reinterpret_cast<cudaEvent_t const*>(events), stream);
 }
 
-int moe_debug_expire_wait(int limit_us, moe_stream_t stream) {
+
+int moe_debug_expire_wait(int limit_us, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
-  unsigned* err = moe::device_error_word();
+  if (ws != nullptr && !forward_status_ok(ws, ws_bytes)) return MOE_ERR_INVALID_ARG;
+  unsigned* err = ws != nullptr ? static_cast<unsigned*>(ws) : moe::device_error_word();
   if (err == nullptr) return MOE_ERR_CUDA;
   moe::expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       1000ull * (unsigned long long)limit_us, err);
@@ -575,19 +653,18 @@ int moe_debug_expire_wait(int limit_us, moe_stream_t stream) {
 
 int moe_device_status(moe_stream_t stream, unsigned* detail) {
   if (detail) *detail = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
-  unsigned word = 0;
-  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (word != 0) {
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
-  if (detail) *detail = word;
-  if (word == 0) return MOE_OK;
-  // a tile map larger than the launch alone: group offsets past a_rows
-  return word == moe::kErrBadIndex ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
+  unsigned* word = global_word(0);
+  unsigned* taken = global_word(1);
+  if (word == nullptr || taken == nullptr) return MOE_ERR_CUDA;
+  return take_status(word, taken, stream, detail);
+}
+
+int moe_workspace_status(void* ws, size_t ws_bytes, moe_stream_t stream,
+                         unsigned* detail) {
+  if (detail) *detail = 0;
+  if (!forward_status_ok(ws, ws_bytes)) return MOE_ERR_INVALID_ARG;
+  auto* w = static_cast<unsigned*>(ws);
+  return take_status(w, w + 1, stream, detail);
 }
 
 }  // extern "C"

@@ -45,7 +45,15 @@ class MoELayer:
         need = max(binding.moe_forward_workspace_size(self.dims(T)), 1)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.w_gu.device)
+            self._ws[:min(need, 256)].zero_()   # the forward's error word
         return self._ws
+
+    def status(self, stream=None):
+        """(status, error bits) of the most recent forward on this layer's
+        workspace (read and cleared; synchronises the stream)."""
+        if self._ws is None:
+            return 0, 0
+        return binding.moe_workspace_status(self._ws, stream)
 
     def forward(self, x, router_logits=None, out=None, topk_ids=None,
                 topk_w=None, stream=None, events=None, residual=None, gamma=None,

@@ -25,7 +25,9 @@
  *    e4m3 codes (OCP "E4M3": bias 7, max 448, no infinities).
  *  - The return value is a status (moe_status) for argument and launch
  *    errors, known before the kernels run. Errors found by a running kernel
- *    (a bounded wait that expired) are reported by moe_device_status().
+ *    (a bounded wait that expired) are reported by moe_workspace_status() for
+ *    moe_forward and its variants (each workspace has its own error word),
+ *    and by moe_device_status() for the standalone steps.
  *  - Device pointers must be 16-byte aligned. D and I must be multiples of
  *    128; 1 <= k <= min(E, 32); E <= 1024.
  *  - NaN or infinite inputs are outside the contract.
@@ -332,7 +334,11 @@ MOE_API int moe_combine_f16(const uint16_t* y16, const float* row_scale,
  *   out [T, D] bf16 (written). topk_ids_out [T, k] / topk_w_out [T, k]:
  *   optional, receive the routing when non-NULL.
  *   ws: device workspace of moe_forward_workspace_size(dims) bytes; it holds
- *   the routing, permutation, quantised activations and GEMM intermediates.
+ *   the routing, permutation, quantised activations and GEMM intermediates,
+ *   and in its first 256 bytes the forward's error word: each call clears it
+ *   (in stream order) before its first kernel, and its kernels record there
+ *   the bounded waits that expire; moe_workspace_status() reads it. Two
+ *   forwards in flight at once need two workspaces.
  * Errors: those of the steps; MOE_ERR_WORKSPACE if ws_bytes is too small.
  */
 MOE_API size_t moe_forward_workspace_size(const moe_dims* dims);
@@ -379,6 +385,22 @@ MOE_API int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
 MOE_API int moe_device_status(moe_stream_t stream, unsigned* detail);
 
 /*
+ * moe_workspace_status - the same for the kernels of the forwards that ran
+ * on workspace `ws` (moe_forward, moe_forward_profiled, moe_forward_prenorm,
+ * or moe_debug_expire_wait given that workspace): enqueue on `stream` a
+ * one-thread kernel that takes the workspace's error word and clears it in
+ * one atomic exchange, copy the bits back and synchronise `stream`. Call it
+ * on the stream the forward ran on (or after synchronising with it). A
+ * forward clears the word when it starts, so the bits are those of the most
+ * recent forward on `ws` (and of debug waits queued after it); a second call
+ * without a new forward returns MOE_OK. Status values and `detail` bits as
+ * for moe_device_status. Errors: MOE_ERR_INVALID_ARG (ws NULL, misaligned or
+ * ws_bytes < 256), MOE_ERR_CUDA.
+ */
+MOE_API int moe_workspace_status(void* ws, size_t ws_bytes, moe_stream_t stream,
+                                 unsigned* detail);
+
+/*
  * moe_forward_prenorm - moe_forward fed from the residual stream: the
  * quantisation step becomes moe_add_rmsnorm_quant(x, pre->residual,
  * pre->gamma, pre->eps), which also writes pre->residual_out, and the shared
@@ -408,13 +430,17 @@ MOE_API int moe_forward_prenorm(const moe_dims* dims, const moe_prenorm* pre,
  * moe_debug_expire_wait - failure-detection check without a GPU fault: one
  * thread waits on an mbarrier that nothing arrives on, bounded exactly like
  * the waits of the layer's kernels but with a limit of `limit_us`
- * microseconds (1 .. 1,000,000), and records the expiry in the device error
- * word. The kernel then ends normally and the context stays usable: the next
- * moe_device_status() returns MOE_ERR_TIMEOUT with `detail` bit 64 and clears
- * it. No counterpart in the pages (test support). Returns MOE_OK,
- * MOE_ERR_INVALID_ARG (limit out of range, nothing launched) or MOE_ERR_CUDA.
+ * microseconds (1 .. 1,000,000), and records the expiry in an error word:
+ * that of the forward workspace `ws` (ws_bytes >= 256) when ws is non-NULL,
+ * else the device error word of the standalone steps. The kernel then ends
+ * normally and the context stays usable: the next moe_workspace_status(ws)
+ * (or moe_device_status()) returns MOE_ERR_TIMEOUT with `detail` bit 64 and
+ * clears it. No counterpart in the pages (test support). Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG (limit out of range, bad workspace; nothing launched)
+ * or MOE_ERR_CUDA.
  */
-MOE_API int moe_debug_expire_wait(int limit_us, moe_stream_t stream);
+MOE_API int moe_debug_expire_wait(int limit_us, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
 
 /*
  * FP8 with per-K-block scales: the alternatives to PTPC that the pages

@@ -93,8 +93,14 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.moe_grouped_gemm_scaled(2, None, None, 0, None, None, None, 2, 128,
                                        256, None, None) == 0              # no rows
     # the failure-detection check validates its limit before touching CUDA
-    assert lib.moe_debug_expire_wait(0, None) == -1
-    assert lib.moe_debug_expire_wait(2000000, None) == -1
+    assert lib.moe_debug_expire_wait(0, None, 0, None) == -1
+    assert lib.moe_debug_expire_wait(2000000, None, 0, None) == -1
+    # a forward workspace smaller than its error word is refused, unlaunched
+    fake16 = ctypes.c_void_p(0x1000)
+    assert lib.moe_debug_expire_wait(10, fake16, 128, None) == -1
+    assert lib.moe_workspace_status(None, 1024, None, None) == -1
+    assert lib.moe_workspace_status(fake16, 255, None, None) == -1
+    assert lib.moe_workspace_status(ctypes.c_void_p(0x1008), 4096, None, None) == -1
     # workspace too small is reported before any launch
     fake = ctypes.c_void_p(0x1000)
     rc = lib.moe_forward(ctypes.byref(d), fake, fake, None, fake, fake, fake,

@@ -78,7 +78,7 @@ class _Run:
         ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
         tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
         out = self.layer.forward(x, logits, topk_ids=ids, topk_w=tw)
-        st, bits = binding.moe_device_status()
+        st, bits = self.layer.status()
         assert st == 0, f"device status {st} bits {bits:#x}"
 
         xn = x.float().cpu().numpy()
@@ -216,7 +216,7 @@ def test_prenorm_layer_all_tokens(cfg):
     res_out = torch.empty_like(res_d)
     out = run.layer.forward(x, logits, residual=res_d, gamma=gamma.cuda(),
                             eps=1e-6, residual_out=res_out)
-    st, bits = binding.moe_device_status()
+    st, bits = run.layer.status()
     assert st == 0, bits
     ref = oracle.add_rmsnorm_ref(x.float().cpu().numpy(), res.float().numpy(),
                                  gamma.float().numpy(), 1e-6)
@@ -252,7 +252,7 @@ def test_prenorm_prefill_sampled():
     res_out = torch.empty((cfg.T, cfg.D), dtype=torch.bfloat16, device="cuda")
     out = run.layer.forward(x, logits, residual=res.cuda(), gamma=gamma.cuda(),
                             eps=1e-6, residual_out=res_out)
-    st, bits = binding.moe_device_status()
+    st, bits = run.layer.status()
     assert st == 0, bits
     ref = oracle.add_rmsnorm_ref(x.float().cpu().numpy(), res.float().numpy(),
                                  gamma.float().numpy(), 1e-6)
@@ -294,8 +294,9 @@ def test_forward_on_two_streams_at_once():
                                 shared_gate_w=L.shared_gate_w, out=outs[i], ws=ws[i],
                                 stream=streams[i])
     torch.cuda.synchronize()
-    st, bits = binding.moe_device_status()
-    assert st == 0, bits
+    for i in range(2):
+        st, bits = binding.moe_workspace_status(ws[i], streams[i])
+        assert st == 0, bits
     assert torch.equal(outs[0].view(torch.int16), ref1.view(torch.int16))
     assert torch.equal(outs[1].view(torch.int16), ref2.view(torch.int16))
 
