@@ -10,8 +10,10 @@ boundary inside its slice (`parity_tokens`). The GPU-quantised weights of
 every expert the sample touches are compared byte for byte with the
 oracle's.
 
-Accuracy contract on bf16 outputs: max|gpu - oracle| <= 2e-2 * rms(oracle) and
-sum|gpu - oracle| / sum|oracle| <= 5e-3."""
+Accuracy contract on bf16 outputs against the oracle's exact output:
+max|gpu - oracle| <= 2e-2 * rms(oracle) beyond the half bf16 ulp that the
+output's own rounding may cost each element, and sum|gpu - oracle| /
+sum|oracle| <= 5e-3 (gpu_helpers.layer_tolerance_ok)."""
 
 import numpy as np
 import pytest
@@ -140,8 +142,9 @@ class _Run:
             xn, k, lambda e: qmap[e], E, logits=ln, w_g=wg,
             renormalize=cfg.renormalize, tokens=tokens)
         got = out.float().cpu().numpy()[tokens]
-        ok, max_rel, l1 = layer_tolerance_ok(got, r["out64"])
-        assert ok, f"{cfg.name}: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
+        ok, max_rel, l1, raw = layer_tolerance_ok(got, r["out64"])
+        assert ok, (f"{cfg.name}: max excess/rms {max_rel:.3e} (raw {raw:.3e}), "
+                    f"L1 ratio {l1:.3e}")
         return max_rel, l1
 
 
@@ -231,8 +234,8 @@ def test_prenorm_layer_all_tokens(cfg):
     wg = run.layer.shared_gate_w.float().cpu().numpy() if cfg.shared else None
     r = oracle.moe_forward_ref(ref[1], cfg.k, lambda e: qmap[e], cfg.E, logits=ln,
                                w_g=wg, renormalize=cfg.renormalize)
-    ok, max_rel, l1 = layer_tolerance_ok(out.float().cpu().numpy(), r["out64"])
-    assert ok, f"{cfg.name}: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
+    ok, max_rel, l1, raw = layer_tolerance_ok(out.float().cpu().numpy(), r["out64"])
+    assert ok, f"{cfg.name}: max excess/rms {max_rel:.3e} (raw {raw:.3e}), L1 ratio {l1:.3e}"
 
 
 def test_prenorm_prefill_sampled():
@@ -264,8 +267,9 @@ def test_prenorm_prefill_sampled():
     qmap = run.expert_weights(touched)
     r = oracle.moe_forward_ref(ref[1], cfg.k, lambda e: qmap[e], cfg.E, logits=ln,
                                renormalize=cfg.renormalize, tokens=tokens)
-    ok, max_rel, l1 = layer_tolerance_ok(out.float().cpu().numpy()[tokens], r["out64"])
-    assert ok, f"prefill prenorm: max/rms {max_rel:.3e}, L1 ratio {l1:.3e}"
+    ok, max_rel, l1, raw = layer_tolerance_ok(out.float().cpu().numpy()[tokens], r["out64"])
+    assert ok, (f"prefill prenorm: max excess/rms {max_rel:.3e} (raw {raw:.3e}), "
+                f"L1 ratio {l1:.3e}")
 
 
 def test_forward_on_two_streams_at_once():

@@ -41,3 +41,20 @@ def test_sample_covers_tile_boundaries(rng, T, E, k, shared, skew):
 def test_sample_is_all_tokens_for_small_batches(rng):
     ids = _routing(100, 16, 2, rng)
     assert np.array_equal(parity_tokens(ids, 16, True, n_min=256), np.arange(100))
+
+
+def test_bf16_half_ulp_bounds_the_rounding(rng):
+    """bf16_half_ulp(v) is the largest move of rounding v to bf16: torch's
+    round-to-nearest-even never exceeds it, and a value half-way between two
+    bf16 numbers reaches it exactly."""
+    import torch
+    from tests.gpu_helpers import bf16_half_ulp
+    v = rng.standard_normal(200_000) * np.exp2(rng.integers(-20, 20, 200_000))
+    r = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    v32 = v.astype(np.float32).astype(np.float64)
+    assert np.all(np.abs(r - v32) <= bf16_half_ulp(v32))
+    mid = np.array([1.0 + 2.0 ** -8, 3.0 + 2.0 ** -7, -0.75 - 2.0 ** -9])
+    assert np.allclose(bf16_half_ulp(mid), [2.0 ** -8, 2.0 ** -7, 2.0 ** -9])
+    r_mid = torch.from_numpy(mid).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(np.abs(r_mid - mid), bf16_half_ulp(mid))
+    assert bf16_half_ulp(np.array([0.0]))[0] == 0.0
