@@ -69,6 +69,7 @@ _SIGNATURES = {
                                   ctypes.POINTER(ctypes.c_void_p), _I, _P]),
     "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "moe_workspace_status": (_I, [_P, _SZ, _P, ctypes.POINTER(ctypes.c_uint)]),
+    "moe_forward_intermediates": (_I, [_P, _P, _SZ, _P]),
     "moe_debug_expire_wait": (_I, [_I, _P, _SZ, _P]),
     "moe_router_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_add_rmsnorm_quant": (_I, [_P, _P, _P, ctypes.c_float, _I64, _I, _P, _P, _I,
@@ -331,6 +332,52 @@ def make_dims(T, D, E, k, I, shared, renormalize=True):
 
 def moe_forward_workspace_size(dims):
     return load_library().moe_forward_workspace_size(ctypes.byref(dims))
+
+
+class Intermediates(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "topk_ids", "topk_w", "expert_offsets", "sorted_to_flat", "flat_to_sorted",
+        "xq", "sx", "gate", "h", "hq", "sh", "y", "y_row_scale")] + \
+        [("y_fp16", ctypes.c_int32)]
+
+
+def moe_forward_intermediates(dims, ws):
+    """Views (torch tensors sharing the workspace's memory) of the
+    intermediates the last forward on `ws` left there: offsets, s2f, f2s,
+    xq [T, D], sx [rows], gate [T], h [rows, I], hq [rows, I], sh [rows], and
+    y ([rows, D] fp32, or fp16 codes with y_row_scale [rows])."""
+    m = Intermediates()
+    _check("moe_forward_intermediates", load_library().moe_forward_intermediates(
+        ctypes.byref(dims), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(m)))
+    base = ws.data_ptr()
+    T, D, E, k, I = dims.T, dims.D, dims.E, dims.k, dims.I
+    R = T * k
+    rows = R + (T if dims.shared else 0)
+    G = E + (1 if dims.shared else 0)
+
+    def view(addr, n, dtype, shape):
+        off = addr - base
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[off:off + nbytes].view(dtype).view(shape)
+
+    out = {
+        "expert_offsets": view(m.expert_offsets, G + 1, torch.int32, (G + 1,)),
+        "sorted_to_flat": view(m.sorted_to_flat, R, torch.int32, (R,)),
+        "flat_to_sorted": view(m.flat_to_sorted, R, torch.int32, (R,)),
+        "xq": view(m.xq, T * D, torch.uint8, (T, D)),
+        "sx": view(m.sx, rows, torch.float32, (rows,)),
+        "gate": view(m.gate, T, torch.float32, (T,)),
+        "h": view(m.h, rows * I, torch.float32, (rows, I)),
+        "hq": view(m.hq, rows * I, torch.uint8, (rows, I)),
+        "sh": view(m.sh, rows, torch.float32, (rows,)),
+        "y_fp16": bool(m.y_fp16),
+    }
+    if m.y_fp16:
+        out["y"] = view(m.y, rows * D, torch.float16, (rows, D))
+        out["y_row_scale"] = view(m.y_row_scale, rows, torch.float32, (rows,))
+    else:
+        out["y"] = view(m.y, rows * D, torch.float32, (rows, D))
+    return out
 
 
 def moe_forward(dims, x, w_gu, s_gu, w_d, s_d, router_logits=None,

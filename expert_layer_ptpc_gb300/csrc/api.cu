@@ -129,7 +129,7 @@ ForwardLayout forward_layout(const moe_dims& d) {
   L.s2f = take(R * 4);
   L.f2s = take(R * 4);
   L.perm = take(permute_ws_bytes(R, d.E));
-  L.xq = take(rows * d.D);
+  L.xq = take((size_t)d.T * d.D);   // token order: the gate/up GEMM gathers
   L.sx = take(rows * 4);
   L.gate = take((size_t)d.T * 4);
   L.h = take(rows * d.I * 4);
@@ -373,6 +373,29 @@ size_t moe_forward_workspace_size(const moe_dims* dims) {
   return forward_layout(*dims).total;
 }
 
+int moe_forward_intermediates(const moe_dims* dims, void* ws, size_t ws_bytes,
+                              moe_intermediates* out) {
+  if (check_dims(dims) != MOE_OK || out == nullptr) return MOE_ERR_INVALID_ARG;
+  const ForwardLayout L = forward_layout(*dims);
+  if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  out->topk_ids = reinterpret_cast<int32_t*>(b + L.ids);
+  out->topk_w = reinterpret_cast<float*>(b + L.w);
+  out->expert_offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  out->sorted_to_flat = reinterpret_cast<int32_t*>(b + L.s2f);
+  out->flat_to_sorted = reinterpret_cast<int32_t*>(b + L.f2s);
+  out->xq = b + L.xq;
+  out->sx = reinterpret_cast<float*>(b + L.sx);
+  out->gate = reinterpret_cast<float*>(b + L.gate);
+  out->h = reinterpret_cast<float*>(b + L.h);
+  out->hq = b + L.hq;
+  out->sh = reinterpret_cast<float*>(b + L.sh);
+  out->y = b + L.y;
+  out->y_row_scale = reinterpret_cast<float*>(b + L.row_scale);
+  out->y_fp16 = y_in_fp16(*dims) ? 1 : 0;
+  return MOE_OK;
+}
+
 }  // extern "C"
 
 namespace {
@@ -485,23 +508,28 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
                                   d.shared ? d.T : -1, at(L.perm), stream, pdl));
   if (st != MOE_OK) return st;
   mark(3);
-  // x -> FP8 codes written straight into each token's k expert rows (and its
-  // shared-expert row R + t), plus the shared-expert gate.
+  // x -> FP8 codes, once per token (row t of xq), with the token's scale
+  // written to each of its k expert rows (and its shared-expert row R + t),
+  // plus the shared-expert gate.
   if (pre != nullptr)   // r = x + residual, RMSNorm, then the same quantiser
     st = cuda_status(launch_add_rmsnorm_quant(
         x, pre->residual, pre->gamma, pre->eps, d.T, d.D, pre->residual_out, f2s,
         d.k, d.shared ? R : -1, xq, sx, d.shared ? shared_gate_w : nullptr,
-        d.shared ? gate : nullptr, stream, pdl));
+        d.shared ? gate : nullptr, stream, pdl, /*codes_once=*/true));
   else
     st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
                                   d.shared ? R : -1, xq, sx,
                                   d.shared ? shared_gate_w : nullptr,
-                                  d.shared ? gate : nullptr, stream, pdl, false));
+                                  d.shared ? gate : nullptr, stream, pdl, false,
+                                  /*codes_once=*/true));
   if (st != MOE_OK) return st;
   mark(4);
   const int hint = (int)std::max<int64_t>(1, R / d.E);
+  // the gate/up GEMM reads each expert row's token codes through the
+  // permutation (sorted row -> token), from the unpermuted codes
+  const TokenGather gather{s2f, d.k, (int)R, (int64_t)d.T};
   st = launch_grouped_gemm(MOE_GEMM_GATEUP_SWIGLU, xq, sx, rows, w_gu, s_gu,
-                           offsets, G, d.I, d.D, h, hint, stream, pdl);
+                           offsets, G, d.I, d.D, h, hint, stream, pdl, &gather);
   if (st != MOE_OK) return st;
   mark(5);
   st = cuda_status(launch_quant(h, MOE_DTYPE_F32, rows, d.I, nullptr, 1, -1, hq,

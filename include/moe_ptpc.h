@@ -351,6 +351,47 @@ MOE_API int moe_forward(const moe_dims* dims, const uint16_t* x,
                         size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_forward_intermediates - where a forward keeps its intermediates inside
+ * workspace `ws` (for inspection and tests; no kernel runs, nothing is
+ * copied). After a moe_forward (or variant) with the same dims and ws has
+ * completed on its stream, the fields below point into ws and hold that
+ * forward's values; R = T k routed rows, rows = R + T (shared) or R, sorted
+ * rows in expert order (the layout of moe_permute), G = E + shared:
+ *   topk_ids, topk_w [T, k]: the routing (valid only when the forward was not
+ *     given topk_ids_out / topk_w_out, which then received it);
+ *   expert_offsets [G + 1], sorted_to_flat [R], flat_to_sorted [R];
+ *   xq [T, D] e4m3: each token's codes once, in token order (the gate/up GEMM
+ *     reads them through the permutation); sx [rows] fp32: the token's scale
+ *     at each of its sorted rows; gate [T] fp32: the shared expert's gate;
+ *   h [rows, I] fp32: SwiGLU output of the gate/up GEMM; hq [rows, I] e4m3 and
+ *     sh [rows] fp32: its per-row requantisation;
+ *   y: the down GEMM's output, fp32 [rows, D] when y_fp16 == 0, else fp16 codes
+ *     [rows, D] with y = y_row_scale[r] * code.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG (bad dims or NULL out) or
+ * MOE_ERR_WORKSPACE (ws NULL, misaligned or smaller than the forward needs).
+ * No counterpart in the pages (inspection support).
+ */
+typedef struct moe_intermediates {
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* expert_offsets;
+  int32_t* sorted_to_flat;
+  int32_t* flat_to_sorted;
+  uint8_t* xq;
+  float* sx;
+  float* gate;
+  float* h;
+  uint8_t* hq;
+  float* sh;
+  void* y;
+  float* y_row_scale;
+  int32_t y_fp16;
+} moe_intermediates;
+
+MOE_API int moe_forward_intermediates(const moe_dims* dims, void* ws, size_t ws_bytes,
+                                      moe_intermediates* out);
+
+/*
  * moe_forward_profiled - moe_forward with timing marks: identical work and
  *   arguments, plus `events`, an array of MOE_FORWARD_EVENTS cudaEvent_t
  *   created by the caller, recorded on `stream` at the step boundaries:

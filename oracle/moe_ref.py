@@ -190,9 +190,17 @@ def expert_ffn_ref(xq, sx, wgu_codes, sgu, wd_codes, sd):
     g, u = gu[:, :I], gu[:, I:]
     h = silu_ref(g) * u
     h32 = h.astype(np.float32)
+    hq, sh, y = down_from_h_ref(h32, wd_codes, sd)
+    return {"g": g, "u": u, "h": h, "h32": h32, "hq": hq, "sh": sh, "y": y}
+
+
+def down_from_h_ref(h32, wd_codes, sd):
+    """The expert's steps after SwiGLU, from fp32 h [rows, I]: per-row FP8
+    requantisation (PTPC, per token), then the down GEMM against
+    wd_codes [D, I] with its per-channel scales. Returns (hq, sh, y fp64)."""
     hq, sh = quant_rows_ref(h32)
     y = ptpc_matmul_ref(hq, sh, wd_codes, sd)
-    return {"h": h, "h32": h32, "hq": hq, "sh": sh, "y": y}
+    return hq, sh, y
 
 
 # ---------------------------------------------------------------------------
@@ -274,6 +282,7 @@ def quantize_expert_ref(w_gu, w_d):
 __all__ = [
     "router_logits_ref", "route_ref", "permute_ref", "quant_rows_ref",
     "dequant_rows_ref", "ptpc_matmul_ref", "silu_ref", "sigmoid_ref",
-    "expert_ffn_ref", "shared_gate_ref", "moe_forward_ref", "moe_flops",
+    "expert_ffn_ref", "down_from_h_ref", "shared_gate_ref", "moe_forward_ref",
+    "moe_flops",
     "quantize_expert_ref",
 ]

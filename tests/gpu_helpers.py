@@ -133,3 +133,112 @@ def parity_tokens(ids, E, shared, n_min=256, seed=0):
         rest = np.setdiff1d(np.arange(T), np.fromiter(toks, np.int64))
         toks.update(int(t) for t in rng.choice(rest, want - len(toks), replace=False))
     return np.array(sorted(toks), dtype=np.int64)
+
+
+def swiglu_bound(g, u, abs_g, abs_u, K):
+    """Bound on |h_gpu - h| for h = silu(g) u computed by the gate/up GEMM's
+    epilogue from fp32 g and u (each within gemm_bound of the exact value):
+    first-order propagation of the two GEMM errors, plus the fp32 evaluation
+    with the fast exponential and division (CUDA documents at most
+    2 + floor(1.173 |x|) ulp for __expf(x) and 2 ulp for __fdividef in this
+    range) and the scaling multiplies."""
+    eg = gemm_bound(abs_g, K)
+    eu = gemm_bound(abs_u, K)
+    sig = oracle.sigmoid_ref(g)
+    silu = g * sig
+    dsilu = np.abs(sig * (1 + g * (1 - sig)))
+    ulps = 16 + 2 + np.floor(1.173 * np.abs(g))
+    return dsilu * np.abs(u) * eg + np.abs(silu) * eu + ulps * U32 * np.abs(silu * u) + 1e-30
+
+
+def staged_layer_check(cfg, xv, out_tokens, ids, w, inter, tokens, qmap, w_g):
+    """Stage-by-stage parity of one forward on the sampled `tokens`, read
+    from the forward's own intermediates (moe_forward_intermediates):
+
+    * x codes (token order) and each row's scale: bit-exact against the
+      oracle's quantiser on the layer input xv;
+    * h of every row of the sample: within the fp32 GEMM + SwiGLU bound of
+      the oracle's exact h;
+    * the requantisation is an integer decision taken in fp32: the oracle
+      takes it on the GPU's own fp32 h, and codes and scales must then match
+      bit for bit;
+    * y: within the fp32 accumulation bound (plus the fp16 encoding's
+      rounding) of the oracle's down GEMM on those codes;
+    * out: the accuracy contract (layer_tolerance_ok) against the oracle's
+      combine of that y, in fp64 with one bf16 rounding.
+
+    `ids` / `w`: the routing (oracle's, equal to the GPU's on these tokens);
+    `qmap[e]`: the oracle-quantised weights of expert e (E: the shared
+    expert), `w_g` the shared gate vector or None. Returns the contract's
+    (max excess / rms, L1 ratio, raw max / rms)."""
+    T, D, E, k, I = cfg.T, cfg.D, cfg.E, cfg.k, cfg.I
+    R = T * k
+    tokens = np.asarray(tokens, np.int64)
+    n = tokens.size
+    f2s = inter["flat_to_sorted"].cpu().numpy().astype(np.int64).reshape(T, k)
+    rows = f2s[tokens]                                   # [n, k]
+    experts = np.asarray(ids)[tokens].astype(np.int64)   # [n, k]
+    flat_rows = rows.ravel()
+    flat_exp = experts.ravel()
+    flat_tok = np.repeat(np.arange(n), k)
+    if cfg.shared:
+        flat_rows = np.concatenate([flat_rows, R + tokens])
+        flat_exp = np.concatenate([flat_exp, np.full(n, E)])
+        flat_tok = np.concatenate([flat_tok, np.arange(n)])
+    dev_rows = torch.as_tensor(flat_rows, device=inter["h"].device)
+    dev_tok = torch.as_tensor(tokens, device=inter["h"].device)
+    h_g = inter["h"].index_select(0, dev_rows).cpu().numpy()
+    hq_g = inter["hq"].index_select(0, dev_rows).cpu().numpy()
+    sh_g = inter["sh"].index_select(0, dev_rows).cpu().numpy()
+    sx_g = inter["sx"].index_select(0, dev_rows).cpu().numpy()
+    xq_g = inter["xq"].index_select(0, dev_tok).cpu().numpy()
+    y_g = inter["y"].index_select(0, dev_rows).double()
+    if inter["y_fp16"]:
+        rs = inter["y_row_scale"].index_select(0, dev_rows).double()
+        y_g = y_g * rs[:, None]
+        rs = rs.cpu().numpy()
+    y_g = y_g.cpu().numpy()
+
+    xq_o, sx_o = oracle.quant_rows_ref(np.asarray(xv, np.float32)[tokens])
+    assert np.array_equal(xq_g, xq_o), "x codes differ"
+    assert np.array_equal(sx_g.view(np.uint32), sx_o[flat_tok].view(np.uint32)), \
+        "x scales differ"
+
+    y_al = np.zeros((flat_rows.size, D))
+    for e in np.unique(flat_exp):
+        sel = np.flatnonzero(flat_exp == e)
+        wgu, sgu, wd, sd = qmap[int(e)]
+        xr, sr = xq_o[flat_tok[sel]], sx_o[flat_tok[sel]]
+        gu = oracle.ptpc_matmul_ref(xr, sr, wgu, sgu)
+        absgu = (np.abs(oracle.e4m3_decode(xr)) @ np.abs(oracle.e4m3_decode(wgu)).T) * \
+            sr[:, None].astype(np.float64) * sgu[None, :].astype(np.float64)
+        g, u = gu[:, :I], gu[:, I:]
+        h64 = oracle.silu_ref(g) * u
+        hb = swiglu_bound(g, u, absgu[:, :I], absgu[:, I:], D)
+        err = np.abs(h_g[sel].astype(np.float64) - h64)
+        bad = err > hb
+        assert not bad.any(), ("h", int(e), np.argwhere(bad)[:3], err[bad][:3], hb[bad][:3])
+        hq_o, sh_o, y64 = oracle.down_from_h_ref(h_g[sel], wd, sd)
+        assert np.array_equal(hq_o, hq_g[sel]), ("h codes", int(e))
+        assert np.array_equal(sh_o.view(np.uint32), sh_g[sel].view(np.uint32)), \
+            ("h scales", int(e))
+        absy = (np.abs(oracle.e4m3_decode(hq_o)) @ np.abs(oracle.e4m3_decode(wd)).T) * \
+            sh_o[:, None].astype(np.float64) * sd[None, :].astype(np.float64)
+        yb = gemm_bound(absy, I) + 1e-30
+        if inter["y_fp16"]:
+            yb = yb * (1 + 1e-3) + np.abs(y64) * (2.0 ** -11 + 4 * U32) + \
+                rs[sel, None] * 2.0 ** -25
+        err = np.abs(y_g[sel] - y64)
+        bad = err > yb
+        assert not bad.any(), ("y", int(e), np.argwhere(bad)[:3], err[bad][:3], yb[bad][:3])
+        y_al[sel] = y64
+
+    w = np.asarray(w, np.float64)[tokens]                 # [n, k]
+    out_al = (w[:, :, None] * y_al[:n * k].reshape(n, k, D)).sum(axis=1)
+    if cfg.shared:
+        gate = oracle.shared_gate_ref(np.asarray(xv, np.float64)[tokens], w_g)
+        out_al = out_al + gate[:, None] * y_al[n * k:]
+    ok, max_rel, l1, raw = layer_tolerance_ok(out_tokens, out_al)
+    assert ok, (f"{cfg.name}: against the oracle on the GPU's requant decisions: "
+                f"max excess/rms {max_rel:.3e} (raw {raw:.3e}), L1 ratio {l1:.3e}")
+    return max_rel, l1, raw
