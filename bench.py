@@ -227,11 +227,10 @@ def algorithmic_bytes(cfg, counts):
 
 def gateup_bytes(cfg, touched):
     """Algorithmic bytes of one gate/up GEMM launch: per touched expert its
-    2I x D FP8 weights and 2I fp32 scales; each token's D FP8 codes (read
-    through the gather, once per token) and each row's scale in, the I fp32
-    outputs of every row out."""
+    2I x D FP8 weights and 2I fp32 scales; per row the D FP8 codes and scale
+    in, the I fp32 outputs out."""
     rows = cfg.rows
-    return touched * (2 * cfg.I * cfg.D + 8 * cfg.I) + cfg.T * cfg.D + rows * 4 + \
+    return touched * (2 * cfg.I * cfg.D + 8 * cfg.I) + rows * (cfg.D + 4) + \
         rows * cfg.I * 4
 
 
@@ -254,9 +253,9 @@ def implementation_bytes(cfg, touched, pre=False):
     # permutation: ids in; counts, offsets and both row maps out
     b += 4 * R + 8 * (cfg.groups + 1) + 8 * R
     # quantiser: x in (and the residual and gamma, the new residual out, for
-    # the pre-norm forward), the codes of every token and the scale of every
-    # destination row out, the shared gate's weights in and gate out
-    b += 2 * T * D + (2 * T * D * 2 + 2 * D if pre else 0) + T * D + rows * 4
+    # the pre-norm forward), codes and scales of every destination row out,
+    # the shared gate's weights in and gate out
+    b += 2 * T * D + (2 * T * D * 2 + 2 * D if pre else 0) + rows * (D + 4)
     b += (2 * D + 4 * T) if cfg.shared else 0
     # gate/up GEMM: weights, codes and scales in, fp32 h out
     b += gateup_bytes(cfg, touched)

@@ -344,7 +344,7 @@ class Intermediates(ctypes.Structure):
 def moe_forward_intermediates(dims, ws):
     """Views (torch tensors sharing the workspace's memory) of the
     intermediates the last forward on `ws` left there: offsets, s2f, f2s,
-    xq [T, D], sx [rows], gate [T], h [rows, I], hq [rows, I], sh [rows], and
+    xq [rows, D], sx [rows], gate [T], h [rows, I], hq [rows, I], sh [rows], and
     y ([rows, D] fp32, or fp16 codes with y_row_scale [rows])."""
     m = Intermediates()
     _check("moe_forward_intermediates", load_library().moe_forward_intermediates(
@@ -364,7 +364,7 @@ def moe_forward_intermediates(dims, ws):
         "expert_offsets": view(m.expert_offsets, G + 1, torch.int32, (G + 1,)),
         "sorted_to_flat": view(m.sorted_to_flat, R, torch.int32, (R,)),
         "flat_to_sorted": view(m.flat_to_sorted, R, torch.int32, (R,)),
-        "xq": view(m.xq, T * D, torch.uint8, (T, D)),
+        "xq": view(m.xq, rows * D, torch.uint8, (rows, D)),
         "sx": view(m.sx, rows, torch.float32, (rows,)),
         "gate": view(m.gate, T, torch.float32, (T,)),
         "h": view(m.h, rows * I, torch.float32, (rows, I)),

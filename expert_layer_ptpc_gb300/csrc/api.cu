@@ -129,7 +129,7 @@ ForwardLayout forward_layout(const moe_dims& d) {
   L.s2f = take(R * 4);
   L.f2s = take(R * 4);
   L.perm = take(permute_ws_bytes(R, d.E));
-  L.xq = take((size_t)d.T * d.D);   // token order: the gate/up GEMM gathers
+  L.xq = take(rows * d.D);
   L.sx = take(rows * 4);
   L.gate = take((size_t)d.T * 4);
   L.h = take(rows * d.I * 4);
@@ -508,28 +508,26 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
                                   d.shared ? d.T : -1, at(L.perm), stream, pdl));
   if (st != MOE_OK) return st;
   mark(3);
-  // x -> FP8 codes, once per token (row t of xq), with the token's scale
-  // written to each of its k expert rows (and its shared-expert row R + t),
-  // plus the shared-expert gate.
+  // x -> FP8 codes written straight into each token's k expert rows (and its
+  // shared-expert row R + t), plus the shared-expert gate. (Writing each
+  // token's codes once and gathering them in the gate/up GEMM's producers
+  // with TMA tile::gather4 was measured 2.4x slower in that GEMM: four rows
+  // per copy instruction instead of 32 or 64.)
   if (pre != nullptr)   // r = x + residual, RMSNorm, then the same quantiser
     st = cuda_status(launch_add_rmsnorm_quant(
         x, pre->residual, pre->gamma, pre->eps, d.T, d.D, pre->residual_out, f2s,
         d.k, d.shared ? R : -1, xq, sx, d.shared ? shared_gate_w : nullptr,
-        d.shared ? gate : nullptr, stream, pdl, /*codes_once=*/true));
+        d.shared ? gate : nullptr, stream, pdl));
   else
     st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
                                   d.shared ? R : -1, xq, sx,
                                   d.shared ? shared_gate_w : nullptr,
-                                  d.shared ? gate : nullptr, stream, pdl, false,
-                                  /*codes_once=*/true));
+                                  d.shared ? gate : nullptr, stream, pdl, false));
   if (st != MOE_OK) return st;
   mark(4);
   const int hint = (int)std::max<int64_t>(1, R / d.E);
-  // the gate/up GEMM reads each expert row's token codes through the
-  // permutation (sorted row -> token), from the unpermuted codes
-  const TokenGather gather{s2f, d.k, (int)R, (int64_t)d.T};
   st = launch_grouped_gemm(MOE_GEMM_GATEUP_SWIGLU, xq, sx, rows, w_gu, s_gu,
-                           offsets, G, d.I, d.D, h, hint, stream, pdl, &gather);
+                           offsets, G, d.I, d.D, h, hint, stream, pdl);
   if (st != MOE_OK) return st;
   mark(5);
   st = cuda_status(launch_quant(h, MOE_DTYPE_F32, rows, d.I, nullptr, 1, -1, hq,

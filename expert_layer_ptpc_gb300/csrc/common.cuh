@@ -155,23 +155,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void* tmap,
       : "memory");
 }
 
-// Four rows r0..r3 of a 2D tensor map whose box is one row high, from inner
-// element x on, into four consecutive rows of shared memory at smem_dst
-// (each row one box wide, laid out and swizzled as rows of a 4-row box).
-// The gather form of the tiled load: a permutation's rows are read straight
-// from the unpermuted tensor.
-__device__ __forceinline__ void tma_gather4(uint32_t smem_dst, const void* tmap, int32_t x,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                            uint32_t bar, uint64_t cache_policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::"
-      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(
-          smem_dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(bar), "l"(cache_policy)
-      : "memory");
-}
-
 // 2D tiled store of a shared-memory box to global memory at (x, y); the
 // box's rows past the tensor's end are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y,

@@ -49,13 +49,6 @@ struct TileInfo {
   int group, ctile, row0, row_end;
 };
 
-using Gather = TokenGather;
-
-// Token (row of the unpermuted matrix) of sorted row r.
-__device__ __forceinline__ int gather_token(const Gather& g, int r) {
-  return r < g.R ? __ldg(g.s2f + r) / g.k : r - g.R;
-}
-
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* prefix,
                                                 int groups, const int32_t* offsets,
                                                 int bn) {

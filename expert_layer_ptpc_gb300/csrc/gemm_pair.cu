@@ -98,21 +98,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void* 
       : "memory");
 }
 
-// tma_gather4 into this CTA's shared memory, completion counted on an
-// mbarrier of either CTA of the pair (`bar` is a shared::cluster address).
-__device__ __forceinline__ void tma_gather4_pair(uint32_t smem_dst, const void* tmap,
-                                                 int32_t x, int32_t r0, int32_t r1,
-                                                 int32_t r2, int32_t r3, uint32_t bar,
-                                                 uint64_t cache_policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4."
-      "mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], "
-      "%8;" ::"r"(smem_dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(bar), "l"(cache_policy)
-      : "memory");
-}
-
 __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag,
                                                   unsigned* err, unsigned code) {
@@ -159,11 +144,8 @@ struct PairCfg {
   // 32 tokens (down) or x 16 tokens (gate/up, after the SwiGLU exchange)
   static constexpr int kOutRows = GATEUP ? 16 : 32;
   static constexpr int kOutBytes = 4 * kOutRows * 32 * 4;
-  // gathered token rows: each token-box producer's row indices for its tile
-  static constexpr int kGatherBytes = GATEUP ? kTBoxes * kTBoxRows * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
-                                    kGatherBytes + kNumBars * 8 + 16 +
-                                    4 * (kMaxGroups + 1) + 64;
+                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
   static_assert(kStages >= 3, "pipeline depth");
@@ -190,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
     __half* __restrict__ out16, float* __restrict__ row_scale,
-    const float* __restrict__ w_bound, Gather gather, unsigned* __restrict__ err) {
+    const float* __restrict__ w_bound, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
   using C = PairCfg<BN, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
@@ -198,10 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
   float* outstage = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kXBytes);
-  int* gtok = reinterpret_cast<int*>(smem + C::kStages * C::kStage + C::kXBytes +
-                                     C::kOutBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
-                                               C::kXBytes + C::kOutBytes + C::kGatherBytes);
+                                               C::kXBytes + C::kOutBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
@@ -292,11 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     if (rank == 0) tma_load_2d(dst, tm, x, y, full_bar(s), pol);
     else tma_load_2d_pair(dst, tm, x, y, map_to_rank(full_bar(s), 0), pol);
   };
-  auto load_gather4 = [&](uint32_t dst, const CUtensorMap* tm, int x, int4 r, int s,
-                          uint64_t pol) {
-    if (rank == 0) tma_gather4(dst, tm, x, r.x, r.y, r.z, r.w, full_bar(s), pol);
-    else tma_gather4_pair(dst, tm, x, r.x, r.y, r.z, r.w, map_to_rank(full_bar(s), 0), pol);
-  };
 
   const int box = producer_box(warp);
   if (warp == kSchedWarp) {
@@ -320,30 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
         else {               // 32 rows of this CTA's half of the token tile
           const int t = box - 2;
           const int half = pair_width<BN>(ti.row_end - ti.row0) / 2;
-          if (t * C::kTBoxRows < half) {
-            const uint32_t dst = stage_b(s) + t * C::kTBoxRows * kBK;
-            if (GATEUP && gather.s2f != nullptr) {
-              const int4* tk = reinterpret_cast<const int4*>(gtok + t * C::kTBoxRows);
-#pragma unroll
-              for (int j = 0; j < C::kTBoxRows / 4; ++j)
-                load_gather4(dst + j * 4 * kBK, &tm_a, x, tk[j], s, pol);
-            } else {
-              load(dst, &tm_a, x, ti.row0 + (int)rank * half + t * C::kTBoxRows, s, pol);
-            }
-          }
+          if (t * C::kTBoxRows < half)
+            load(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
+                 ti.row0 + (int)rank * half + t * C::kTBoxRows, s, pol);
         }
-      };
-      // gathered token rows of this box for tile ti (rows past the expert's
-      // end repeat its last row; the epilogue discards them)
-      auto gather_rows = [&](const TileInfo& ti) {
-        if (!GATEUP || weight_box || gather.s2f == nullptr) return;
-        const int t = box - 2;
-        const int half = pair_width<BN>(ti.row_end - ti.row0) / 2;
-        const int r0 = ti.row0 + (int)rank * half + t * C::kTBoxRows;
-        int* tk = gtok + t * C::kTBoxRows;
-#pragma unroll 4
-        for (int i = 0; i < C::kTBoxRows; ++i)
-          tk[i] = gather_token(gather, min(r0 + i, ti.row_end - 1));
       };
       // a token box past the tile's MMA width is not loaded by either CTA
       auto expect = [&](int s, const TileInfo& ti) {
@@ -383,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
         if (tile < 0) break;
         const bool pre = first && npre > 0 && tile == first_tile;
         const TileInfo ti = pre ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
-        gather_rows(ti);
         for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!wait_cluster_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                     kErrTimeoutProducer)) {
@@ -627,23 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   }
 }
 
-// With g.s2f set (gate/up only), A is the unpermuted [g.src_rows, K] token
-// matrix, read through the gather; a_rows still counts the sorted rows.
 template <int BN, bool GATEUP, bool OUT16 = false>
 int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
              const uint8_t* W, const float* w_scale, const int32_t* offsets,
              int groups, int N, int K, float* out, cudaStream_t stream, bool pdl,
              __half* out16 = nullptr, float* row_scale = nullptr,
-             const float* w_bound = nullptr, Gather g = {}) {
+             const float* w_bound = nullptr) {
   using C = PairCfg<BN, GATEUP>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
-  if (g.s2f != nullptr) {
-    if (!GATEUP || g.src_rows <= 0 || !make_tmap(&tm_a, A, g.src_rows, K, 1)) return -3;
-  } else if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) {
-    return -3;
-  }
+  if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
   CUtensorMap tm_out;
   const bool made = OUT16 ? make_tmap_out(&tm_out, out16, a_rows, N, C::kOutRows, 32, 2)
                           : make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, 32, 4);
@@ -673,7 +621,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
-                         groups, N, K, out, out16, row_scale, w_bound, g,
+                         groups, N, K, out, out16, row_scale, w_bound,
                          device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
@@ -688,15 +636,13 @@ int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
                              int64_t a_rows, const uint8_t* W,
                              const float* w_scale, const int32_t* offsets,
                              int groups, int N, int K, float* out, int bn,
-                             cudaStream_t stream, bool pdl, const TokenGather* gather) {
-  if (gather != nullptr && kind != 0) return -1;
-  const Gather g = gather != nullptr ? *gather : Gather{nullptr, 1, 0, 0};
+                             cudaStream_t stream, bool pdl) {
   if (kind == 0) {
     if (bn <= 128)
       return run_pair<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                 K, out, stream, pdl, nullptr, nullptr, nullptr, g);
+                                 K, out, stream, pdl);
     return run_pair<256, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
-                               out, stream, pdl, nullptr, nullptr, nullptr, g);
+                               out, stream, pdl);
   }
   if (bn <= 128)
     return run_pair<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,

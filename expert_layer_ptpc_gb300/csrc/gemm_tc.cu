@@ -86,11 +86,8 @@ struct Cfg {
   // output in shared memory and write it with one TMA store
   static constexpr bool kStagedOut = !kPacked && BN >= 64;
   static constexpr int kOutBytes = kStagedOut ? 4 * 32 * 32 * 4 : 0;
-  // gathered token rows: each token-box producer's row indices for its tile
-  static constexpr int kGatherBytes = GATEUP ? kTBoxes * kTBoxRows * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
-                                    kGatherBytes + kNumBars * 8 + 16 +
-                                    4 * (kMaxGroups + 1) + 64;
+                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(MINB == 1 || (MINB == 2 && 2 * (kSmemBytes + 1024) <= 233472 &&
                               2 * kTmemCols <= 512),
@@ -118,7 +115,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
     __half* __restrict__ out16, float* __restrict__ row_scale,
-    const float* __restrict__ w_bound, Gather gather, unsigned* __restrict__ err) {
+    const float* __restrict__ w_bound, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
   using C = Cfg<BN, BMW, GATEUP, OUT16, MINB>;
   extern __shared__ uint8_t smem_raw[];
@@ -126,10 +123,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
   float* outstage = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kXBytes);
-  int* gtok = reinterpret_cast<int*>(smem + C::kStages * C::kStage + C::kXBytes +
-                                     C::kOutBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
-                                               C::kXBytes + C::kOutBytes + C::kGatherBytes);
+                                               C::kXBytes + C::kOutBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
@@ -247,30 +242,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
           tma_load_2d(stage_a(s, 0) + off, &tm_w, x, row, full_bar(s), pol);
         } else {
           const int t = box - C::kWBoxes;
-          const uint32_t dst = stage_b(s) + t * C::kTBoxRows * kBK;
-          if (GATEUP && gather.s2f != nullptr) {
-            const int4* tk = reinterpret_cast<const int4*>(gtok + t * C::kTBoxRows);
-#pragma unroll
-            for (int j = 0; j < C::kTBoxRows / 4; ++j) {
-              const int4 r = tk[j];
-              tma_gather4(dst + j * 4 * kBK, &tm_a, x, r.x, r.y, r.z, r.w, full_bar(s),
-                          pol);
-            }
-          } else {
-            tma_load_2d(dst, &tm_a, x, ti.row0 + t * C::kTBoxRows, full_bar(s), pol);
-          }
+          tma_load_2d(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
+                      ti.row0 + t * C::kTBoxRows, full_bar(s), pol);
         }
-      };
-      // gathered token rows of this box for tile ti (rows past the expert's
-      // end repeat its last row; the epilogue discards them)
-      auto gather_rows = [&](const TileInfo& ti) {
-        if (!GATEUP || weight_box || gather.s2f == nullptr) return;
-        const int t = box - C::kWBoxes;
-        const int r0 = ti.row0 + t * C::kTBoxRows;
-        int* tk = gtok + t * C::kTBoxRows;
-#pragma unroll 4
-        for (int i = 0; i < C::kTBoxRows; ++i)
-          tk[i] = gather_token(gather, min(r0 + i, ti.row_end - 1));
       };
       int last_phase[C::kStages];
 #pragma unroll
@@ -306,7 +280,6 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
         if (tile < 0) break;
         const bool pre = first_tile && npre > 0 && tile == first;
         const TileInfo ti = pre ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
-        gather_rows(ti);
         for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                  kErrTimeoutProducer)) {
@@ -617,23 +590,16 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
 }
 
 // out (fp32) or, with OUT16, out16 + row_scale given w_bound (down only).
-// With g.s2f set (gate/up only), A is the unpermuted [src_rows, K] token
-// matrix, read through the gather; a_rows still counts the sorted rows.
 template <int BN, int BMW, bool GATEUP, bool OUT16 = false, int MINB = 1>
 int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W,
         const float* w_scale, const int32_t* offsets, int groups, int N, int K,
         float* out, cudaStream_t stream, bool pdl, __half* out16 = nullptr,
-        float* row_scale = nullptr, const float* w_bound = nullptr, Gather g = {},
-        int64_t src_rows = 0) {
+        float* row_scale = nullptr, const float* w_bound = nullptr) {
   using C = Cfg<BN, BMW, GATEUP, OUT16, MINB>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;
-  if (g.s2f != nullptr) {
-    if (!GATEUP || src_rows <= 0 || !make_tmap(&tm_a, A, src_rows, K, 1)) return -3;
-  } else if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) {
-    return -3;
-  }
+  if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
   CUtensorMap tm_out{};
   if (C::kStagedOut) {
     const bool made = OUT16 ? make_tmap_out(&tm_out, out16, a_rows, N, 32, 32, 2)
@@ -665,7 +631,7 @@ int run(const uint8_t* A, const float* a_scale, int64_t a_rows, const uint8_t* W
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
-                         groups, N, K, out, out16, row_scale, w_bound, g,
+                         groups, N, K, out, out16, row_scale, w_bound,
                          device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
@@ -753,10 +719,8 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         int64_t a_rows, const uint8_t* W, const float* w_scale,
                         const int32_t* offsets, int groups, int N, int K,
                         float* out, int rows_hint, cudaStream_t stream,
-                        bool pdl, const TokenGather* gather) {
+                        bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
-  if (gather != nullptr && kind != 0) return -1;
-  const Gather g = gather != nullptr ? *gather : Gather{nullptr, 1, 0, 0};
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
   // Wide token tiles of the gate/up projection run one M = 256 MMA over a
   // pair of SMs (each loads half of the token tile, one N = 256 instruction
@@ -771,23 +735,18 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   if (pair && grouped_gemm_pair_supported(kind, N))
     return launch_grouped_gemm_pair(kind, A, a_scale, a_rows, W, w_scale, offsets,
                                     groups, N, K, out, avg <= 128 ? 128 : 256,
-                                    stream, pdl, gather);
+                                    stream, pdl);
   if (kind == 0) {
-#define MOE_GATEUP(bn, bmw, minb)                                                        \
-  return run<bn, bmw, true, false, minb>(A, a_scale, a_rows, W, w_scale, offsets, groups, \
-                                         N, K, out, stream, pdl, nullptr, nullptr,       \
-                                         nullptr, g, g.src_rows)
     if (avg <= 16) {
       // fewer tiles than two per SM: two CTAs an SM, so no SM streams a
       // second tile alone after the others are done
       if (token_tiles_upper(a_rows, groups, 16) * (N / 64) <= 2 * (int64_t)sm_count())
-        MOE_GATEUP(16, 64, 2);
-      MOE_GATEUP(16, 64, 1);
+        return run<16, 64, true, false, 2>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+      return run<16, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
     }
-    if (avg <= 32) MOE_GATEUP(32, 64, 1);
-    if (avg <= 64) MOE_GATEUP(64, 128, 1);
-    MOE_GATEUP(128, 128, 1);
-#undef MOE_GATEUP
+    if (avg <= 32) return run<32, 64, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    if (avg <= 64) return run<64, 128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
+    return run<128, 128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);
   }
   // 16-token down tiles (short K, per-tile overhead) always run two CTAs an SM
   if (avg <= 16) return run<16, 128, false, false, 2>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K, out, stream, pdl);

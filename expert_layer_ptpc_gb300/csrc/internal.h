@@ -57,15 +57,13 @@ cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
 // Per-row e4m3 quantisation with scatter; `gate_w` non-null also computes
 // gate_out[r] = sigmoid(in[r] . gate_w) (bf16 input only). `release_early`
 // lets the next kernel launch before this one's dependency wait (see
-// quant.cu for when that is safe). `codes_once`: the codes of row r go to
-// out_q row r only (the gather of the gate/up GEMM reads them there), the
-// scale to every destination row.
+// quant.cu for when that is safe).
 cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          const int32_t* dst_rows, int copies,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
                          float* gate_out, cudaStream_t stream, bool pdl,
-                         bool release_early, bool codes_once = false);
+                         bool release_early);
 
 // Add + RMSNorm + per-token quantisation (see quant.cu); same destinations
 // and limits as launch_quant.
@@ -75,8 +73,7 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
                                      const int32_t* dst_rows, int copies,
                                      int64_t extra_row_base, uint8_t* out_q,
                                      float* out_scale, const uint16_t* gate_w,
-                                     float* gate_out, cudaStream_t stream, bool pdl,
-                                     bool codes_once = false);
+                                     float* gate_out, cudaStream_t stream, bool pdl);
 
 // Router projection (tcgen05, bf16) with the top-k selection and softmax in
 // its epilogue (router_gemm.cu). Returns a moe_status.
@@ -102,26 +99,12 @@ constexpr int kMaxQuantCols = 32768;
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* w_g, int T,
                                int D, float* gate, cudaStream_t stream);
 
-// Token operand of the gate/up GEMM read through a gather: sorted row r
-// (expert-contiguous, from the permutation) holds token s2f[r] / k for the
-// routed rows r < R and token r - R for the shared expert's rows after them.
-// The GEMM then reads each token's FP8 codes from the unpermuted
-// [src_rows = T, K] matrix, and no k-fold copy of them is written.
-// s2f == nullptr: the operand is already in sorted order.
-struct TokenGather {
-  const int32_t* s2f;
-  int k;
-  int R;
-  int64_t src_rows;
-};
-
-// Returns a moe_status. `gather` (gate/up only; nullable): A is the
-// unpermuted token matrix, read through the gather.
+// Returns a moe_status.
 int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         int64_t a_rows, const uint8_t* W, const float* w_scale,
                         const int32_t* offsets, int groups, int N, int K,
                         float* out, int rows_hint, cudaStream_t stream,
-                        bool pdl, const TokenGather* gather = nullptr);
+                        bool pdl);
 
 // The CTA-pair (cta_group::2) grouped GEMM for wide token tiles (bn 128 or
 // 256); needs N divisible by 128 (gate/up) or 256 (down). Returns a status.
@@ -130,8 +113,7 @@ int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
                              int64_t a_rows, const uint8_t* W,
                              const float* w_scale, const int32_t* offsets,
                              int groups, int N, int K, float* out, int bn,
-                             cudaStream_t stream, bool pdl,
-                             const TokenGather* gather = nullptr);
+                             cudaStream_t stream, bool pdl);
 
 cudaError_t launch_combine(const float* y, const int32_t* f2s,
                            const float* topk_w, int T, int k, int D,

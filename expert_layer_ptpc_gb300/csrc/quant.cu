@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
     const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
     uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
     const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out,
-    int release_early, int codes_once) {
+    int release_early) {
   __shared__ float red_max[kMaxThreads / 32];
   __shared__ float red_dot[kMaxThreads / 32];
   __shared__ int64_t dst[kMaxTopK + 1];
@@ -132,11 +132,8 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
         w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
       }
       const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
-      if (codes_once)   // codes once, in the row's own place
-        *reinterpret_cast<uint4*>(out_q + r * cols + u * kVec) = packed;
-      else
-        for (int d = 0; d < ndst; ++d)
-          *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
+      for (int d = 0; d < ndst; ++d)
+        *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
     }
   }
 }
@@ -153,7 +150,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_warp_kernel(
     const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
     uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
     const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out,
-    int release_early, int codes_once) {
+    int release_early) {
   if (release_early) pdl_launch_dependents();
   pdl_wait();
   if (!release_early) pdl_launch_dependents();
@@ -212,10 +209,6 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_warp_kernel(
       }
       packed = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    if (codes_once) {   // codes once, in the row's own place
-      if (u < nunits) *reinterpret_cast<uint4*>(out_q + r * cols + u * kVec) = packed;
-      continue;
-    }
     // every lane takes part in the shuffles; only lanes with a unit store
     for (int d = 0; d < ndst; ++d) {
       const int64_t dd = __shfl_sync(0xffffffffu, my_dst, d);
@@ -253,7 +246,7 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
     __nv_bfloat16* res_out, const int32_t* __restrict__ dst_rows,
     int copies, int64_t extra_row_base, uint8_t* __restrict__ out_q,
     float* __restrict__ out_scale, const __nv_bfloat16* __restrict__ gate_w,
-    float* __restrict__ gate_out, int sbits, int codes_once) {
+    float* __restrict__ gate_out, int sbits) {
   __shared__ unsigned long long red_sq[kMaxThreads / 32];
   __shared__ int red_e[kMaxThreads / 32];
   __shared__ float red_max[kMaxThreads / 32];
@@ -392,11 +385,8 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
         w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
       }
       const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
-      if (codes_once)   // codes once, in the row's own place
-        *reinterpret_cast<uint4*>(out_q + r * cols + u * kVec) = packed;
-      else
-        for (int d = 0; d < ndst; ++d)
-          *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
+      for (int d = 0; d < ndst; ++d)
+        *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
     }
   }
 }
@@ -426,7 +416,7 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
                         int64_t extra_row_base, uint8_t* out_q,
                         float* out_scale, const __nv_bfloat16* gate_w,
                         float* gate_out, cudaStream_t stream, bool pdl,
-                        bool release_early, bool codes_once) {
+                        bool release_early) {
   const int nunits = cols / kVec;
   const int ndst = (dst_rows != nullptr ? copies : 1) + (extra_row_base >= 0 ? 1 : 0);
   if (nunits <= 64 && ndst <= 32) {
@@ -434,8 +424,7 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
     auto go = [&](auto kern) {
       return launch_kernel(pdl, grid, dim3(kWarpsPerBlock * 32), 0, stream, kern, in,
                            rows, cols, dst_rows, copies, extra_row_base, out_q,
-                           out_scale, gate_w, gate_out, release_early ? 1 : 0,
-                           codes_once ? 1 : 0);
+                           out_scale, gate_w, gate_out, release_early ? 1 : 0);
     };
     if (nunits <= 32) return go(quant_rows_warp_kernel<InT, 1>);
     return go(quant_rows_warp_kernel<InT, 2>);
@@ -446,7 +435,7 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
   auto go = [&](auto kern) {
     return launch_kernel(pdl, grid, block, 0, stream, kern, in, rows, cols,
                          dst_rows, copies, extra_row_base, out_q, out_scale,
-                         gate_w, gate_out, release_early ? 1 : 0, codes_once ? 1 : 0);
+                         gate_w, gate_out, release_early ? 1 : 0);
   };
   if (units <= 1) return go(quant_rows_kernel<InT, 1>);
   if (units <= 2) return go(quant_rows_kernel<InT, 2>);
@@ -460,17 +449,17 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
                          float* gate_out, cudaStream_t stream, bool pdl,
-                         bool release_early, bool codes_once) {
+                         bool release_early) {
   if (rows == 0) return cudaSuccess;
   if (in_dtype == 0)
     return launch_rows(static_cast<const __nv_bfloat16*>(in), rows, cols,
                        dst_rows, copies, extra_row_base, out_q, out_scale,
                        reinterpret_cast<const __nv_bfloat16*>(gate_w), gate_out,
-                       stream, pdl, release_early, codes_once);
+                       stream, pdl, release_early);
   return launch_rows(static_cast<const float*>(in), rows, cols, dst_rows, copies,
                      extra_row_base, out_q, out_scale,
                      (const __nv_bfloat16*)nullptr, (float*)nullptr, stream, pdl,
-                     release_early, codes_once);
+                     release_early);
 }
 
 cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
@@ -479,8 +468,7 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
                                      const int32_t* dst_rows, int copies,
                                      int64_t extra_row_base, uint8_t* out_q,
                                      float* out_scale, const uint16_t* gate_w,
-                                     float* gate_out, cudaStream_t stream, bool pdl,
-                                     bool codes_once) {
+                                     float* gate_out, cudaStream_t stream, bool pdl) {
   if (rows == 0) return cudaSuccess;
   const int nunits = cols / kVec;
   const int threads = std::min(kMaxThreads, ((nunits + 31) / 32) * 32);
@@ -496,7 +484,7 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
     return launch_kernel(pdl, grid, block, 0, stream, kern, bf(x), bf(res), bf(gamma),
                          eps, cols, reinterpret_cast<__nv_bfloat16*>(res_out),
                          dst_rows, copies, extra_row_base, out_q, out_scale,
-                         bf(gate_w), gate_out, sbits, codes_once ? 1 : 0);
+                         bf(gate_w), gate_out, sbits);
   };
   if (units <= 1) return go(add_rmsnorm_quant_kernel<1>);
   if (units <= 2) return go(add_rmsnorm_quant_kernel<2>);

@@ -360,9 +360,8 @@ MOE_API int moe_forward(const moe_dims* dims, const uint16_t* x,
  *   topk_ids, topk_w [T, k]: the routing (valid only when the forward was not
  *     given topk_ids_out / topk_w_out, which then received it);
  *   expert_offsets [G + 1], sorted_to_flat [R], flat_to_sorted [R];
- *   xq [T, D] e4m3: each token's codes once, in token order (the gate/up GEMM
- *     reads them through the permutation); sx [rows] fp32: the token's scale
- *     at each of its sorted rows; gate [T] fp32: the shared expert's gate;
+ *   xq [rows, D] e4m3 and sx [rows] fp32: the token's codes and scale at each
+ *     of its sorted rows; gate [T] fp32: the shared expert's gate;
  *   h [rows, I] fp32: SwiGLU output of the gate/up GEMM; hq [rows, I] e4m3 and
  *     sh [rows] fp32: its per-row requantisation;
  *   y: the down GEMM's output, fp32 [rows, D] when y_fp16 == 0, else fp16 codes

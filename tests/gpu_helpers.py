@@ -155,7 +155,7 @@ def staged_layer_check(cfg, xv, out_tokens, ids, w, inter, tokens, qmap, w_g):
     """Stage-by-stage parity of one forward on the sampled `tokens`, read
     from the forward's own intermediates (moe_forward_intermediates):
 
-    * x codes (token order) and each row's scale: bit-exact against the
+    * x codes and scale at each of the sample's rows: bit-exact against the
       oracle's quantiser on the layer input xv;
     * h of every row of the sample: within the fp32 GEMM + SwiGLU bound of
       the oracle's exact h;
@@ -186,12 +186,11 @@ def staged_layer_check(cfg, xv, out_tokens, ids, w, inter, tokens, qmap, w_g):
         flat_exp = np.concatenate([flat_exp, np.full(n, E)])
         flat_tok = np.concatenate([flat_tok, np.arange(n)])
     dev_rows = torch.as_tensor(flat_rows, device=inter["h"].device)
-    dev_tok = torch.as_tensor(tokens, device=inter["h"].device)
     h_g = inter["h"].index_select(0, dev_rows).cpu().numpy()
     hq_g = inter["hq"].index_select(0, dev_rows).cpu().numpy()
     sh_g = inter["sh"].index_select(0, dev_rows).cpu().numpy()
     sx_g = inter["sx"].index_select(0, dev_rows).cpu().numpy()
-    xq_g = inter["xq"].index_select(0, dev_tok).cpu().numpy()
+    xq_g = inter["xq"].index_select(0, dev_rows).cpu().numpy()
     y_g = inter["y"].index_select(0, dev_rows).double()
     if inter["y_fp16"]:
         rs = inter["y_row_scale"].index_select(0, dev_rows).double()
@@ -200,7 +199,7 @@ def staged_layer_check(cfg, xv, out_tokens, ids, w, inter, tokens, qmap, w_g):
     y_g = y_g.cpu().numpy()
 
     xq_o, sx_o = oracle.quant_rows_ref(np.asarray(xv, np.float32)[tokens])
-    assert np.array_equal(xq_g, xq_o), "x codes differ"
+    assert np.array_equal(xq_g, xq_o[flat_tok]), "x codes differ"
     assert np.array_equal(sx_g.view(np.uint32), sx_o[flat_tok].view(np.uint32)), \
         "x scales differ"
 

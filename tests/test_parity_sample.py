@@ -62,7 +62,7 @@ def test_bf16_half_ulp_bounds_the_rounding(rng):
 
 def _oracle_intermediates(cfg, x, ids, qmap, wg):
     """A forward's intermediates as the oracle computes them, laid out like
-    the library's workspace (token-order x codes; sorted rows for the rest)."""
+    the library's workspace (rows in sorted, expert-contiguous order)."""
     import torch
     T, D, E, k, I = cfg.T, cfg.D, cfg.E, cfg.k, cfg.I
     R = T * k
@@ -81,7 +81,8 @@ def _oracle_intermediates(cfg, x, ids, qmap, wg):
         r = oracle.expert_ffn_ref(xq[srow_tok[sel]], sx[srow_tok[sel]], *qmap[int(e)])
         h[sel], hq[sel], sh[sel], y[sel] = r["h32"], r["hq"], r["sh"], r["y"]
     t = torch.from_numpy
-    return {"flat_to_sorted": t(f2s.astype(np.int32)), "xq": t(xq), "sx": t(sx[srow_tok]),
+    return {"flat_to_sorted": t(f2s.astype(np.int32)), "xq": t(xq[srow_tok]),
+            "sx": t(sx[srow_tok]),
             "h": t(h), "hq": t(hq), "sh": t(sh), "y": t(y.astype(np.float32)),
             "y_fp16": False}
 
