@@ -70,6 +70,7 @@ _SIGNATURES = {
     "moe_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "moe_workspace_status": (_I, [_P, _SZ, _P, ctypes.POINTER(ctypes.c_uint)]),
     "moe_forward_intermediates": (_I, [_P, _P, _SZ, _P]),
+    "moe_forward_workspace_layout": (_I, [_P, _P, _P, _I]),
     "moe_debug_expire_wait": (_I, [_I, _P, _SZ, _P]),
     "moe_router_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_add_rmsnorm_quant": (_I, [_P, _P, _P, ctypes.c_float, _I64, _I, _P, _P, _I,
@@ -332,6 +333,19 @@ def make_dims(T, D, E, k, I, shared, renormalize=True):
 
 def moe_forward_workspace_size(dims):
     return load_library().moe_forward_workspace_size(ctypes.byref(dims))
+
+
+def moe_forward_workspace_layout(dims):
+    """[(offset, size)] of the forward workspace's sub-buffers for dims; each
+    is followed by a guard band of at least 256 bytes that no kernel writes."""
+    lib = load_library()
+    n = lib.moe_forward_workspace_layout(ctypes.byref(dims), None, None, 0)
+    if n < 0:
+        raise MoeError("moe_forward_workspace_layout", n)
+    offs = (ctypes.c_size_t * n)()
+    sizes = (ctypes.c_size_t * n)()
+    lib.moe_forward_workspace_layout(ctypes.byref(dims), offs, sizes, n)
+    return list(zip(offs, sizes))
 
 
 class Intermediates(ctypes.Structure):

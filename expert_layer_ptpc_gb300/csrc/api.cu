@@ -95,6 +95,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // first kForwardStatusBytes hold the forward's error word and the slot its
 // read-and-clear copies from (moe_workspace_status).
 constexpr size_t kForwardStatusBytes = 256;
+constexpr size_t kGuardBytes = 256;
 
 struct ForwardLayout {
   size_t status, ids, w, logits, counts, offsets, s2f, f2s, perm, xq, sx, gate, h,
@@ -115,9 +116,13 @@ ForwardLayout forward_layout(const moe_dims& d) {
   const int64_t G = (int64_t)d.E + (d.shared ? 1 : 0);
   ForwardLayout L{};
   size_t off = 0;
+  // every sub-buffer is followed by at least kGuardBytes that no kernel
+  // writes: a guard band, so that a test can fill the workspace with a
+  // pattern and find any write past a buffer's end (compute-sanitizer is not
+  // available to catch it)
   auto take = [&](size_t bytes) {
     const size_t o = off;
-    off = align256(off + bytes);
+    off = align256(off + bytes + kGuardBytes);
     return o;
   };
   L.status = take(kForwardStatusBytes);
@@ -371,6 +376,32 @@ int moe_combine(const float* y, const int32_t* flat_to_sorted,
 size_t moe_forward_workspace_size(const moe_dims* dims) {
   if (check_dims(dims) != MOE_OK) return 0;
   return forward_layout(*dims).total;
+}
+
+int moe_forward_workspace_layout(const moe_dims* dims, size_t* offsets, size_t* sizes,
+                                 int max_entries) {
+  if (check_dims(dims) != MOE_OK) return MOE_ERR_INVALID_ARG;
+  const ForwardLayout L = forward_layout(*dims);
+  const moe_dims& d = *dims;
+  const int64_t R = (int64_t)d.T * d.k;
+  const int64_t rows = R + (d.shared ? d.T : 0);
+  const int64_t G = (int64_t)d.E + (d.shared ? 1 : 0);
+  const size_t off[] = {L.status, L.ids, L.w, L.logits, L.counts, L.offsets, L.s2f,
+                        L.f2s, L.perm, L.xq, L.sx, L.gate, L.h, L.hq, L.sh, L.y,
+                        L.row_scale, L.w_bound};
+  const size_t size[] = {kForwardStatusBytes, (size_t)R * 4, (size_t)R * 4,
+                         (size_t)d.T * d.E * 4, (size_t)G * 4, (size_t)(G + 1) * 4,
+                         (size_t)R * 4, (size_t)R * 4, permute_ws_bytes(R, d.E),
+                         (size_t)rows * d.D, (size_t)rows * 4, (size_t)d.T * 4,
+                         (size_t)rows * d.I * 4, (size_t)rows * d.I, (size_t)rows * 4,
+                         (size_t)rows * d.D * 4, (size_t)rows * 4, (size_t)G * 4};
+  const int n = (int)(sizeof(off) / sizeof(off[0]));
+  if (offsets != nullptr && sizes != nullptr)
+    for (int i = 0; i < n && i < max_entries; ++i) {
+      offsets[i] = off[i];
+      sizes[i] = size[i];
+    }
+  return n;
 }
 
 int moe_forward_intermediates(const moe_dims* dims, void* ws, size_t ws_bytes,

@@ -356,5 +356,9 @@ int sm_count();
 // disables it, unset (-1) leaves the choice to the dispatch rule.
 int cta_pair_mode();
 
+// MOE_GEMM_DOWN_PAIR: the same switch for the down projection alone (its
+// fp16-output form); unset (-1) follows MOE_GEMM_CTA_PAIR, then the rule.
+int down_pair_mode();
+
 }  // namespace gemm
 }  // namespace moe

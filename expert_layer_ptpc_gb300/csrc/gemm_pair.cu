@@ -121,7 +121,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int BN, bool GATEUP>
+template <int BN, bool GATEUP, bool OUT16 = false>
 struct PairCfg {
   static constexpr int kHalfB = BN / 2;                  // token rows per CTA
   // TMA boxes of one stage (per CTA): two 64-row weight boxes, then 32-row
@@ -149,6 +149,13 @@ struct PairCfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
   static_assert(kStages >= 3, "pipeline depth");
+  // fp16 down output: four more epilogue warps (12-15, the same TMEM lane
+  // quarters) take every other 32-token chunk. A down tile's K is short
+  // (K = I), and four warps drained 128 channels x 256 tokens slower than
+  // the MMAs filled them. Their fp16 boxes fit the same staging bytes.
+  static constexpr bool kWideEpi = !GATEUP && OUT16;
+  static constexpr int kEpiSets = kWideEpi ? 2 : 1;
+  static constexpr int kThreadsT = kThreads + (kWideEpi ? 4 * 32 : 0);
 };
 
 // MMA width (token columns) of a tile with `nvalid` token rows: BN, halved
@@ -165,7 +172,8 @@ __device__ __forceinline__ int pair_width(int nvalid) {
 // OUT16 (down projection only): y as fp16 codes plus one factor per row, the
 // encoding of the single-CTA kernel (gemm_tc.cu, fp16_rho).
 template <int BN, bool GATEUP, bool OUT16>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
+__global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
+    grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ a_scale,
@@ -174,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     __half* __restrict__ out16, float* __restrict__ row_scale,
     const float* __restrict__ w_bound, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
-  using C = PairCfg<BN, GATEUP>;
+  using C = PairCfg<BN, GATEUP, OUT16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
-  __shared__ int warp_tot[kThreads / 32 + 1];
+  __shared__ int warp_tot[C::kThreadsT / 32 + 1];
   __shared__ Sched sched;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -214,13 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 8);     // one per epilogue warp of both CTAs (leader)
+      mbar_init(acce_bar(b), 8 * C::kEpiSets);   // each epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     mbar_init(xfull_bar, 4);       // one per epilogue warp
     mbar_init(xempty_bar, 4);
     // ring consumers: each producer, each epilogue warp, the leader's MMA issuer
-    sched_init(sched, C::kBoxes + 4 + (rank == 0 ? 1 : 0));
+    sched_init(sched, C::kBoxes + 4 * C::kEpiSets + (rank == 0 ? 1 : 0));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   if (warp == kMmaWarp) tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
 
   {   // tile prefix: prefix[g] = sum_{g' < g} ceil(rows_g' / BN) * n_ctiles
-    const int per = (groups + kThreads - 1) / kThreads;
+    const int per = (groups + C::kThreadsT - 1) / C::kThreadsT;
     const int g0 = threadIdx.x * per;
     int local = 0;
     for (int g = g0; g < g0 + per && g < groups; ++g)
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       prefix[g] = run;
       run += ((offsets[g + 1] - offsets[g] + BN - 1) / BN) * n_ctiles;
     }
-    if (threadIdx.x == kThreads - 1) prefix[groups] = base + incl;
+    if (threadIdx.x == C::kThreadsT - 1) prefix[groups] = base + incl;
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -432,7 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     // channels ch0 + lane (v[j] = token r0 + j). A box inside the expert goes
     // through shared memory and one TMA store; a box crossing the expert's end
     // is stored directly, so rows of the next expert are never written.
-    float* obuf = outstage + (warp - kEpiWarp0) * C::kOutRows * 32;
+    // epilogue warp index e = 0..3 (warps 1-4), 4..7 (12-15)
+    const int e_idx = warp < kSchedWarp ? warp - kEpiWarp0 : warp - kSchedWarp + 3;
+    const int eset = warp < kSchedWarp ? 0 : 1;
+    float* obuf = OUT16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(outstage) +
+                                                   e_idx * C::kOutRows * 32)
+                        : outstage + e_idx * C::kOutRows * 32;
     auto emit = [&](int r0, int row_end, int ch0, const float* v) {
       if (r0 + C::kOutRows <= row_end) {
         if (lane == 0) bulk_wait_read_all();
@@ -539,11 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
           const float rho = fp16_rho(w_bound[ti.group], K);
           swr = sw * rho;
           if (ti.ctile == 0 && rank == 0) {   // one factor per row
-            for (int r = (warp - kEpiWarp0) * 32 + lane; r < nvalid; r += 128)
+            for (int r = e_idx * 32 + lane; r < nvalid; r += 128 * C::kEpiSets)
               row_scale[ti.row0 + r] = __fdiv_rn(a_scale[ti.row0 + r], rho);
           }
         }
-        for (int n0 = 0; n0 < nvalid; n0 += 32) {
+        for (int n0 = 32 * eset; n0 < nvalid; n0 += 32 * C::kEpiSets) {
           float acc[32];
           tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
           tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
@@ -587,7 +600,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
              int groups, int N, int K, float* out, cudaStream_t stream, bool pdl,
              __half* out16 = nullptr, float* row_scale = nullptr,
              const float* w_bound = nullptr) {
-  using C = PairCfg<BN, GATEUP>;
+  using C = PairCfg<BN, GATEUP, OUT16>;
   CUtensorMap tm_w, tm_a;
   const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
   if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
@@ -614,7 +627,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * upper));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreadsT);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -224,21 +224,25 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
                                        : l2_policy_evict_normal();
       const uint32_t bytes =
           weight_box ? 64u * kBK : (uint32_t)(C::kTBoxRows * kBK);
+      // weight row of this producer's box in tile ti, and its stage offset
+      auto box_row = [&](const TileInfo& ti, int& off) {
+        const int wrow = weight_row(ti);
+        if (GATEUP && !C::kPacked) {   // boxes 0,1: gate halves; 2,3: up halves
+          off = (box >= 2 ? C::kATile : 0) + (box & 1) * 64 * kBK;
+          return wrow + (box >= 2 ? N : 0) + (box & 1) * 64;
+        } else if (GATEUP) {           // packed: 64 gate rows, 64 up rows
+          off = box * 64 * kBK;
+          return wrow + (box == 1 ? N : 0);
+        }
+        // down: 64-row quarters (halves) of the tile
+        off = (box >> 1) * C::kATile + (box & 1) * 64 * kBK;
+        return wrow + box * 64;
+      };
       auto issue = [&](int s, int kb, const TileInfo& ti) {
         const int x = kb * kBK;
         if (weight_box) {
-          const int wrow = weight_row(ti);
-          int row, off;   // weight row of the box and its offset in the stage
-          if (GATEUP && !C::kPacked) {   // boxes 0,1: gate halves; 2,3: up halves
-            row = wrow + (box >= 2 ? N : 0) + (box & 1) * 64;
-            off = (box >= 2 ? C::kATile : 0) + (box & 1) * 64 * kBK;
-          } else if (GATEUP) {           // packed: 64 gate rows, 64 up rows
-            row = wrow + (box == 1 ? N : 0);
-            off = box * 64 * kBK;
-          } else {                       // down: 64-row quarters (halves) of the tile
-            row = wrow + box * 64;
-            off = (box >> 1) * C::kATile + (box & 1) * 64 * kBK;
-          }
+          int off;
+          const int row = box_row(ti, off);
           tma_load_2d(stage_a(s, 0) + off, &tm_w, x, row, full_bar(s), pol);
         } else {
           const int t = box - C::kWBoxes;
@@ -713,6 +717,15 @@ int cta_pair_mode() {
   return mode;
 }
 
+int down_pair_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("MOE_GEMM_DOWN_PAIR");
+    if (v == nullptr || v[0] == '\0') return -1;
+    return v[0] == '1' ? 1 : v[0] == '0' ? 0 : -1;
+  }();
+  return mode;
+}
+
 }  // namespace gemm
 
 int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
@@ -767,8 +780,16 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
                                  cudaStream_t stream, bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
-  // single-CTA kernel unless MOE_GEMM_CTA_PAIR=1 forces the pair
-  if (cta_pair_mode() == 1 && avg > 64 && grouped_gemm_pair_supported(1, N))
+  // From 512 rows per expert on, 256-token tiles run on a CTA pair: one
+  // M = 256 MMA of 256 channels per K step, each SM loading 128 weight rows
+  // and half of the token tile (prefill 0.399 -> 0.387 ms). With fewer rows
+  // per expert the pair's narrowed tail tiles cost more than the feed it
+  // saves (T=16384: 0.97 -> 1.08 ms, T=4096 at 128-token tiles: 0.38 ->
+  // 0.61 ms). MOE_GEMM_DOWN_PAIR=1 / =0 (or MOE_GEMM_CTA_PAIR=1 / =0) forces
+  // the pair (above 64 rows per expert) or the single CTA.
+  const int dm = down_pair_mode() >= 0 ? down_pair_mode() : cta_pair_mode();
+  const bool pair = dm == 1 ? avg > 64 : dm == 0 ? false : avg >= 512;
+  if (pair && grouped_gemm_pair_supported(1, N))
     return launch_grouped_gemm_pair_down_f16(A, a_scale, a_rows, W, w_scale, w_bound,
                                              offsets, groups, N, K, y16, row_scale,
                                              avg <= 128 ? 128 : 256, stream, pdl);

@@ -21,7 +21,9 @@
 // is only a stand-in, not a device address. The first call on each device,
 // with that device current, looks up the array's device address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
-// capture on the device.
+// capture on the device. The cache lives as long as the process: after a
+// cudaDeviceReset the module is loaded again at another address, and this
+// entry point must not be used on that device any more.
 #include <mutex>
 
 #include "../../include/moe_ptpc.h"

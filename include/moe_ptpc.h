@@ -143,7 +143,11 @@ MOE_API int moe_permute(const int32_t* topk_ids, int T, int E, int k,
  *   E = 128: 4,194,304; for E = 1024: 524,288). Larger calls return
  *   MOE_ERR_UNSUPPORTED before launching anything.
  *   The first call on each device (with that device current) looks up the
- *   array's device address; make it before any stream capture on the device.
+ *   array's device address and caches it for the life of the process; make
+ *   it before any stream capture on the device. cudaDeviceReset (or anything
+ *   else that tears down the device's context and reloads the library's
+ *   module) invalidates that cached address: do not call this entry point on
+ *   a device after resetting it.
  *   All calls share the array and it keeps the last call's contents (nothing
  *   in it needs to start at zero): calls whose kernels overlap on the GPU race
  *   on it, so the caller must serialise them. Allocates nothing.
@@ -389,6 +393,18 @@ typedef struct moe_intermediates {
 
 MOE_API int moe_forward_intermediates(const moe_dims* dims, void* ws, size_t ws_bytes,
                                       moe_intermediates* out);
+
+/*
+ * moe_forward_workspace_layout - the sub-buffers of the forward workspace for
+ * `dims`: writes the byte offset and size of each (up to max_entries; host
+ * arrays, both non-NULL, or both NULL to only count) and returns their
+ * number (a negative status for bad dims). Every sub-buffer is followed by
+ * at least 256 bytes that no kernel writes (a guard band: a test fills the
+ * workspace with a pattern and checks the bands after a forward).
+ * No counterpart in the pages (inspection support).
+ */
+MOE_API int moe_forward_workspace_layout(const moe_dims* dims, size_t* offsets,
+                                         size_t* sizes, int max_entries);
 
 /*
  * moe_forward_profiled - moe_forward with timing marks: identical work and

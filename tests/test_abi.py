@@ -114,3 +114,19 @@ def test_permute_workspace_size(lib):
     # one int histogram row per chunk of 2048 flat entries (ragged last chunk)
     assert lib.moe_permute_workspace_size(8192, 128, 8) == 32 * 128 * 4
     assert lib.moe_permute_workspace_size(1025, 128, 8) == 5 * 128 * 4
+
+
+@pytest.mark.parametrize("dims_args", [(64, 256, 8, 2, 128, 0), (1000, 1024, 16, 8, 256, 1),
+                                       (16384, 4096, 512, 10, 1024, 1), (1, 128, 1, 1, 128, 0)])
+def test_workspace_layout_has_guard_bands(lib, dims_args):
+    """Sub-buffers of the forward workspace are disjoint, in order, 256-byte
+    aligned, each followed by at least 256 guard bytes, inside the size
+    moe_forward_workspace_size reports."""
+    from expert_layer_ptpc_gb300 import binding
+    d = binding.make_dims(*dims_args)
+    lay = binding.moe_forward_workspace_layout(d)
+    total = lib.moe_forward_workspace_size(ctypes.byref(d))
+    assert len(lay) >= 10
+    ends = [o for o, _ in lay[1:]] + [total]
+    for (o, n), nxt in zip(lay, ends):
+        assert o % 256 == 0 and o + n + 256 <= nxt, (o, n, nxt)

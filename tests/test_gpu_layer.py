@@ -330,3 +330,36 @@ def test_empty_batch_is_noop():
     out = run.layer.forward(x, lg)
     assert out.shape == (0, 256)
     assert cfg.T == 0
+
+
+@pytest.mark.parametrize("cfg", [
+    syn.LayerConfig("g1", 300, 512, 16, 4, 256, True, "normal"),
+    syn.LayerConfig("g2", 1024, 1024, 16, 8, 256, True, "normal"),    # fp16 y, CTA pairs
+    syn.LayerConfig("g3", 40, 256, 12, 2, 128, True, "weights"),      # exact router GEMM
+    syn.LayerConfig("g4", 256, 1024, 16, 4, 256, False, "weights"),   # fused router
+    syn.LayerConfig("g5", 9000, 256, 8, 2, 128, False, "normal"),     # multi-block permute
+], ids=lambda c: c.name)
+def test_forward_leaves_guard_bands_intact(cfg):
+    """Canaries in place of a memory checker: the forward workspace is filled
+    with a pattern, the forward runs, and the guard band behind every
+    sub-buffer (moe_forward_workspace_layout) still holds the pattern, so no
+    kernel wrote past the end of a buffer it owns. The output tensor's
+    neighbours are checked the same way."""
+    from expert_layer_ptpc_gb300 import binding
+    run = _Run(cfg)
+    x, logits = run.inputs(cfg)
+    L = run.layer
+    dims = L.dims(cfg.T)
+    ws = L.workspace(cfg.T)
+    ws.fill_(0xA5)
+    pad = 4096
+    big = torch.full((cfg.T * cfg.D + 2 * pad,), 0x5A5A, dtype=torch.int16, device="cuda")
+    out = big[pad:pad + cfg.T * cfg.D].view(torch.bfloat16).view(cfg.T, cfg.D)
+    L.forward(x, logits, out=out)
+    assert L.status() == (0, 0)
+    host = ws.cpu().numpy()
+    for off, n in binding.moe_forward_workspace_layout(dims):
+        band = host[off + n:off + n + 256]
+        assert np.all(band == 0xA5), (cfg.name, off, n, np.flatnonzero(band != 0xA5)[:4])
+    b = big.cpu().numpy()
+    assert np.all(b[:pad] == 0x5A5A) and np.all(b[pad + cfg.T * cfg.D:] == 0x5A5A)
