@@ -800,7 +800,9 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
   if (avg <= 16) MOE_DOWN16(16, 2);
   if (avg <= 32) MOE_DOWN16(32, 1);
   if (avg <= 64) MOE_DOWN16(64, 1);
-  if (avg <= 128 && N % 256 == 0)
+  // 128 tokens x 256 channels up to 384 rows per expert: at 320 (T=16384,
+  // 512 experts, top-10) they beat 256 x 128 tiles, 0.970 -> 0.934 ms
+  if (avg <= 384 && N % 256 == 0)
     return run<128, 256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
                                       nullptr, stream, pdl, o, row_scale, w_bound);
   if (avg <= 128) MOE_DOWN16(128, 1);
