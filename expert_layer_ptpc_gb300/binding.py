@@ -90,10 +90,11 @@ _lib = None
 
 
 def load_library(path=None):
-    """Load (once) and return the ctypes handle of the library."""
+    """Load (once) and return the ctypes handle of the library: the checked
+    variant (libmoe_ptpc_check.so) when MOE_LIBRARY_VARIANT=check."""
     global _lib
     if _lib is None:
-        path = path or _build.library_path()
+        path = path or _build.library_path(os.environ.get("MOE_LIBRARY_VARIANT", ""))
         if not os.path.exists(path):
             raise RuntimeError(
                 f"{path} is missing: build it with "

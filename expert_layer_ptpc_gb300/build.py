@@ -4,6 +4,11 @@ Each translation unit compiles in parallel, then one link step produces the
 shared library (static CUDA runtime, only the moe_* C symbols exported).
 A stamp file records the host architecture and a hash of the sources and
 flags, so a library built on another machine is never reused.
+
+Variant "check" builds libmoe_ptpc_check.so with -DMOE_CHECK: every
+data-dependent index (expert ids, row maps) is validated where it is used, and
+a bad one sets an error bit instead of going out of bounds. The binding loads
+it when MOE_LIBRARY_VARIANT=check.
 """
 
 import hashlib
@@ -27,8 +32,12 @@ NVCC_FLAGS = ARCH_FLAGS + [
 ]
 
 
-def library_path():
-    return os.path.join(PKG, LIB_NAME)
+VARIANTS = {"": ([], LIB_NAME, "_build"),
+            "check": (["-DMOE_CHECK"], "libmoe_ptpc_check.so", "_build_check")}
+
+
+def library_path(variant=""):
+    return os.path.join(PKG, VARIANTS[variant][1])
 
 
 def _nvcc():
@@ -62,18 +71,21 @@ def _stamp(extra_flags):
     return h.hexdigest()
 
 
-def build(force=False, extra_flags=(), verbose=False, jobs=None):
-    """Compile and link the library; returns its path."""
-    lib = library_path()
-    stamp_file = os.path.join(BUILD_DIR, "stamp")
+def build(force=False, extra_flags=(), verbose=False, jobs=None, variant=""):
+    """Compile and link the library (or its variant); returns its path."""
+    vflags, _, vdir = VARIANTS[variant]
+    extra_flags = list(vflags) + list(extra_flags)
+    build_dir = os.path.join(PKG, vdir)
+    lib = library_path(variant)
+    stamp_file = os.path.join(build_dir, "stamp")
     stamp = _stamp(extra_flags)
     if (not force and os.path.exists(lib) and os.path.exists(stamp_file)
             and open(stamp_file).read() == stamp):
         return lib
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
-    objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o")
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
             for s in srcs]
 
     def compile_one(pair):

@@ -548,12 +548,12 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
     st = cuda_status(launch_add_rmsnorm_quant(
         x, pre->residual, pre->gamma, pre->eps, d.T, d.D, pre->residual_out, f2s,
         d.k, d.shared ? R : -1, xq, sx, d.shared ? shared_gate_w : nullptr,
-        d.shared ? gate : nullptr, stream, pdl));
+        d.shared ? gate : nullptr, stream, pdl, rows));
   else
     st = cuda_status(launch_quant(x, MOE_DTYPE_BF16, d.T, d.D, f2s, d.k,
                                   d.shared ? R : -1, xq, sx,
                                   d.shared ? shared_gate_w : nullptr,
-                                  d.shared ? gate : nullptr, stream, pdl, false));
+                                  d.shared ? gate : nullptr, stream, pdl, false, rows));
   if (st != MOE_OK) return st;
   mark(4);
   const int hint = (int)std::max<int64_t>(1, R / d.E);
@@ -563,7 +563,7 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
   mark(5);
   st = cuda_status(launch_quant(h, MOE_DTYPE_F32, rows, d.I, nullptr, 1, -1, hq,
                                 sh, nullptr, nullptr, stream, pdl,
-                                /*release_early=*/true));
+                                /*release_early=*/true, rows));
   if (st != MOE_OK) return st;
   mark(6);
   if (f16)
@@ -605,8 +605,10 @@ int take_status(unsigned* word, unsigned* taken, moe_stream_t stream, unsigned* 
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (detail) *detail = bits;
   if (bits == 0) return MOE_OK;
-  // a tile map larger than the launch alone: group offsets past a_rows
-  return bits == moe::kErrBadIndex ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
+  // only bad data (group offsets past a_rows; in the checked build, an index
+  // out of range) and no expired wait
+  return (bits & ~(moe::kErrBadIndex | moe::kErrCheck)) == 0 ? MOE_ERR_INVALID_ARG
+                                                              : MOE_ERR_TIMEOUT;
 }
 
 bool forward_status_ok(const void* ws, size_t ws_bytes) {

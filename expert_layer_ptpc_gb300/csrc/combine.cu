@@ -23,15 +23,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
     const float* __restrict__ y, const int32_t* __restrict__ f2s,
     const float* __restrict__ topk_w, int k, int D,
     const float* __restrict__ y_shared, const float* __restrict__ gate,
-    __nv_bfloat16* __restrict__ out) {
+    __nv_bfloat16* __restrict__ out, int64_t nrows, unsigned* __restrict__ err) {
   const int t = blockIdx.x;
   __shared__ int32_t rows[kMaxTopK];
   __shared__ float wts[kMaxTopK];
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x < k) {
-    rows[threadIdx.x] = f2s[(int64_t)t * k + threadIdx.x];
-    wts[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
+    const int32_t r = f2s[(int64_t)t * k + threadIdx.x];
+    const bool ok = MOE_CHECKED(r >= 0 && r < nrows, err);
+    rows[threadIdx.x] = ok ? r : 0;
+    wts[threadIdx.x] = ok ? topk_w[(int64_t)t * k + threadIdx.x] : 0.f;
   }
   __syncthreads();
   const float g = y_shared != nullptr ? gate[t] : 0.f;
@@ -79,7 +81,8 @@ __global__ void __launch_bounds__(kThreads) combine_f16_kernel(
     const __half* __restrict__ y16, const float* __restrict__ row_scale,
     const int32_t* __restrict__ f2s, const float* __restrict__ topk_w, int k, int D,
     const __half* __restrict__ y16_shared, const float* __restrict__ row_scale_shared,
-    const float* __restrict__ gate, __nv_bfloat16* __restrict__ out) {
+    const float* __restrict__ gate, __nv_bfloat16* __restrict__ out, int64_t nrows,
+    unsigned* __restrict__ err) {
   const int t = blockIdx.x;
   __shared__ int32_t rows[kMaxTopK];
   __shared__ float coef[kMaxTopK];
@@ -87,8 +90,9 @@ __global__ void __launch_bounds__(kThreads) combine_f16_kernel(
   pdl_launch_dependents();
   if (threadIdx.x < k) {
     const int32_t r = f2s[(int64_t)t * k + threadIdx.x];
-    rows[threadIdx.x] = r;
-    coef[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x] * row_scale[r];
+    const bool ok = MOE_CHECKED(r >= 0 && r < nrows, err);
+    rows[threadIdx.x] = ok ? r : 0;
+    coef[threadIdx.x] = ok ? topk_w[(int64_t)t * k + threadIdx.x] * row_scale[r] : 0.f;
   }
   __syncthreads();
   const int c = (blockIdx.y * kThreads + threadIdx.x) * VEC;
@@ -141,7 +145,8 @@ cudaError_t launch_combine_f16(const uint16_t* y16, const float* row_scale,
                          reinterpret_cast<const __half*>(y16), row_scale, f2s, topk_w,
                          k, D, reinterpret_cast<const __half*>(y16_shared),
                          row_scale_shared, shared_gate,
-                         reinterpret_cast<__nv_bfloat16*>(out));
+                         reinterpret_cast<__nv_bfloat16*>(out), (int64_t)T * k,
+                         device_error_word());
   };
   if (D % 16 == 0) return go(combine_f16_kernel<16>, 16);
   return go(combine_f16_kernel<8>, 8);
@@ -155,7 +160,8 @@ cudaError_t launch_combine(const float* y, const int32_t* f2s,
   const dim3 grid((unsigned)T, (unsigned)((D / kVec + kThreads - 1) / kThreads));
   return launch_kernel(pdl, grid, dim3(kThreads), 0, stream, combine_kernel, y,
                        f2s, topk_w, k, D, y_shared, shared_gate,
-                       reinterpret_cast<__nv_bfloat16*>(out));
+                       reinterpret_cast<__nv_bfloat16*>(out), (int64_t)T * k,
+                       device_error_word());
 }
 
 }  // namespace moe

@@ -24,7 +24,24 @@ enum : unsigned {
   kErrBadIndex = 1u << 4,
   kErrTimeoutSched = 1u << 5,
   kErrDebugWait = 1u << 6,
+  kErrCheck = 1u << 7,   // checked build: an index out of range (access skipped)
 };
+
+// Checked build (-DMOE_CHECK, the library variant libmoe_ptpc_check.so): the
+// data-dependent indices (expert ids, row maps, group offsets) are validated
+// where they are used; a bad one sets kErrCheck in the error word and the
+// access is skipped instead of going out of bounds. Compute-sanitizer is not
+// available, and a failing device assert would trap the GPU. In the normal
+// build MOE_CHECKED(ok, err) is the constant true and costs nothing.
+#ifdef MOE_CHECK
+__device__ __forceinline__ bool moe_checked(bool ok, unsigned* err) {
+  if (!ok) atomicOr(err, kErrCheck);
+  return ok;
+}
+#define MOE_CHECKED(ok, err) ::moe::moe_checked((ok), (err))
+#else
+#define MOE_CHECKED(ok, err) true
+#endif
 
 // Wall-clock limit of one wait (ns). Every wait in these kernels normally
 // completes within microseconds; a wait that runs a full second means a

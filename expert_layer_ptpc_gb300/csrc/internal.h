@@ -57,13 +57,14 @@ cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
 // Per-row e4m3 quantisation with scatter; `gate_w` non-null also computes
 // gate_out[r] = sigmoid(in[r] . gate_w) (bf16 input only). `release_early`
 // lets the next kernel launch before this one's dependency wait (see
-// quant.cu for when that is safe).
+// quant.cu for when that is safe). `out_rows`: rows of out_q / out_scale,
+// which the checked build holds destinations to (-1: unknown).
 cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          const int32_t* dst_rows, int copies,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
                          float* gate_out, cudaStream_t stream, bool pdl,
-                         bool release_early);
+                         bool release_early, int64_t out_rows = -1);
 
 // Add + RMSNorm + per-token quantisation (see quant.cu); same destinations
 // and limits as launch_quant.
@@ -73,7 +74,8 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
                                      const int32_t* dst_rows, int copies,
                                      int64_t extra_row_base, uint8_t* out_q,
                                      float* out_scale, const uint16_t* gate_w,
-                                     float* gate_out, cudaStream_t stream, bool pdl);
+                                     float* gate_out, cudaStream_t stream, bool pdl,
+                                     int64_t out_rows = -1);
 
 // Router projection (tcgen05, bf16) with the top-k selection and softmax in
 // its epilogue (router_gemm.cu). Returns a moe_status.

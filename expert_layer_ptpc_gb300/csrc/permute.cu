@@ -72,13 +72,17 @@ __device__ int block_exclusive_scan(int* vals, int n, int* warp_tot) {
 // (i < PL); -1 past the end. All loads are issued before any is used.
 template <int PL>
 __device__ __forceinline__ void load_warp_ids(const int32_t* __restrict__ ids,
-                                              int64_t f0, int64_t R, int (&e)[PL]) {
+                                              int64_t f0, int64_t R, int E, int (&e)[PL],
+                                              unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t begin = f0 + (int64_t)warp * (PL * 32);
 #pragma unroll
   for (int i = 0; i < PL; ++i) {
     const int64_t f = begin + 32 * i + lane;
     e[i] = f < R ? ids[f] : -1;
+#ifdef MOE_CHECK
+    if (f < R && !MOE_CHECKED(e[i] >= 0 && e[i] < E, err)) e[i] = -1;
+#endif
   }
 }
 
@@ -148,7 +152,7 @@ __device__ void write_extra_group(int E, int total, int extra,
 __global__ void __launch_bounds__(kThreads) permute_small_kernel(
     const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ s2f,
-    int32_t* __restrict__ f2s, int extra) {
+    int32_t* __restrict__ f2s, int extra, unsigned* __restrict__ err) {
   extern __shared__ int smem[];
   int* whist = smem;                       // kWarps * E
   int* scan = whist + kWarps * E;          // E + 1
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) permute_small_kernel(
   pdl_launch_dependents();
   constexpr int PL = kSmallChunk / kThreads;
   int mine[PL];
-  load_warp_ids<PL>(ids, 0, R, mine);
+  load_warp_ids<PL>(ids, 0, R, E, mine, err);
   chunk_warp_histograms<PL>(mine, E, whist);
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int c = 0;
@@ -176,7 +180,8 @@ __global__ void __launch_bounds__(kThreads) permute_small_kernel(
 
 // R > kSmallChunk, pass 1: per-chunk expert counts -> hist[c * E + e].
 __global__ void __launch_bounds__(kThreads) permute_hist_kernel(
-    const int32_t* __restrict__ ids, int64_t R, int E, int* __restrict__ hist) {
+    const int32_t* __restrict__ ids, int64_t R, int E, int* __restrict__ hist,
+    unsigned* __restrict__ err) {
   extern __shared__ int smem[];
   pdl_wait();
   pdl_launch_dependents();
@@ -189,6 +194,9 @@ __global__ void __launch_bounds__(kThreads) permute_hist_kernel(
   for (int i = 0; i < PL; ++i) {
     const int64_t f = f0 + threadIdx.x + (int64_t)i * kThreads;
     e[i] = f < R ? ids[f] : -1;
+#ifdef MOE_CHECK
+    if (f < R && !MOE_CHECKED(e[i] >= 0 && e[i] < E, err)) e[i] = -1;
+#endif
   }
   __syncthreads();
 #pragma unroll
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(
 __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
     const int32_t* __restrict__ ids, int64_t R, int E,
     const int* __restrict__ hist, int32_t* __restrict__ s2f,
-    int32_t* __restrict__ f2s) {
+    int32_t* __restrict__ f2s, unsigned* __restrict__ err) {
   extern __shared__ int smem[];
   int* whist = smem;                  // kWarps * E
   int* base = whist + kWarps * E;     // E
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
     base[e] = hist[(int64_t)blockIdx.x * E + e];
   constexpr int PL = kChunk / kThreads;
   int mine[PL];
-  load_warp_ids<PL>(ids, f0, R, mine);
+  load_warp_ids<PL>(ids, f0, R, E, mine, err);
   chunk_warp_histograms<PL>(mine, E, whist);
   warp_bases(base, E, whist);
   chunk_scatter<PL>(mine, f0, R, E, whist, s2f, f2s);
@@ -271,13 +279,13 @@ cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
     if (err != cudaSuccess) return err;
     return launch_kernel(pdl, dim3(1), dim3(kThreads), smem, stream,
                          permute_small_kernel, ids, (int)R, E, counts, offsets,
-                         s2f, f2s, extra_group_rows);
+                         s2f, f2s, extra_group_rows, device_error_word());
   }
   const int nchunks = (int)((R + kChunk - 1) / kChunk);
   int* hist = static_cast<int*>(ws);
   cudaError_t err = launch_kernel(pdl, dim3(nchunks), dim3(kThreads),
                                   E * sizeof(int), stream, permute_hist_kernel,
-                                  ids, R, E, hist);
+                                  ids, R, E, hist, device_error_word());
   if (err != cudaSuccess) return err;
   const size_t smem_scan = (size_t)(E + 1 + kWarps + 1) * sizeof(int);
   err = launch_kernel(pdl, dim3(1), dim3(kThreads), smem_scan, stream,
@@ -291,7 +299,7 @@ cudaError_t launch_permute(const int32_t* ids, int64_t R, int E,
   if (err != cudaSuccess) return err;
   return launch_kernel(pdl, dim3(nchunks), dim3(kThreads), smem_sc, stream,
                        permute_scatter_kernel, ids, R, E, (const int*)hist, s2f,
-                       f2s);
+                       f2s, device_error_word());
 }
 
 }  // namespace moe

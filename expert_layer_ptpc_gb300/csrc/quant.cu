@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
     const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
     uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
     const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out,
-    int release_early) {
+    int release_early, int64_t out_rows, unsigned* __restrict__ err) {
   __shared__ float red_max[kMaxThreads / 32];
   __shared__ float red_dot[kMaxThreads / 32];
   __shared__ int64_t dst[kMaxTopK + 1];
@@ -99,9 +99,13 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
   const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
   // strided: a block narrower than ndst (32 threads, 32 copies + the shared
   // row) still fills every entry
-  for (int i = tid; i < ndst; i += blockDim.x)
-    dst[i] = i < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + i] : r)
-                       : extra_row_base + r;
+  for (int i = tid; i < ndst; i += blockDim.x) {
+    int64_t d = i < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + i] : r)
+                          : extra_row_base + r;
+    // checked build: a destination outside [0, out_rows) is skipped
+    if (!MOE_CHECKED(d >= 0 && (out_rows < 0 || d < out_rows), err)) d = -1;
+    dst[i] = d;
+  }
   __syncthreads();
   if (warp == 0) {
     float a = lane < nwarps ? red_max[lane] : 0.f;
@@ -115,7 +119,8 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
   }
   __syncthreads();
   const float s = __fdiv_rn(fmaxf(red_max[0], 1e-12f), 448.0f);
-  for (int i = tid; i < ndst; i += blockDim.x) out_scale[dst[i]] = s;
+  for (int i = tid; i < ndst; i += blockDim.x)
+    if (dst[i] >= 0) out_scale[dst[i]] = s;
   if (gate_w != nullptr && tid == 0) gate_out[r] = 1.0f / (1.0f + expf(-red_dot[0]));
 
 #pragma unroll
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(kMaxThreads) quant_rows_kernel(
       }
       const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
       for (int d = 0; d < ndst; ++d)
-        *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
+        if (dst[d] >= 0) *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
     }
   }
 }
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_warp_kernel(
     const int32_t* __restrict__ dst_rows, int copies, int64_t extra_row_base,
     uint8_t* __restrict__ out_q, float* __restrict__ out_scale,
     const __nv_bfloat16* __restrict__ gate_w, float* __restrict__ gate_out,
-    int release_early) {
+    int release_early, int64_t out_rows, unsigned* __restrict__ err) {
   if (release_early) pdl_launch_dependents();
   pdl_wait();
   if (!release_early) pdl_launch_dependents();
@@ -182,12 +187,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_warp_kernel(
   const int nmain = dst_rows != nullptr ? copies : 1;
   const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
   int64_t my_dst = 0;
-  if (lane < ndst)
+  if (lane < ndst) {
     my_dst = lane < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + lane] : r)
                           : extra_row_base + r;
+    // checked build: a destination outside [0, out_rows) is skipped
+    if (!MOE_CHECKED(my_dst >= 0 && (out_rows < 0 || my_dst < out_rows), err)) my_dst = -1;
+  }
   amax = warp_max(amax);
   const float s = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
-  if (lane < ndst) out_scale[my_dst] = s;
+  if (lane < ndst && my_dst >= 0) out_scale[my_dst] = s;
   if (gate_w != nullptr) {
     dot = warp_sum(dot);
     if (lane == 0) gate_out[r] = 1.0f / (1.0f + expf(-dot));
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quant_rows_warp_kernel(
     // every lane takes part in the shuffles; only lanes with a unit store
     for (int d = 0; d < ndst; ++d) {
       const int64_t dd = __shfl_sync(0xffffffffu, my_dst, d);
-      if (u < nunits) *reinterpret_cast<uint4*>(out_q + dd * cols + u * kVec) = packed;
+      if (u < nunits && dd >= 0) *reinterpret_cast<uint4*>(out_q + dd * cols + u * kVec) = packed;
     }
   }
 }
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
     __nv_bfloat16* res_out, const int32_t* __restrict__ dst_rows,
     int copies, int64_t extra_row_base, uint8_t* __restrict__ out_q,
     float* __restrict__ out_scale, const __nv_bfloat16* __restrict__ gate_w,
-    float* __restrict__ gate_out, int sbits) {
+    float* __restrict__ gate_out, int sbits, int64_t out_rows, unsigned* __restrict__ err) {
   __shared__ unsigned long long red_sq[kMaxThreads / 32];
   __shared__ int red_e[kMaxThreads / 32];
   __shared__ float red_max[kMaxThreads / 32];
@@ -353,9 +361,13 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
   const int ndst = nmain + (extra_row_base >= 0 ? 1 : 0);
   // strided: a block narrower than ndst (32 threads, 32 copies + the shared
   // row) still fills every entry
-  for (int i = tid; i < ndst; i += blockDim.x)
-    dst[i] = i < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + i] : r)
-                       : extra_row_base + r;
+  for (int i = tid; i < ndst; i += blockDim.x) {
+    int64_t d = i < nmain ? (dst_rows != nullptr ? (int64_t)dst_rows[r * copies + i] : r)
+                          : extra_row_base + r;
+    // checked build: a destination outside [0, out_rows) is skipped
+    if (!MOE_CHECKED(d >= 0 && (out_rows < 0 || d < out_rows), err)) d = -1;
+    dst[i] = d;
+  }
   __syncthreads();
   if (warp == 0) {
     float a = lane < nwarps ? red_max[lane] : 0.f;
@@ -369,7 +381,8 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
   }
   __syncthreads();
   const float s = __fdiv_rn(fmaxf(red_max[0], 1e-12f), 448.0f);
-  for (int i = tid; i < ndst; i += blockDim.x) out_scale[dst[i]] = s;
+  for (int i = tid; i < ndst; i += blockDim.x)
+    if (dst[i] >= 0) out_scale[dst[i]] = s;
   if (gate_w != nullptr && tid == 0) gate_out[r] = 1.0f / (1.0f + expf(-red_dot[0]));
 #pragma unroll
   for (int i = 0; i < UNITS; ++i) {
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kMaxThreads) add_rmsnorm_quant_kernel(
       }
       const uint4 packed = make_uint4(w[0], w[1], w[2], w[3]);
       for (int d = 0; d < ndst; ++d)
-        *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
+        if (dst[d] >= 0) *reinterpret_cast<uint4*>(out_q + dst[d] * cols + u * kVec) = packed;
     }
   }
 }
@@ -416,7 +429,7 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
                         int64_t extra_row_base, uint8_t* out_q,
                         float* out_scale, const __nv_bfloat16* gate_w,
                         float* gate_out, cudaStream_t stream, bool pdl,
-                        bool release_early) {
+                        bool release_early, int64_t out_rows) {
   const int nunits = cols / kVec;
   const int ndst = (dst_rows != nullptr ? copies : 1) + (extra_row_base >= 0 ? 1 : 0);
   if (nunits <= 64 && ndst <= 32) {
@@ -424,7 +437,8 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
     auto go = [&](auto kern) {
       return launch_kernel(pdl, grid, dim3(kWarpsPerBlock * 32), 0, stream, kern, in,
                            rows, cols, dst_rows, copies, extra_row_base, out_q,
-                           out_scale, gate_w, gate_out, release_early ? 1 : 0);
+                           out_scale, gate_w, gate_out, release_early ? 1 : 0, out_rows,
+                           device_error_word());
     };
     if (nunits <= 32) return go(quant_rows_warp_kernel<InT, 1>);
     return go(quant_rows_warp_kernel<InT, 2>);
@@ -435,7 +449,8 @@ cudaError_t launch_rows(const InT* in, int64_t rows, int cols,
   auto go = [&](auto kern) {
     return launch_kernel(pdl, grid, block, 0, stream, kern, in, rows, cols,
                          dst_rows, copies, extra_row_base, out_q, out_scale,
-                         gate_w, gate_out, release_early ? 1 : 0);
+                         gate_w, gate_out, release_early ? 1 : 0, out_rows,
+                         device_error_word());
   };
   if (units <= 1) return go(quant_rows_kernel<InT, 1>);
   if (units <= 2) return go(quant_rows_kernel<InT, 2>);
@@ -449,17 +464,17 @@ cudaError_t launch_quant(const void* in, int in_dtype, int64_t rows, int cols,
                          int64_t extra_row_base, uint8_t* out_q,
                          float* out_scale, const uint16_t* gate_w,
                          float* gate_out, cudaStream_t stream, bool pdl,
-                         bool release_early) {
+                         bool release_early, int64_t out_rows) {
   if (rows == 0) return cudaSuccess;
   if (in_dtype == 0)
     return launch_rows(static_cast<const __nv_bfloat16*>(in), rows, cols,
                        dst_rows, copies, extra_row_base, out_q, out_scale,
                        reinterpret_cast<const __nv_bfloat16*>(gate_w), gate_out,
-                       stream, pdl, release_early);
+                       stream, pdl, release_early, out_rows);
   return launch_rows(static_cast<const float*>(in), rows, cols, dst_rows, copies,
                      extra_row_base, out_q, out_scale,
                      (const __nv_bfloat16*)nullptr, (float*)nullptr, stream, pdl,
-                     release_early);
+                     release_early, out_rows);
 }
 
 cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
@@ -468,7 +483,8 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
                                      const int32_t* dst_rows, int copies,
                                      int64_t extra_row_base, uint8_t* out_q,
                                      float* out_scale, const uint16_t* gate_w,
-                                     float* gate_out, cudaStream_t stream, bool pdl) {
+                                     float* gate_out, cudaStream_t stream, bool pdl,
+                                     int64_t out_rows) {
   if (rows == 0) return cudaSuccess;
   const int nunits = cols / kVec;
   const int threads = std::min(kMaxThreads, ((nunits + 31) / 32) * 32);
@@ -484,7 +500,7 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t* x, const uint16_t* res,
     return launch_kernel(pdl, grid, block, 0, stream, kern, bf(x), bf(res), bf(gamma),
                          eps, cols, reinterpret_cast<__nv_bfloat16*>(res_out),
                          dst_rows, copies, extra_row_base, out_q, out_scale,
-                         bf(gate_w), gate_out, sbits);
+                         bf(gate_w), gate_out, sbits, out_rows, device_error_word());
   };
   if (units <= 1) return go(add_rmsnorm_quant_kernel<1>);
   if (units <= 2) return go(add_rmsnorm_quant_kernel<2>);

@@ -431,12 +431,15 @@ MOE_API int moe_forward_profiled(const moe_dims* dims, const uint16_t* x,
  * moe_device_status - synchronise `stream`, then read and clear the device
  * error word that kernels set when a bounded wait expires or a grouped GEMM
  * finds group offsets that describe more rows than `a_rows`. Returns MOE_OK;
- * MOE_ERR_INVALID_ARG when the offsets bit alone is set; MOE_ERR_TIMEOUT when
+ * MOE_ERR_INVALID_ARG when only bad-data bits (16, 128) are set; MOE_ERR_TIMEOUT when
  * a wait expired; MOE_ERR_CUDA if the stream reported a CUDA error.
  * `detail` (nullable) receives the raw error bits:
  *   1 TMA producer wait, 2 MMA issuer wait, 4 epilogue wait, 8 drain wait,
  *   16 tile map larger than the launch (offsets past a_rows; those tiles are
- *   not computed), 32 tile scheduler wait, 64 moe_debug_expire_wait.
+ *   not computed), 32 tile scheduler wait, 64 moe_debug_expire_wait,
+ *   128 (checked build libmoe_ptpc_check.so only) an expert id, row map entry
+ *   or destination row out of range: the access was skipped. MOE_ERR_INVALID_ARG
+ *   is returned when only bits 16 and 128 are set.
  */
 MOE_API int moe_device_status(moe_stream_t stream, unsigned* detail);
 

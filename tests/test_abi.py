@@ -130,3 +130,14 @@ def test_workspace_layout_has_guard_bands(lib, dims_args):
     ends = [o for o, _ in lay[1:]] + [total]
     for (o, n), nxt in zip(lay, ends):
         assert o % 256 == 0 and o + n + 256 <= nxt, (o, n, nxt)
+
+
+def test_checked_build_exports_the_same_symbols():
+    """The checked variant (-DMOE_CHECK) compiles and exports exactly the
+    header's entry points, like the normal library."""
+    import subprocess
+    lib = build.build(variant="check")
+    out = subprocess.run(["nm", "-D", "--defined-only", lib], capture_output=True,
+                         text=True, check=True).stdout
+    names = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert {n for n in names if n.startswith("moe_")} == set(binding.exported_names())
