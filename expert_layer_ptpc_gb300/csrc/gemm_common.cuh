@@ -47,6 +47,7 @@ __device__ __forceinline__ float fp16_rho(float bound, int K) {
 
 struct TileInfo {
   int group, ctile, row0, row_end;
+  int width;   // token rows of the tile (the last tile of a group may hold fewer)
 };
 
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* prefix,
@@ -68,6 +69,35 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* prefix,
   t.ctile = local / tt;
   t.row0 = start + (local % tt) * bn;
   t.row_end = end;
+  t.width = bn;
+  return t;
+}
+
+// Balanced tiles of at most bn_max rows: a group of r rows is cut into
+// tt = ceil(r / bn_max) tiles of w = 32 * ceil(ceil(r / tt) / 32) rows, the
+// last one holding the rest (w <= bn_max, and every tile holds rows). The
+// prefix counts ceil(r / bn_max) tiles per channel tile, as for decode_tile.
+__device__ __forceinline__ TileInfo decode_tile_balanced(int tile, const int* prefix,
+                                                         int groups,
+                                                         const int32_t* offsets,
+                                                         int bn_max) {
+  int lo = 0, hi = groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int start = offsets[g], end = offsets[g + 1];
+  const int rows = end - start;
+  const int tt = (rows + bn_max - 1) / bn_max;
+  const int w = ((rows + tt - 1) / tt + 31) / 32 * 32;
+  const int local = tile - prefix[g];
+  TileInfo t;
+  t.group = g;
+  t.ctile = local / tt;
+  t.row0 = start + (local % tt) * w;
+  t.row_end = end;
+  t.width = w;
   return t;
 }
 
@@ -344,6 +374,13 @@ inline int64_t token_tiles_upper(int64_t a_rows, int groups, int bn) {
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
                int box_rows);
 
+// The gate/up weights [groups][2N][K] (gate rows, then up rows) as a 5D TMA
+// tensor map whose 16 KB box holds 4 blocks of 16 channels, each as its 16
+// gate rows followed by the same channels' 16 up rows (128-byte swizzle).
+// Coordinates: (k, 0, 0, first channel / 16, expert). Needs N % 64 == 0.
+bool make_tmap_gateup_interleaved(CUtensorMap* map, const void* W, int groups, int N,
+                                  int K);
+
 // Row-major [rows, cols] fp32 (elem_bytes 4) or fp16 (2) matrix as a 2D TMA
 // tensor map for stores of box_rows x box_cols boxes (no swizzle).
 bool make_tmap_out(CUtensorMap* map, void* base, int64_t rows, int cols,
@@ -359,6 +396,15 @@ int cta_pair_mode();
 // MOE_GEMM_DOWN_PAIR: the same switch for the down projection alone (its
 // fp16-output form); unset (-1) follows MOE_GEMM_CTA_PAIR, then the rule.
 int down_pair_mode();
+
+// Token tiles of the CTA-pair kernels: 1 (default) cuts an expert's rows into
+// equal tiles (widths rounded up to 32 rows), MOE_GEMM_BALANCED=0 into
+// full tiles and one partial tail.
+int balanced_tiles();
+
+// MOE_GEMM_WIDE: 1 runs gate/up CTA-pair tiles of up to 512 tokens (two MMAs
+// per K step) above 256 rows per expert, 0 never; unset (-1): the rule.
+int wide_tiles_mode();
 
 }  // namespace gemm
 }  // namespace moe

@@ -11,18 +11,20 @@
 // halves the shared-memory traffic per multiply-add on the B side.
 //
 // Tile = 256 MMA rows x BN tokens of one expert:
-//   gate/up: 128 channels; each CTA packs 64 gate rows and the matching 64
-//            up rows (its channels ctile*128 + rank*64 + [0, 64)), so SwiGLU
-//            partners meet in one CTA (exchanged through shared memory);
+//   gate/up: 128 channels; each CTA holds the gate and the up rows of its 64
+//            channels ctile*128 + rank*64 + [0, 64), interleaved in blocks
+//            of 16 (16 gate rows, the same channels' 16 up rows, ...) by one
+//            5D TMA box, so that SwiGLU partners land in one warp's TMEM
+//            lane quarter, 16 lanes apart;
 //   down:    256 output channels, 128 per CTA.
 //
 // Roles per CTA (11 warps), both CTAs of the pair:
 //   warp 0      TMEM allocation (both CTAs); the MMA issuer (leader)
 //   warps 1-4   epilogue on this CTA's TMEM rows
-//   warps 5-10  TMA producers, one box each: this CTA's two 64-row weight
-//               boxes and its 32-row token boxes, into its own ring of
-//               stages; both CTAs' copies complete on the leader's stage
-//               barrier, which expects both halves
+//   warps 5-10  TMA producers, one box each: this CTA's weight box(es) and
+//               its token boxes, into its own ring of stages; both CTAs'
+//               copies complete on the leader's stage barrier, which expects
+//               both halves
 // The leader's commits are multicast to both CTAs (stage free, accumulator
 // ready); both CTAs' epilogues release an accumulator buffer by arriving on
 // the leader's barrier. All waits are bounded (common.cuh).
@@ -98,6 +100,29 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void* 
       : "memory");
 }
 
+// 5D tiled load (the interleaved gate/up weights) into this CTA's shared
+// memory; `pair` counts its completion on the leader's barrier (a
+// shared::cluster address), else on this CTA's own.
+__device__ __forceinline__ void tma_load_5d(uint32_t smem_dst, const void* tmap, int32_t x0,
+                                            int32_t x3, int32_t x4, uint32_t bar,
+                                            uint64_t cache_policy, bool pair) {
+  if (pair)
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::"
+        "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %3, %4, %5}], [%6], %7;" ::"r"(
+            smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x0), "r"(0), "r"(x3), "r"(x4), "r"(bar),
+        "l"(cache_policy)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes."
+        "L2::cache_hint [%0], [%1, {%2, %3, %3, %4, %5}], [%6], %7;" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x0), "r"(0), "r"(x3), "r"(x4), "r"(bar),
+        "l"(cache_policy)
+        : "memory");
+}
+
 __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag,
                                                   unsigned* err, unsigned code) {
@@ -121,14 +146,17 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int BN, bool GATEUP, bool OUT16 = false>
+template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false>
 struct PairCfg {
   static constexpr int kHalfB = BN / 2;                  // token rows per CTA
-  // TMA boxes of one stage (per CTA): two 64-row weight boxes, then 32-row
-  // token boxes; one producer warp per box
-  static constexpr int kTBoxRows = 32;
+  // TMA boxes of one stage (per CTA): the weights (gate/up: one 128-row 5D
+  // box; down: two 64-row boxes), then 32-row (wide tiles: 64-row) token
+  // boxes; one producer warp per box
+  static constexpr int kWBoxes = GATEUP ? 1 : 2;
+  static constexpr int kWBoxRows = 128 / kWBoxes;
+  static constexpr int kTBoxRows = WIDE ? 64 : 32;
   static constexpr int kTBoxes = kHalfB / kTBoxRows;
-  static constexpr int kBoxes = 2 + kTBoxes;
+  static constexpr int kBoxes = kWBoxes + kTBoxes;
   static_assert(kBoxes <= kMaxBoxes, "one producer warp per box");
   static constexpr int kATile = 128 * kBK;               // this CTA's 128 MMA rows
   static constexpr int kBTile = kHalfB * kBK;
@@ -137,42 +165,76 @@ struct PairCfg {
   static constexpr int kAccBufs = 2 * BN <= 512 ? 2 : 1;
   static constexpr int kTmemCols = pow2_at_least(kAccBufs * BN);
   static constexpr int kChunk = 32;                      // epilogue columns per pass
-  static constexpr int kXBytes = GATEUP ? 64 * kChunk * 4 : 0;
   static constexpr int kTileCh = GATEUP ? 128 : 256;     // channels per tile
-  static constexpr int kNumBars = 2 * kStages + 7;
-  // output staging for TMA stores: per epilogue warp a box of 32 channels x
-  // 32 tokens (down) or x 16 tokens (gate/up, after the SwiGLU exchange)
-  static constexpr int kOutRows = GATEUP ? 16 : 32;
-  static constexpr int kOutBytes = 4 * kOutRows * 32 * 4;
-  static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
-                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
-  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
+  static constexpr int kNumBars = 2 * kStages + 5;
+  // output staging for TMA stores, per epilogue warp a box of 32 tokens x
+  // 32 channels (down) or 16 channels (gate/up)
+  static constexpr int kOutRows = 32;
+  static constexpr int kOutCols = GATEUP ? 16 : 32;
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= (WIDE ? 512 : 256), "token tile");
+  static_assert(!WIDE || (GATEUP && BN == 512), "wide tiles: gate/up, 512 tokens");
   static_assert(kStages >= 3, "pipeline depth");
   // fp16 down output: four more epilogue warps (12-15, the same TMEM lane
   // quarters) take every other 32-token chunk. A down tile's K is short
   // (K = I), and four warps drained 128 channels x 256 tokens slower than
   // the MMAs filled them. Their fp16 boxes fit the same staging bytes.
-  static constexpr bool kWideEpi = !GATEUP && OUT16;
+  // Wide gate/up tiles (one accumulator buffer, so the epilogue does not
+  // overlap the next tile's MMAs) use the second set too.
+  static constexpr bool kWideEpi = (!GATEUP && OUT16) || WIDE;
   static constexpr int kEpiSets = kWideEpi ? 2 : 1;
   static constexpr int kThreadsT = kThreads + (kWideEpi ? 4 * 32 : 0);
+  // fp16 boxes of the down projection's second set fit the first set's bytes
+  static constexpr int kOutBytes =
+      4 * (GATEUP ? kEpiSets : 1) * kOutRows * kOutCols * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStage + kOutBytes +
+                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-// MMA width (token columns) of a tile with `nvalid` token rows: BN, halved
-// while half of it still covers them, down to 64 so that each CTA's share is
-// at least one 32-row token box. An expert's last, partial tile then neither
-// loads nor multiplies the rows past its end.
-template <int BN>
-__device__ __forceinline__ int pair_width(int nvalid) {
-  int n = BN;
-  while (n > 64 && n / 2 >= nvalid) n /= 2;
-  return n;
+// Token rows a tile holds, and its MMA width: those rows rounded up to a
+// multiple of 32, at least 64 so that each CTA's share is at least one
+// 32-row token box. A partial tile then neither loads nor multiplies more
+// than 31 rows past its end. A wide tile (up to 512 tokens) runs as two MMAs
+// per K step, N1 = 256 columns and N2 = the rest, at least 64; the width is
+// N1 + N2.
+__device__ __forceinline__ int tile_rows(const TileInfo& ti) {
+  return min(ti.width, ti.row_end - ti.row0);
+}
+__device__ __forceinline__ int pair_width(const TileInfo& ti) {
+  const int n = max(64, (tile_rows(ti) + 31) & ~31);
+  return n <= 256 ? n : 256 + max(64, n - 256);
+}
+
+// Token box t of a CTA (rank) in a tile of MMA width n: whether it is
+// loaded, the row of the stage's token tile it fills and the first token row
+// it copies. Narrow tiles: the CTA's n/2 tokens in 32-row boxes. Wide tiles
+// (64-row boxes): boxes 0-1 fill rows 0-127 with the CTA's half of the first
+// N1 tokens, boxes 2-3 rows 128-255 with its half of the next N2.
+template <bool WIDE>
+__device__ __forceinline__ bool token_box(int t, int n, int row0, int rank, int& smem_row,
+                                          int& token_row) {
+  if constexpr (!WIDE) {
+    const int half = n / 2;
+    smem_row = t * 32;
+    token_row = row0 + rank * half + t * 32;
+    return t * 32 < half;
+  } else {
+    const int n1 = min(n, 256), n2 = n - n1;
+    if (t < 2) {
+      smem_row = t * 64;
+      token_row = row0 + rank * (n1 / 2) + t * 64;
+      return t * 64 < n1 / 2;
+    }
+    smem_row = 128 + (t - 2) * 64;
+    token_row = row0 + n1 + rank * (n2 / 2) + (t - 2) * 64;
+    return (t - 2) * 64 < n2 / 2;
+  }
 }
 
 // OUT16 (down projection only): y as fp16 codes plus one factor per row, the
 // encoding of the single-CTA kernel (gemm_tc.cu, fp16_rho).
-template <int BN, bool GATEUP, bool OUT16>
-__global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
+template <int BN, bool GATEUP, bool OUT16, bool WIDE>
+__global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1)
     grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
@@ -180,16 +242,15 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
     const float* __restrict__ w_scale, const int32_t* __restrict__ offsets,
     int groups, int N, int K, float* __restrict__ out,
     __half* __restrict__ out16, float* __restrict__ row_scale,
-    const float* __restrict__ w_bound, unsigned* __restrict__ err) {
+    const float* __restrict__ w_bound, int balanced, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
-  using C = PairCfg<BN, GATEUP, OUT16>;
+  using C = PairCfg<BN, GATEUP, OUT16, WIDE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
-  float* outstage = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kXBytes);
+  float* outstage = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage +
-                                               C::kXBytes + C::kOutBytes);
+                                               C::kOutBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
@@ -209,8 +270,6 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
   auto accf_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
   auto acce_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * C::kStages + 4);
-  const uint32_t xfull_bar = smem_u32(bars + 2 * C::kStages + 5);
-  const uint32_t xempty_bar = smem_u32(bars + 2 * C::kStages + 6);
   auto stage_a = [&](int s) { return smem_u32(smem + s * C::kStage); };
   auto stage_b = [&](int s) { return smem_u32(smem + s * C::kStage + C::kATile); };
 
@@ -225,8 +284,6 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
       mbar_init(acce_bar(b), 8 * C::kEpiSets);   // each epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
-    mbar_init(xfull_bar, 4);       // one per epilogue warp
-    mbar_init(xempty_bar, 4);
     // ring consumers: each producer, each epilogue warp, the leader's MMA issuer
     sched_init(sched, C::kBoxes + 4 * C::kEpiSets + (rank == 0 ? 1 : 0));
     *abort_flag = 0;
@@ -267,11 +324,16 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
   const int total_tiles = prefix[groups];
+  // an expert's rows in ceil(rows / BN) tiles of BN rows (the last partial),
+  // or, balanced, of equal widths (multiples of 32)
+  auto decode = [&](int tile) {
+    return balanced ? decode_tile_balanced(tile, prefix, groups, offsets, BN)
+                    : decode_tile(tile, prefix, groups, offsets, BN);
+  };
 
-  // this CTA's first weight row of a tile (gate rows for gate/up)
+  // down: this CTA's first weight row of a tile
   auto weight_row = [&](const TileInfo& ti) {
-    return GATEUP ? ti.group * 2 * N + ti.ctile * 128 + (int)rank * 64
-                  : ti.group * N + ti.ctile * 256 + (int)rank * 128;
+    return ti.group * N + ti.ctile * 256 + (int)rank * 128;
   };
   // Both CTAs' copies of stage s complete on the leader's full[s]: the
   // leader's own with a plain TMA, the peer's with the pair form.
@@ -288,31 +350,33 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
       sched_run(sched, first_tile, total_tiles, 2, rank, abort_flag, err);
   } else if (box >= 0) {
     // ---------------- TMA producers (both CTAs): box `box` of every stage ----------------
-    const bool weight_box = box < 2;
+    const bool weight_box = box < C::kWBoxes;
     if (lane == 0 && box < C::kBoxes) {
       const uint64_t pol = weight_box ? l2_policy_evict_normal() : l2_policy_evict_last();
       // bytes of this box in one CTA; the leader expects both CTAs' bytes
-      const uint32_t bytes = weight_box ? 64u * kBK : (uint32_t)(C::kTBoxRows * kBK);
+      const uint32_t bytes =
+          (uint32_t)((weight_box ? C::kWBoxRows : C::kTBoxRows) * kBK);
       auto issue = [&](int s, int kb, const TileInfo& ti) {
         const int x = kb * kBK;
-        if (box == 0)        // gate rows, or the first half of the down rows
-          load(stage_a(s), &tm_w, x, weight_row(ti), s, pol);
-        else if (box == 1)   // up rows, or the second half of the down rows
-          load(stage_a(s) + 64 * kBK, &tm_w, x, weight_row(ti) + (GATEUP ? N : 64), s,
-               pol);
-        else {               // 32 rows of this CTA's half of the token tile
-          const int t = box - 2;
-          const int half = pair_width<BN>(ti.row_end - ti.row0) / 2;
-          if (t * C::kTBoxRows < half)
-            load(stage_b(s) + t * C::kTBoxRows * kBK, &tm_a, x,
-                 ti.row0 + (int)rank * half + t * C::kTBoxRows, s, pol);
+        if (GATEUP && box == 0) {   // gate and up rows of this CTA's 64 channels
+          tma_load_5d(stage_a(s), &tm_w, x, (ti.ctile * 128 + (int)rank * 64) / 16,
+                      ti.group, rank == 0 ? full_bar(s) : map_to_rank(full_bar(s), 0),
+                      pol, rank != 0);
+        } else if (weight_box) {    // down rows: 64-row halves
+          load(stage_a(s) + box * 64 * kBK, &tm_w, x, weight_row(ti) + box * 64, s, pol);
+        } else {                    // rows of this CTA's half of the token tile
+          int srow, trow;
+          if (token_box<WIDE>(box - C::kWBoxes, pair_width(ti), ti.row0, (int)rank, srow,
+                              trow))
+            load(stage_b(s) + srow * kBK, &tm_a, x, trow, s, pol);
         }
       };
       // a token box past the tile's MMA width is not loaded by either CTA
       auto expect = [&](int s, const TileInfo& ti) {
         if (rank != 0) return;
-        const bool used = weight_box || (box - 2) * C::kTBoxRows <
-                                            pair_width<BN>(ti.row_end - ti.row0) / 2;
+        int srow, trow;
+        const bool used = weight_box || token_box<WIDE>(box - C::kWBoxes, pair_width(ti),
+                                                        ti.row0, 0, srow, trow);
         mbar_arrive_expect_tx(full_bar(s), used ? 2 * bytes : 0u);
       };
       int last_phase[C::kStages];
@@ -325,7 +389,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
       int npre = 0;
       TileInfo t0{};
       if (weight_box && first_tile < total_tiles) {
-        t0 = decode_tile(first_tile, prefix, groups, offsets, BN);
+        t0 = decode(first_tile);
         npre = kblocks < C::kStages ? kblocks : C::kStages;
         for (int kb = 0; kb < npre; ++kb) {
           expect(kb, t0);
@@ -345,7 +409,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
                                           err, kErrTimeoutProducer);
         if (tile < 0) break;
         const bool pre = first && npre > 0 && tile == first_tile;
-        const TileInfo ti = pre ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
+        const TileInfo ti = pre ? t0 : decode(tile);
         for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!wait_cluster_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                     kErrTimeoutProducer)) {
@@ -401,9 +465,10 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
                                   kErrTimeoutMma)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)(ab * BN);
-        const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
-        const uint32_t idesc =
-            idesc_e4m3_f32(256, pair_width<BN>(ti.row_end - ti.row0));
+        const int n = pair_width(decode(tile));
+        const int n1 = min(n, 256), n2 = n - n1;   // n2 > 0: wide tiles only
+        const uint32_t idesc = idesc_e4m3_f32(256, n1);
+        const uint32_t idesc2 = idesc_e4m3_f32(256, n2 > 0 ? n2 : 64);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_cluster_bounded(full_bar(s), ph, abort_flag, err, kErrTimeoutMma)) {
             ok = false;
@@ -412,9 +477,13 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
           tc_fence_after_sync();
           const uint32_t a = stage_a(s), b = stage_b(s);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk)
-            mma_pair(d, smem_desc_k_sw128(a + kk * 32), smem_desc_k_sw128(b + kk * 32),
-                     idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 32; ++kk) {
+            const uint64_t adesc = smem_desc_k_sw128(a + kk * 32);
+            mma_pair(d, adesc, smem_desc_k_sw128(b + kk * 32), idesc, (kb | kk) != 0);
+            if (WIDE && n2 > 0)   // columns 256.. from token rows 128.. of the stage
+              mma_pair(d + 256, adesc, smem_desc_k_sw128(b + 128 * kBK + kk * 32), idesc2,
+                       (kb | kk) != 0);
+          }
           mma_commit_pair_mc(empty_bar(s), 0x3);   // stage free in both CTAs
           if (++s == C::kStages) {
             s = 0;
@@ -434,7 +503,6 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
     const int q = warp & 3;               // TMEM lane quarter of this warp
     const int m = q * 32 + lane;          // accumulator row of this thread
     int it = 0;
-    uint32_t xc = 0;
     bool ok = true;
     // Output of C::kOutRows tokens from token r0 on, for this warp's 32
     // channels ch0 + lane (v[j] = token r0 + j). A box inside the expert goes
@@ -445,7 +513,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
     const int eset = warp < kSchedWarp ? 0 : 1;
     float* obuf = OUT16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(outstage) +
                                                    e_idx * C::kOutRows * 32)
-                        : outstage + e_idx * C::kOutRows * 32;
+                        : outstage + e_idx * C::kOutRows * C::kOutCols;
     auto emit = [&](int r0, int row_end, int ch0, const float* v) {
       if (r0 + C::kOutRows <= row_end) {
         if (lane == 0) bulk_wait_read_all();
@@ -485,64 +553,67 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
                              kErrTimeoutEpilogue))
         break;
       tc_fence_after_sync();
-      const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
-      const int nvalid = min(BN, ti.row_end - ti.row0);
+      const TileInfo ti = decode(tile);
+      const int nvalid = tile_rows(ti);
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN);
       if (GATEUP) {
-        // lanes 0-63 hold gate, 64-127 up, of channels ctile*128 + rank*64 +
-        // [0, 64). Per 32-column chunk the gate threads hand their columns
-        // 16-31 to the up threads and receive up columns 0-15, so every
-        // thread finishes 16 outputs.
-        const bool is_gate = q < 2;
-        const int pm = is_gate ? m : m - 64;          // channel within the CTA
-        const int ch = ti.ctile * 128 + (int)rank * 64 + pm;
+        // TMEM lanes 32q .. 32q+15 hold the gate rows of channels ch0 + [0,
+        // 16), ch0 = ctile*128 + rank*64 + 16q, and lanes 32q+16 .. 32q+31
+        // the up rows of the same channels. Per 32-column chunk a gate
+        // thread trades its columns 16-31 for its up partner's (lane + 16)
+        // columns 0-15, one shuffle each, so every thread finishes 16
+        // outputs of its channel.
+        const bool is_gate = lane < 16;
+        const int ch = ti.ctile * 128 + (int)rank * 64 + q * 16 + (lane & 15);
         const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
         const float swu = w_scale[(int64_t)ti.group * 2 * N + N + ch];
-        float* xg = xbuf;              // gate values of columns 16-31 [16][64]
-        float* xu = xbuf + 16 * 64;    // up values of columns 0-15    [16][64]
-        for (int n0 = 0; ok && n0 < nvalid; n0 += C::kChunk, ++xc) {
+        const int c0 = is_gate ? 0 : 16;           // this thread's columns
+        // token scales of a chunk (lane = column), loaded one chunk ahead;
+        // with two epilogue sets, set e takes chunks e, e + 2, ...
+        constexpr int kStep = C::kChunk * C::kEpiSets;
+        const int nfirst = C::kChunk * eset;
+        float sx_next = nfirst + lane < nvalid ? a_scale[ti.row0 + nfirst + lane] : 0.f;
+        for (int n0 = nfirst; n0 < nvalid; n0 += kStep) {
+          const float sx_l = sx_next;
+          if (n0 + kStep < nvalid)
+            sx_next = n0 + kStep + lane < nvalid ? a_scale[ti.row0 + n0 + kStep + lane] : 0.f;
           float a[C::kChunk];
           tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&a[0]));
           tmem_ld_x16(taddr + n0 + 16, *reinterpret_cast<float(*)[16]>(&a[16]));
           tmem_ld_wait();
-          const float sx_l = n0 + lane < nvalid ? a_scale[ti.row0 + n0 + lane] : 0.f;
-          if (!warp_wait(xempty_bar, (xc & 1u) ^ 1u, abort_flag, err,
-                         kErrTimeoutEpilogue)) {
-            ok = false;
-            break;
-          }
-          if (is_gate) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xg[j * 64 + pm] = a[16 + j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xu[j * 64 + pm] = a[j];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(xfull_bar);
-          if (!warp_wait(xfull_bar, xc & 1u, abort_flag, err, kErrTimeoutEpilogue)) {
-            ok = false;
-            break;
-          }
-          float g[16], u[16];
-          const int c0 = is_gate ? 0 : 16;           // this thread's columns
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            g[j] = is_gate ? a[j] : xg[j * 64 + pm];
-            u[j] = is_gate ? xu[j * 64 + pm] : a[16 + j];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(xempty_bar);
           float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
+            const float got =
+                __shfl_xor_sync(0xffffffffu, is_gate ? a[16 + j] : a[j], 16);
+            const float g = is_gate ? a[j] : got;
+            const float u = is_gate ? got : a[16 + j];
             const float sx = __shfl_sync(0xffffffffu, sx_l, c0 + j);
-            const float gg = g[j] * sx * swg;
-            const float uu = u[j] * sx * swu;
+            const float gg = g * sx * swg;
+            const float uu = u * sx * swu;
             hv[j] = __fdividef(gg * uu, 1.0f + __expf(-gg));
           }
-          emit(ti.row0 + n0 + c0, ti.row0 + nvalid, ch - lane, hv);
+          // 32 tokens x this warp's 16 channels: one TMA store through shared
+          // memory ([token][channel]); a chunk crossing the tile's end is
+          // stored directly, so rows past it are never written
+          if (n0 + C::kChunk <= nvalid) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) obuf[(c0 + j) * 16 + (lane & 15)] = hv[j];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_out, ch - (lane & 15), ti.row0 + n0, smem_u32(obuf));
+              bulk_commit();
+            }
+          } else {
+            float* o = out + (int64_t)(ti.row0 + n0 + c0) * N + ch;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (n0 + c0 + j < nvalid) o[(int64_t)j * N] = hv[j];
+          }
         }
       } else {
         const int ch = ti.ctile * 256 + (int)rank * 128 + m;
@@ -581,7 +652,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
         else mbar_arrive_cluster(map_to_rank(acce_bar(ab), 0));
       }
     }
-    if (lane == 0) bulk_wait_all();   // this warp's output stores are complete
+    if (lane == 0) bulk_wait_all();   // this warp's TMA stores are complete
   }
 
   // ---------------- tear-down ----------------
@@ -594,22 +665,26 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16>::kThreadsT, 1)
   }
 }
 
-template <int BN, bool GATEUP, bool OUT16 = false>
+template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false>
 int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
              const uint8_t* W, const float* w_scale, const int32_t* offsets,
              int groups, int N, int K, float* out, cudaStream_t stream, bool pdl,
-             __half* out16 = nullptr, float* row_scale = nullptr,
+             int balanced, __half* out16 = nullptr, float* row_scale = nullptr,
              const float* w_bound = nullptr) {
-  using C = PairCfg<BN, GATEUP, OUT16>;
+  using C = PairCfg<BN, GATEUP, OUT16, WIDE>;
   CUtensorMap tm_w, tm_a;
-  const int64_t w_rows = (int64_t)groups * (GATEUP ? 2 : 1) * N;
-  if (!make_tmap(&tm_w, W, w_rows, K, 64)) return -3;   // 64-row weight parts
+  if (GATEUP) {   // one box: 64 channels' gate and up rows, interleaved by 16
+    if (!make_tmap_gateup_interleaved(&tm_w, W, groups, N, K)) return -3;
+  } else if (!make_tmap(&tm_w, W, (int64_t)groups * N, K, 64)) {   // 64-row parts
+    return -3;
+  }
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
   CUtensorMap tm_out;
-  const bool made = OUT16 ? make_tmap_out(&tm_out, out16, a_rows, N, C::kOutRows, 32, 2)
-                          : make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, 32, 4);
+  const bool made = OUT16
+                        ? make_tmap_out(&tm_out, out16, a_rows, N, C::kOutRows, 32, 2)
+                        : make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, C::kOutCols, 4);
   if (!made) return -3;
-  auto kern = grouped_gemm_pair_kernel<BN, GATEUP, OUT16>;
+  auto kern = grouped_gemm_pair_kernel<BN, GATEUP, OUT16, WIDE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
@@ -634,7 +709,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   cfg.numAttrs = pdl ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, tm_w, tm_a, tm_out, a_scale, w_scale, offsets,
-                         groups, N, K, out, out16, row_scale, w_bound,
+                         groups, N, K, out, out16, row_scale, w_bound, balanced,
                          device_error_word());
   return e == cudaSuccess ? 0 : -3;
 }
@@ -650,18 +725,22 @@ int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
                              const float* w_scale, const int32_t* offsets,
                              int groups, int N, int K, float* out, int bn,
                              cudaStream_t stream, bool pdl) {
+  const int bal = balanced_tiles();
   if (kind == 0) {
+    if (bn > 256)   // wide tiles are always balanced
+      return run_pair<512, true, false, true>(A, a_scale, a_rows, W, w_scale, offsets,
+                                              groups, N, K, out, stream, pdl, 1);
     if (bn <= 128)
       return run_pair<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                 K, out, stream, pdl);
+                                 K, out, stream, pdl, bal);
     return run_pair<256, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
-                               out, stream, pdl);
+                               out, stream, pdl, bal);
   }
   if (bn <= 128)
     return run_pair<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                K, out, stream, pdl);
+                                K, out, stream, pdl, bal);
   return run_pair<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
-                              out, stream, pdl);
+                              out, stream, pdl, bal);
 }
 
 int launch_grouped_gemm_pair_down_f16(const uint8_t* A, const float* a_scale,
@@ -671,11 +750,13 @@ int launch_grouped_gemm_pair_down_f16(const uint8_t* A, const float* a_scale,
                                       int K, uint16_t* y16, float* row_scale, int bn,
                                       cudaStream_t stream, bool pdl) {
   __half* o = reinterpret_cast<__half*>(y16);
+  const int bal = balanced_tiles();
   if (bn <= 128)
     return run_pair<128, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups,
-                                      N, K, nullptr, stream, pdl, o, row_scale, w_bound);
+                                      N, K, nullptr, stream, pdl, bal, o, row_scale,
+                                      w_bound);
   return run_pair<256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                    K, nullptr, stream, pdl, o, row_scale, w_bound);
+                                    K, nullptr, stream, pdl, bal, o, row_scale, w_bound);
 }
 
 }  // namespace moe

@@ -679,6 +679,25 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int K,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_gateup_interleaved(CUtensorMap* map, const void* W, int groups, int N,
+                                  int K) {
+  auto fn = encode_fn();
+  if (fn == nullptr || N % 64 != 0) return false;
+  // dims (innermost first): K bytes, 16 rows of a channel block, gate / up,
+  // channel blocks, experts; a box walks them in that order, so its 128
+  // rows arrive as [block][gate, up][16 rows]
+  const cuuint64_t dims[5] = {(cuuint64_t)K, 16, 2, (cuuint64_t)(N / 16),
+                              (cuuint64_t)groups};
+  const cuuint64_t strides[4] = {(cuuint64_t)K, (cuuint64_t)N * K, (cuuint64_t)16 * K,
+                                 (cuuint64_t)2 * N * K};
+  const cuuint32_t box[5] = {(cuuint32_t)kBK, 16, 2, 4, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(W), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_out(CUtensorMap* map, void* base, int64_t rows, int cols,
                    int box_rows, int box_cols, int elem_bytes) {
   auto fn = encode_fn();
@@ -717,6 +736,23 @@ int cta_pair_mode() {
   return mode;
 }
 
+int wide_tiles_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("MOE_GEMM_WIDE");
+    if (v == nullptr || v[0] == '\0') return -1;
+    return v[0] == '1' ? 1 : v[0] == '0' ? 0 : -1;
+  }();
+  return mode;
+}
+
+int balanced_tiles() {
+  static const int mode = [] {
+    const char* v = std::getenv("MOE_GEMM_BALANCED");
+    return (v != nullptr && v[0] == '0') ? 0 : 1;
+  }();
+  return mode;
+}
+
 int down_pair_mode() {
   static const int mode = [] {
     const char* v = std::getenv("MOE_GEMM_DOWN_PAIR");
@@ -745,10 +781,16 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   const bool pair = pair_mode == 1   ? avg > 64
                     : pair_mode == 0 ? false
                                      : kind == 0 && avg >= 256;
+  // Tiles of up to 512 tokens (two MMAs per K step, one accumulator buffer)
+  // move 25-30% fewer operand bytes per FLOP, but their epilogue cannot
+  // overlap the next tile's MMAs: on GB300 they tie at 320 rows per expert
+  // (T=16384 gate/up 1.384 ms either way) and lose at 512 (prefill 0.634 ->
+  // 0.721 ms). MOE_GEMM_WIDE=1 turns them on above 256 rows per expert.
+  const bool wide = kind == 0 && avg > 256 && wide_tiles_mode() == 1;
   if (pair && grouped_gemm_pair_supported(kind, N))
     return launch_grouped_gemm_pair(kind, A, a_scale, a_rows, W, w_scale, offsets,
-                                    groups, N, K, out, avg <= 128 ? 128 : 256,
-                                    stream, pdl);
+                                    groups, N, K, out,
+                                    wide ? 512 : avg <= 128 ? 128 : 256, stream, pdl);
   if (kind == 0) {
     if (avg <= 16) {
       // fewer tiles than two per SM: two CTAs an SM, so no SM streams a

@@ -348,6 +348,9 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
     (3, [400, 5, 90], 768, 384, 100),                # BN 128; down: 256-channel tiles
     # BN 16 with more possible tiles than two per SM: gate/up one CTA an SM
     (40, [3, 1, 4, 1, 5, 9, 2, 6, 5, 3] * 4, 512, 256, 0),
+    # CTA pairs, balanced token tiles (rows per tile): 160+160, 160+97,
+    # 256+256+161, 33 (MMA 64), 256+194, 96
+    (6, [320, 257, 673, 33, 450, 96], 256, 512, 0),
 ])
 def test_grouped_gemm(gateup, G, counts, N, K, hint):
     aq, sa, wq, sw, offs = _grouped_case(G, counts, N, K, gateup,
@@ -487,21 +490,31 @@ def test_combine_f16(T, k, D, shared):
     assert np.all(np.abs(got - ref) <= bound + 1e-30)
 
 
-@pytest.mark.parametrize("mode", ["1", "0"])
-def test_grouped_gemm_cta_pair_variant(mode):
+@pytest.mark.parametrize("switches", [
+    {"MOE_GEMM_CTA_PAIR": "1"},
+    {"MOE_GEMM_CTA_PAIR": "1", "MOE_GEMM_BALANCED": "0", "MOE_GEMM_WIDE": "0"},
+    {"MOE_GEMM_CTA_PAIR": "0"},
+    {"MOE_GEMM_WIDE": "1"},
+    {"MOE_GEMM_WIDE": "0"},
+], ids=["pair", "pair-unbalanced", "single", "wide", "no-wide"])
+def test_grouped_gemm_cta_pair_variant(switches):
     """The wide-tile cases with the kernel choice forced, in a child process:
     MOE_GEMM_CTA_PAIR=1 runs the CTA-pair (cta_group::2) kernel for every
     shape with more than 64 rows per expert (the down projection included),
     =0 the single-CTA kernel everywhere (the gate/up shapes that otherwise
-    take the pair)."""
+    take the pair). MOE_GEMM_BALANCED=0 cuts the pair kernel's token tiles
+    into full ones and a partial tail instead of equal widths.
+    MOE_GEMM_WIDE=1 / =0 turns the 512-token gate/up tiles (two MMAs per K
+    step) on / off above 256 rows per expert."""
     import os
     import subprocess
     import sys
-    env = dict(os.environ, MOE_GEMM_CTA_PAIR=mode)
+    env = dict(os.environ, **switches)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     cmd = [sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m",
            "gpu", os.path.join(root, "tests", "test_gpu_ops.py"), "-k",
-           "test_grouped_gemm and (counts2 or counts3 or counts4 or counts5 or counts6)"]
+           "test_grouped_gemm and (counts2 or counts3 or counts4 or counts5 or counts6 "
+           "or counts10)"]
     r = subprocess.run(cmd, env=env, cwd=root, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
