@@ -188,7 +188,9 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t pari
 // unequal tile costs no longer leave some SMs with more work than others.
 //
 // One scheduler thread per CTA publishes the sequence to the CTA's roles
-// through a small ring in shared memory; -1 ends it. The next tile is
+// through a small ring in shared memory, each tile with its decoded
+// coordinates (expert, channel tile, rows), so that no role decodes a tile
+// on its own critical path; -1 ends it. The next tile is
 // requested only when the first producer has taken the last one, so a CTA
 // holds at most one tile in reserve beyond those in its pipeline. In a CTA
 // pair the leader requests, the response is multicast to both CTAs, and both
@@ -203,6 +205,7 @@ struct Sched {
   uint64_t resp_bar[2];        // a response landed (16 bytes expected)
   uint64_t resp_free[2];       // pair: the peer has read a response
   int tile[kRing];
+  TileInfo info[kRing];        // tile[i] decoded
 };
 
 // `consumers`: arrivals that free a ring slot (one per consuming thread or
@@ -251,10 +254,12 @@ __device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& x) {
 }
 
 // The scheduler thread. `first`: this CTA's (pair's) own tile; `cta_per_tile`:
-// 1, or 2 for CTA pairs; `rank`: rank in the pair (0 requests).
+// 1, or 2 for CTA pairs; `rank`: rank in the pair (0 requests); `decode`
+// maps a tile index to its TileInfo.
+template <typename Decode>
 __device__ inline void sched_run(Sched& sc, int first, int total, int cta_per_tile,
                                  uint32_t rank, volatile int* abort_flag,
-                                 unsigned* err) {
+                                 unsigned* err, Decode decode) {
   int slot = 0;
   uint32_t ph = 0;
   uint32_t resp_ph[2] = {0u, 0u}, free_ph[2] = {0u, 0u};
@@ -264,6 +269,7 @@ __device__ inline void sched_run(Sched& sc, int first, int total, int cta_per_ti
     if (!mbar_wait_bounded(smem_u32(&sc.empty[slot]), ph ^ 1u, abort_flag, err,
                            kErrTimeoutSched))
       return false;
+    if (t >= 0) sc.info[slot] = decode(t);
     *reinterpret_cast<volatile int*>(&sc.tile[slot]) = t;
     mbar_arrive(smem_u32(&sc.full[slot]));
     if (++slot == kRing) {
@@ -325,14 +331,16 @@ struct TileCursor {
   uint32_t phase = 0;
 };
 
-// Next tile for a role run by one thread (-1: no more, or a wait ran out).
-// `take` marks the first producer, whose taking releases the next request.
+// Next tile for a role run by one thread (-1: no more, or a wait ran out),
+// its coordinates in `ti`. `take` marks the first producer, whose taking
+// releases the next request.
 __device__ __forceinline__ int next_tile_thread(Sched& sc, TileCursor& c, bool take,
                                                 volatile int* abort_flag, unsigned* err,
-                                                unsigned code) {
+                                                unsigned code, TileInfo& ti) {
   if (!mbar_wait_bounded(smem_u32(&sc.full[c.slot]), c.phase, abort_flag, err, code))
     return -1;
   const int t = *reinterpret_cast<volatile int*>(&sc.tile[c.slot]);
+  if (t >= 0) ti = sc.info[c.slot];
   mbar_arrive(smem_u32(&sc.empty[c.slot]));
   if (take && t >= 0) mbar_arrive(smem_u32(&sc.taken));
   if (++c.slot == kRing) {
@@ -345,9 +353,10 @@ __device__ __forceinline__ int next_tile_thread(Sched& sc, TileCursor& c, bool t
 // Next tile for a role run by a whole warp (the same answer in every lane).
 __device__ __forceinline__ int next_tile_warp(Sched& sc, TileCursor& c,
                                               volatile int* abort_flag, unsigned* err,
-                                              unsigned code) {
+                                              unsigned code, TileInfo& ti) {
   if (!warp_wait(smem_u32(&sc.full[c.slot]), c.phase, abort_flag, err, code)) return -1;
   const int t = *reinterpret_cast<volatile int*>(&sc.tile[c.slot]);
+  if (t >= 0) ti = sc.info[c.slot];
   __syncwarp();
   if (lane_id() == 0) mbar_arrive(smem_u32(&sc.empty[c.slot]));
   if (++c.slot == kRing) {
@@ -405,6 +414,10 @@ int balanced_tiles();
 // MOE_GEMM_WIDE: 1 runs gate/up CTA-pair tiles of up to 512 tokens (two MMAs
 // per K step) above 256 rows per expert, 0 never; unset (-1): the rule.
 int wide_tiles_mode();
+
+// MOE_GEMM_PAIR_BN=128 / 256: token tile of the CTA-pair kernels when they
+// run; unset (0): from the rows per expert.
+int pair_bn_mode();
 
 }  // namespace gemm
 }  // namespace moe

@@ -187,7 +187,7 @@ struct PairCfg {
   static constexpr int kOutBytes =
       4 * (GATEUP ? kEpiSets : 1) * kOutRows * kOutCols * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kOutBytes +
-                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+                                    kNumBars * 8 + 16 + 8 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -254,6 +254,8 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
+  // the group offsets, copied: tile decoding reads only shared memory
+  int* soff = prefix + (kMaxGroups + 1);
   __shared__ int warp_tot[C::kThreadsT / 32 + 1];
   __shared__ Sched sched;
 
@@ -314,9 +316,13 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
     int run = base + incl - local;
     for (int g = g0; g < g0 + per && g < groups; ++g) {
       prefix[g] = run;
+      soff[g] = offsets[g];
       run += ((offsets[g + 1] - offsets[g] + BN - 1) / BN) * n_ctiles;
     }
-    if (threadIdx.x == C::kThreadsT - 1) prefix[groups] = base + incl;
+    if (threadIdx.x == C::kThreadsT - 1) {
+      prefix[groups] = base + incl;
+      soff[groups] = offsets[groups];
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -327,8 +333,8 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
   // an expert's rows in ceil(rows / BN) tiles of BN rows (the last partial),
   // or, balanced, of equal widths (multiples of 32)
   auto decode = [&](int tile) {
-    return balanced ? decode_tile_balanced(tile, prefix, groups, offsets, BN)
-                    : decode_tile(tile, prefix, groups, offsets, BN);
+    return balanced ? decode_tile_balanced(tile, prefix, groups, soff, BN)
+                    : decode_tile(tile, prefix, groups, soff, BN);
   };
 
   // down: this CTA's first weight row of a tile
@@ -347,7 +353,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
   if (warp == kSchedWarp) {
     // ---------------- tile scheduler (both CTAs; the leader requests) ----------------
     if (lane == 0)
-      sched_run(sched, first_tile, total_tiles, 2, rank, abort_flag, err);
+      sched_run(sched, first_tile, total_tiles, 2, rank, abort_flag, err, decode);
   } else if (box >= 0) {
     // ---------------- TMA producers (both CTAs): box `box` of every stage ----------------
     const bool weight_box = box < C::kWBoxes;
@@ -405,11 +411,11 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
       pdl_launch_dependents();
       TileCursor cur;
       for (bool first = true; ok; first = false) {
+        TileInfo ti;
         const int tile = next_tile_thread(sched, cur, box == 0 && rank == 0, abort_flag,
-                                          err, kErrTimeoutProducer);
+                                          err, kErrTimeoutProducer, ti);
         if (tile < 0) break;
         const bool pre = first && npre > 0 && tile == first_tile;
-        const TileInfo ti = pre ? t0 : decode(tile);
         for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!wait_cluster_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                     kErrTimeoutProducer)) {
@@ -457,7 +463,9 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
       bool ok = true;
       TileCursor cur;
       for (; ok; ++it) {
-        const int tile = next_tile_thread(sched, cur, false, abort_flag, err, kErrTimeoutMma);
+        TileInfo ti;
+        const int tile =
+            next_tile_thread(sched, cur, false, abort_flag, err, kErrTimeoutMma, ti);
         if (tile < 0) break;
         const int ab = it % C::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
                                   kErrTimeoutMma)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)(ab * BN);
-        const int n = pair_width(decode(tile));
+        const int n = pair_width(ti);
         const int n1 = min(n, 256), n2 = n - n1;   // n2 > 0: wide tiles only
         const uint32_t idesc = idesc_e4m3_f32(256, n1);
         const uint32_t idesc2 = idesc_e4m3_f32(256, n2 > 0 ? n2 : 64);
@@ -545,16 +553,28 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
     };
     TileCursor cur;
     for (; ok; ++it) {
-      const int tile = next_tile_warp(sched, cur, abort_flag, err, kErrTimeoutEpilogue);
+      TileInfo ti;
+      const int tile =
+          next_tile_warp(sched, cur, abort_flag, err, kErrTimeoutEpilogue, ti);
       if (tile < 0) break;
       const int ab = it % C::kAccBufs;
       const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
+      const int nvalid = tile_rows(ti);
+      // gate/up: this thread's channel, its two weight scales and the first
+      // chunk's token scales, loaded while the MMAs finish
+      const bool is_gate = lane < 16;
+      const int ch_gu = ti.ctile * 128 + (int)rank * 64 + q * 16 + (lane & 15);
+      float swg = 0.f, swu = 0.f, sx_next = 0.f;
+      if constexpr (GATEUP) {
+        swg = w_scale[(int64_t)ti.group * 2 * N + ch_gu];
+        swu = w_scale[(int64_t)ti.group * 2 * N + N + ch_gu];
+        const int nfirst = C::kChunk * eset;
+        sx_next = nfirst + lane < nvalid ? a_scale[ti.row0 + nfirst + lane] : 0.f;
+      }
       if (!warp_wait_cluster(accf_bar(ab), acc_ph, abort_flag, err,
                              kErrTimeoutEpilogue))
         break;
       tc_fence_after_sync();
-      const TileInfo ti = decode(tile);
-      const int nvalid = tile_rows(ti);
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN);
       if (GATEUP) {
@@ -564,17 +584,12 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
         // thread trades its columns 16-31 for its up partner's (lane + 16)
         // columns 0-15, one shuffle each, so every thread finishes 16
         // outputs of its channel.
-        const bool is_gate = lane < 16;
-        const int ch = ti.ctile * 128 + (int)rank * 64 + q * 16 + (lane & 15);
-        const float swg = w_scale[(int64_t)ti.group * 2 * N + ch];
-        const float swu = w_scale[(int64_t)ti.group * 2 * N + N + ch];
+        const int ch = ch_gu;
         const int c0 = is_gate ? 0 : 16;           // this thread's columns
         // token scales of a chunk (lane = column), loaded one chunk ahead;
         // with two epilogue sets, set e takes chunks e, e + 2, ...
         constexpr int kStep = C::kChunk * C::kEpiSets;
-        const int nfirst = C::kChunk * eset;
-        float sx_next = nfirst + lane < nvalid ? a_scale[ti.row0 + nfirst + lane] : 0.f;
-        for (int n0 = nfirst; n0 < nvalid; n0 += kStep) {
+        for (int n0 = C::kChunk * eset; n0 < nvalid; n0 += kStep) {
           const float sx_l = sx_next;
           if (n0 + kStep < nvalid)
             sx_next = n0 + kStep + lane < nvalid ? a_scale[ti.row0 + n0 + kStep + lane] : 0.f;

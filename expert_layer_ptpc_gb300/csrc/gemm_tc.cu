@@ -87,7 +87,7 @@ struct Cfg {
   static constexpr bool kStagedOut = !kPacked && BN >= 64;
   static constexpr int kOutBytes = kStagedOut ? 4 * 32 * 32 * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStage + kXBytes + kOutBytes +
-                                    kNumBars * 8 + 16 + 4 * (kMaxGroups + 1) + 64;
+                                    kNumBars * 8 + 16 + 8 * (kMaxGroups + 1) + 64;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(MINB == 1 || (MINB == 2 && 2 * (kSmemBytes + 1024) <= 233472 &&
                               2 * kTmemCols <= 512),
@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* prefix = reinterpret_cast<int*>(tmem_holder + 4);   // groups + 1
+  // the group offsets, copied: tile decoding reads only shared memory
+  int* soff = prefix + (kMaxGroups + 1);
   __shared__ int warp_tot[C::kThreadsT / 32 + 1];
   __shared__ Sched sched;
 
@@ -193,9 +195,13 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
     int run = base + incl - local;
     for (int g = g0; g < g0 + per && g < groups; ++g) {
       prefix[g] = run;
+      soff[g] = offsets[g];
       run += ((offsets[g + 1] - offsets[g] + BN - 1) / BN) * n_ctiles;
     }
-    if (threadIdx.x == C::kThreadsT - 1) prefix[groups] = base + incl;
+    if (threadIdx.x == C::kThreadsT - 1) {
+      prefix[groups] = base + incl;
+      soff[groups] = offsets[groups];
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -212,7 +218,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
   if (warp == kSchedWarp) {
     // ---------------- tile scheduler ----------------
     // (touches nothing the previous kernel writes)
-    if (lane == 0) sched_run(sched, blockIdx.x, total_tiles, 1, 0, abort_flag, err);
+    if (lane == 0)
+      sched_run(sched, blockIdx.x, total_tiles, 1, 0, abort_flag, err, [&](int t) {
+        return decode_tile(t, prefix, groups, soff, BN);
+      });
   } else if (box >= 0) {
     // ---------------- TMA producers: box `box` of every stage ----------------
     const bool weight_box = box < C::kWBoxes;
@@ -263,7 +272,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
       int npre = 0;
       TileInfo t0{};
       if (weight_box && first < total_tiles) {
-        t0 = decode_tile(first, prefix, groups, offsets, BN);
+        t0 = decode_tile(first, prefix, groups, soff, BN);
         npre = kblocks < C::kStages ? kblocks : C::kStages;
         for (int kb = 0; kb < npre; ++kb) {   // fresh ring: stage kb, phase 0
           mbar_arrive_expect_tx(full_bar(kb), bytes);
@@ -279,11 +288,11 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
       pdl_launch_dependents();
       TileCursor cur;
       for (bool first_tile = true; ok; first_tile = false) {
+        TileInfo ti;
         const int tile = next_tile_thread(sched, cur, box == 0, abort_flag, err,
-                                          kErrTimeoutProducer);
+                                          kErrTimeoutProducer, ti);
         if (tile < 0) break;
         const bool pre = first_tile && npre > 0 && tile == first;
-        const TileInfo ti = pre ? t0 : decode_tile(tile, prefix, groups, offsets, BN);
         for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                  kErrTimeoutProducer)) {
@@ -325,8 +334,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
       bool ok = true;
       TileCursor cur;
       for (; ok; ++it) {
+        TileInfo ti;
         const int tile = next_tile_thread(sched, cur, false, abort_flag, err,
-                                          kErrTimeoutMma);
+                                          kErrTimeoutMma, ti);
         if (tile < 0) break;
         const int ab = it % C::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
@@ -339,7 +349,6 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
         // the smallest width (halving BN, not below 32) that covers its rows.
         int n_mma = BN;
         {
-          const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
           const int nvalid = ti.row_end - ti.row0;
           while (n_mma >= 64 && n_mma / 2 >= nvalid) n_mma /= 2;
         }
@@ -426,14 +435,15 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
     bool ok = true;
     TileCursor cur;
     for (; ok; ++it) {
-      const int tile = next_tile_warp(sched, cur, abort_flag, err, kErrTimeoutEpilogue);
+      TileInfo ti;
+      const int tile =
+          next_tile_warp(sched, cur, abort_flag, err, kErrTimeoutEpilogue, ti);
       if (tile < 0) break;
       const int ab = it % C::kAccBufs;
       const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
       if (!warp_wait(accf_bar(ab), acc_ph, abort_flag, err, kErrTimeoutEpilogue))
         break;
       tc_fence_after_sync();
-      const TileInfo ti = decode_tile(tile, prefix, groups, offsets, BN);
       const int nvalid = min(BN, ti.row_end - ti.row0);
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
@@ -745,6 +755,15 @@ int wide_tiles_mode() {
   return mode;
 }
 
+int pair_bn_mode() {
+  static const int bn = [] {
+    const char* v = std::getenv("MOE_GEMM_PAIR_BN");
+    const int b = v != nullptr ? std::atoi(v) : 0;
+    return b == 128 || b == 256 ? b : 0;
+  }();
+  return bn;
+}
+
 int balanced_tiles() {
   static const int mode = [] {
     const char* v = std::getenv("MOE_GEMM_BALANCED");
@@ -790,7 +809,11 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   if (pair && grouped_gemm_pair_supported(kind, N))
     return launch_grouped_gemm_pair(kind, A, a_scale, a_rows, W, w_scale, offsets,
                                     groups, N, K, out,
-                                    wide ? 512 : avg <= 128 ? 128 : 256, stream, pdl);
+                                    wide              ? 512
+                                    : pair_bn_mode()  ? pair_bn_mode()
+                                    : avg <= 128      ? 128
+                                                      : 256,
+                                    stream, pdl);
   if (kind == 0) {
     if (avg <= 16) {
       // fewer tiles than two per SM: two CTAs an SM, so no SM streams a
@@ -832,9 +855,9 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
   const int dm = down_pair_mode() >= 0 ? down_pair_mode() : cta_pair_mode();
   const bool pair = dm == 1 ? avg > 64 : dm == 0 ? false : avg >= 512;
   if (pair && grouped_gemm_pair_supported(1, N))
-    return launch_grouped_gemm_pair_down_f16(A, a_scale, a_rows, W, w_scale, w_bound,
-                                             offsets, groups, N, K, y16, row_scale,
-                                             avg <= 128 ? 128 : 256, stream, pdl);
+    return launch_grouped_gemm_pair_down_f16(
+        A, a_scale, a_rows, W, w_scale, w_bound, offsets, groups, N, K, y16, row_scale,
+        pair_bn_mode() ? pair_bn_mode() : avg <= 128 ? 128 : 256, stream, pdl);
   __half* o = reinterpret_cast<__half*>(y16);
 #define MOE_DOWN16(bn, minb)                                                             \
   return run<bn, 128, false, true, minb>(A, a_scale, a_rows, W, w_scale, offsets, groups, \
