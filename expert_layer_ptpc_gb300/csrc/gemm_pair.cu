@@ -149,19 +149,23 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false>
 struct PairCfg {
   static constexpr int kHalfB = BN / 2;                  // token rows per CTA
-  // TMA boxes of one stage (per CTA): the weights (gate/up: one 128-row 5D
-  // box; down: two 64-row boxes), then 32-row (wide tiles: 64-row) token
-  // boxes; one producer warp per box
-  static constexpr int kWBoxes = GATEUP ? 1 : 2;
-  static constexpr int kWBoxRows = 128 / kWBoxes;
-  static constexpr int kTBoxRows = WIDE ? 64 : 32;
+  // TMA boxes of one stage (per CTA): the weights in one 128-row box
+  // (gate/up: the 5D interleaving box), then 64-row token boxes.
+  static constexpr int kWBoxes = 1;
+  static constexpr int kWBoxRows = 128;
+  static constexpr int kTBoxRows = kHalfB % 64 == 0 ? 64 : kHalfB;   // BN 192: one 96-row box
   static constexpr int kTBoxes = kHalfB / kTBoxRows;
   static constexpr int kBoxes = kWBoxes + kTBoxes;
-  static_assert(kBoxes <= kMaxBoxes, "one producer warp per box");
   static constexpr int kATile = 128 * kBK;               // this CTA's 128 MMA rows
   static constexpr int kBTile = kHalfB * kBK;
   static constexpr int kStage = kATile + kBTile;
   static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
+  // Producer warps per box: one thread issues a TMA copy about every 0.35 us
+  // on GB300, so when the warps allow, two warps share each box and take
+  // alternate stages (warp 2b: even stages, 2b + 1: odd ones). An even
+  // stage count keeps each ring slot with one warp of a box.
+  static constexpr int kPar = (2 * kBoxes <= kMaxBoxes && kStages % 2 == 0) ? 2 : 1;
+  static_assert(kBoxes * kPar <= kMaxBoxes, "producer warps");
   static constexpr int kAccBufs = 2 * BN <= 512 ? 2 : 1;
   static constexpr int kTmemCols = pow2_at_least(kAccBufs * BN);
   static constexpr int kChunk = 32;                      // epilogue columns per pass
@@ -205,19 +209,19 @@ __device__ __forceinline__ int pair_width(const TileInfo& ti) {
   return n <= 256 ? n : 256 + max(64, n - 256);
 }
 
-// Token box t of a CTA (rank) in a tile of MMA width n: whether it is
-// loaded, the row of the stage's token tile it fills and the first token row
-// it copies. Narrow tiles: the CTA's n/2 tokens in 32-row boxes. Wide tiles
-// (64-row boxes): boxes 0-1 fill rows 0-127 with the CTA's half of the first
-// N1 tokens, boxes 2-3 rows 128-255 with its half of the next N2.
-template <bool WIDE>
+// Token box t (ROWS rows) of a CTA (rank) in a tile of MMA width n: whether
+// it is loaded, the row of the stage's token tile it fills and the first
+// token row it copies. Narrow tiles: the CTA's n/2 tokens. Wide tiles
+// (64-row boxes): boxes 0-1 fill rows 0-127 with the CTA's half of the
+// first N1 tokens, boxes 2-3 rows 128-255 with its half of the next N2.
+template <bool WIDE, int ROWS>
 __device__ __forceinline__ bool token_box(int t, int n, int row0, int rank, int& smem_row,
                                           int& token_row) {
   if constexpr (!WIDE) {
     const int half = n / 2;
-    smem_row = t * 32;
-    token_row = row0 + rank * half + t * 32;
-    return t * 32 < half;
+    smem_row = t * ROWS;
+    token_row = row0 + rank * half + t * ROWS;
+    return t * ROWS < half;
   } else {
     const int n1 = min(n, 256), n2 = n - n1;
     if (t < 2) {
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
     }
     mbar_init(drain_bar, 1);
     // ring consumers: each producer, each epilogue warp, the leader's MMA issuer
-    sched_init(sched, C::kBoxes + 4 * C::kEpiSets + (rank == 0 ? 1 : 0));
+    sched_init(sched, C::kBoxes * C::kPar + 4 * C::kEpiSets + (rank == 0 ? 1 : 0));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -349,13 +353,16 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
     else tma_load_2d_pair(dst, tm, x, y, map_to_rank(full_bar(s), 0), pol);
   };
 
-  const int box = producer_box(warp);
+  const int pwarp = producer_box(warp);             // producer warp index, or -1
+  const int box = pwarp >= 0 ? pwarp / C::kPar : -1;
+  const int par = pwarp >= 0 ? pwarp % C::kPar : 0;  // the stages it takes
   if (warp == kSchedWarp) {
     // ---------------- tile scheduler (both CTAs; the leader requests) ----------------
     if (lane == 0)
       sched_run(sched, first_tile, total_tiles, 2, rank, abort_flag, err, decode);
   } else if (box >= 0) {
     // ---------------- TMA producers (both CTAs): box `box` of every stage ----------------
+    // (of every kPar-th stage, from stage `par` on)
     const bool weight_box = box < C::kWBoxes;
     if (lane == 0 && box < C::kBoxes) {
       const uint64_t pol = weight_box ? l2_policy_evict_normal() : l2_policy_evict_last();
@@ -368,11 +375,11 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
           tma_load_5d(stage_a(s), &tm_w, x, (ti.ctile * 128 + (int)rank * 64) / 16,
                       ti.group, rank == 0 ? full_bar(s) : map_to_rank(full_bar(s), 0),
                       pol, rank != 0);
-        } else if (weight_box) {    // down rows: 64-row halves
-          load(stage_a(s) + box * 64 * kBK, &tm_w, x, weight_row(ti) + box * 64, s, pol);
+        } else if (weight_box) {    // down: this CTA's 128 rows
+          load(stage_a(s), &tm_w, x, weight_row(ti), s, pol);
         } else {                    // rows of this CTA's half of the token tile
           int srow, trow;
-          if (token_box<WIDE>(box - C::kWBoxes, pair_width(ti), ti.row0, (int)rank, srow,
+          if (token_box<WIDE, C::kTBoxRows>(box - C::kWBoxes, pair_width(ti), ti.row0, (int)rank, srow,
                               trow))
             load(stage_b(s) + srow * kBK, &tm_a, x, trow, s, pol);
         }
@@ -381,15 +388,17 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
       auto expect = [&](int s, const TileInfo& ti) {
         if (rank != 0) return;
         int srow, trow;
-        const bool used = weight_box || token_box<WIDE>(box - C::kWBoxes, pair_width(ti),
+        const bool used = weight_box || token_box<WIDE, C::kTBoxRows>(box - C::kWBoxes, pair_width(ti),
                                                         ti.row0, 0, srow, trow);
         mbar_arrive_expect_tx(full_bar(s), used ? 2 * bytes : 0u);
       };
       int last_phase[C::kStages];
 #pragma unroll
       for (int i = 0; i < C::kStages; ++i) last_phase[i] = -1;
-      int s = 0;
-      uint32_t ph = 0;
+      // q numbers this CTA's stages in order (tile by tile, K block by K
+      // block); stage q fills slot q % kStages in phase (q / kStages) & 1,
+      // and this warp issues the stages with q % kPar == par
+      uint32_t q = 0;
       bool ok = true;
       // weights and the tile map do not depend on the previous kernel
       int npre = 0;
@@ -397,26 +406,28 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
       if (weight_box && first_tile < total_tiles) {
         t0 = decode(first_tile);
         npre = kblocks < C::kStages ? kblocks : C::kStages;
-        for (int kb = 0; kb < npre; ++kb) {
+        for (int kb = par; kb < npre; kb += C::kPar) {   // fresh ring: phase 0
           expect(kb, t0);
           issue(kb, kb, t0);
 #pragma unroll
           for (int i = 0; i < C::kStages; ++i)
             if (i == kb) last_phase[i] = 0;
         }
-        s = npre % C::kStages;
-        ph = npre == C::kStages ? 1u : 0u;
+        q = (uint32_t)npre;
       }
       pdl_wait();
       pdl_launch_dependents();
       TileCursor cur;
       for (bool first = true; ok; first = false) {
         TileInfo ti;
-        const int tile = next_tile_thread(sched, cur, box == 0 && rank == 0, abort_flag,
-                                          err, kErrTimeoutProducer, ti);
+        const int tile = next_tile_thread(sched, cur, box == 0 && par == 0 && rank == 0,
+                                          abort_flag, err, kErrTimeoutProducer, ti);
         if (tile < 0) break;
         const bool pre = first && npre > 0 && tile == first_tile;
-        for (int kb = pre ? npre : 0; kb < kblocks; ++kb) {
+        for (int kb = pre ? npre : 0; kb < kblocks; ++kb, ++q) {
+          if ((int)(q % C::kPar) != par) continue;
+          const int s = (int)(q % C::kStages);
+          const uint32_t ph = (q / C::kStages) & 1u;
           if (!wait_cluster_bounded(empty_bar(s), ph ^ 1, abort_flag, err,
                                     kErrTimeoutProducer)) {
             ok = false;
@@ -427,10 +438,6 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
 #pragma unroll
           for (int i = 0; i < C::kStages; ++i)
             if (i == s) last_phase[i] = (int)ph;
-          if (++s == C::kStages) {
-            s = 0;
-            ph ^= 1;
-          }
         }
       }
       // drain: this CTA's copies have landed before its memory is released.
@@ -690,7 +697,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
   CUtensorMap tm_w, tm_a;
   if (GATEUP) {   // one box: 64 channels' gate and up rows, interleaved by 16
     if (!make_tmap_gateup_interleaved(&tm_w, W, groups, N, K)) return -3;
-  } else if (!make_tmap(&tm_w, W, (int64_t)groups * N, K, 64)) {   // 64-row parts
+  } else if (!make_tmap(&tm_w, W, (int64_t)groups * N, K, C::kWBoxRows)) {
     return -3;
   }
   if (!make_tmap(&tm_a, A, a_rows, K, C::kTBoxRows)) return -3;
@@ -745,6 +752,9 @@ int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
     if (bn > 256)   // wide tiles are always balanced
       return run_pair<512, true, false, true>(A, a_scale, a_rows, W, w_scale, offsets,
                                               groups, N, K, out, stream, pdl, 1);
+    if (bn == 192)
+      return run_pair<192, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
+                                 out, stream, pdl, bal);
     if (bn <= 128)
       return run_pair<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
                                  K, out, stream, pdl, bal);

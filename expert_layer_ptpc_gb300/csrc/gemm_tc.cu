@@ -759,7 +759,7 @@ int pair_bn_mode() {
   static const int bn = [] {
     const char* v = std::getenv("MOE_GEMM_PAIR_BN");
     const int b = v != nullptr ? std::atoi(v) : 0;
-    return b == 128 || b == 256 ? b : 0;
+    return b == 128 || b == 192 || b == 256 ? b : 0;
   }();
   return bn;
 }
@@ -800,6 +800,11 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
   const bool pair = pair_mode == 1   ? avg > 64
                     : pair_mode == 0 ? false
                                      : kind == 0 && avg >= 256;
+  // From 256 to 384 rows per expert an expert takes two balanced tiles of at
+  // most 192 tokens: a 28 KB stage leaves room for seven in the ring instead
+  // of six 32 KB ones, and the ring's copy latency bounds these tiles
+  // (uniform 320 rows per expert 1.156 -> 1.105 ms, T=16384 gate/up 1.289 ->
+  // 1.257 ms).
   // Tiles of up to 512 tokens (two MMAs per K step, one accumulator buffer)
   // move 25-30% fewer operand bytes per FLOP, but their epilogue cannot
   // overlap the next tile's MMAs: on GB300 they tie at 320 rows per expert
@@ -812,6 +817,8 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                                     wide              ? 512
                                     : pair_bn_mode()  ? pair_bn_mode()
                                     : avg <= 128      ? 128
+                                    : avg <= 256      ? 256
+                                    : avg <= 384      ? 192
                                                       : 256,
                                     stream, pdl);
   if (kind == 0) {

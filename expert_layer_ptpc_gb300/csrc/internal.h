@@ -109,7 +109,8 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                         bool pdl);
 
 // The CTA-pair (cta_group::2) grouped GEMM for wide token tiles (bn 128 or
-// 256); needs N divisible by 128 (gate/up) or 256 (down). Returns a status.
+// 256; gate/up also 192 and 512); needs N divisible by 128 (gate/up) or 256
+// (down). Returns a status.
 bool grouped_gemm_pair_supported(int kind, int N);
 int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
                              int64_t a_rows, const uint8_t* W,

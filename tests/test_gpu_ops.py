@@ -348,8 +348,9 @@ def _ref_grouped(aq, sa, wq, sw, offs, N, gateup):
     (3, [400, 5, 90], 768, 384, 100),                # BN 128; down: 256-channel tiles
     # BN 16 with more possible tiles than two per SM: gate/up one CTA an SM
     (40, [3, 1, 4, 1, 5, 9, 2, 6, 5, 3] * 4, 512, 256, 0),
-    # CTA pairs, balanced token tiles (rows per tile): 160+160, 160+97,
-    # 256+256+161, 33 (MMA 64), 256+194, 96
+    # CTA pairs, balanced token tiles of at most 192 rows (gate/up, 256 to
+    # 384 rows per expert on average): 160+160, 160+97, 192+192+192+97, 33
+    # (MMA 64), 160+160+130, 96
     (6, [320, 257, 673, 33, 450, 96], 256, 512, 0),
 ])
 def test_grouped_gemm(gateup, G, counts, N, K, hint):
