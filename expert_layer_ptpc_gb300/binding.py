@@ -71,6 +71,7 @@ _SIGNATURES = {
     "moe_workspace_status": (_I, [_P, _SZ, _P, ctypes.POINTER(ctypes.c_uint)]),
     "moe_forward_intermediates": (_I, [_P, _P, _SZ, _P]),
     "moe_forward_workspace_layout": (_I, [_P, _P, _P, _I]),
+    "moe_forward_single_launch": (_I, [_P, _I, _I]),
     "moe_debug_expire_wait": (_I, [_I, _P, _SZ, _P]),
     "moe_router_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_add_rmsnorm_quant": (_I, [_P, _P, _P, ctypes.c_float, _I64, _I, _P, _P, _I,
@@ -334,6 +335,16 @@ def make_dims(T, D, E, k, I, shared, renormalize=True):
 
 def moe_forward_workspace_size(dims):
     return load_library().moe_forward_workspace_size(ctypes.byref(dims))
+
+
+def moe_forward_single_launch(dims, router_weights=False, prenorm=False):
+    """Whether moe_forward with these dims runs as one cooperative launch."""
+    r = load_library().moe_forward_single_launch(ctypes.byref(dims),
+                                                 int(bool(router_weights)),
+                                                 int(bool(prenorm)))
+    if r < 0:
+        raise MoeError("moe_forward_single_launch", r)
+    return bool(r)
 
 
 def moe_forward_workspace_layout(dims):

@@ -1,6 +1,7 @@
 // C ABI of the PTPC-FP8 MoE layer: argument checks, workspace layout and the
 // chaining of the kernels on the caller's stream. Declared in moe_ptpc.h.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/moe_ptpc.h"
@@ -95,6 +96,21 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // first kForwardStatusBytes hold the forward's error word and the slot its
 // read-and-clear copies from (moe_workspace_status).
 constexpr size_t kForwardStatusBytes = 256;
+// the single-launch forward's grid barrier counter, inside the status bytes
+constexpr size_t kGridCounterOffset = 64;
+
+// MOE_SMALL_FORWARD=1 turns on the single-launch forward for a few tokens.
+// It is off by default: on GB300 at T=1 (D=4096, 512 experts, top-10 +
+// shared) it took 69-79 us against 53-56 us for the chained kernels, its
+// CUDA-core dot products and its 4-slot weight ring being slower than the
+// tensor-core GEMMs' streaming.
+int small_forward_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("MOE_SMALL_FORWARD");
+    return (v != nullptr && v[0] == '1') ? 1 : 0;
+  }();
+  return mode;
+}
 constexpr size_t kGuardBytes = 256;
 
 struct ForwardLayout {
@@ -145,6 +161,13 @@ ForwardLayout forward_layout(const moe_dims& d) {
   L.w_bound = take(G * 4);
   L.total = off;
   return L;
+}
+
+// Whether moe_forward runs the layer as one launch: at most kSfMaxTokens
+// tokens, given router logits, no pre-norm, y in fp32 and a supported shape.
+bool small_forward_applies(const moe_dims& d, bool router_weights, bool prenorm) {
+  return small_forward_mode() != 0 && !router_weights && !prenorm && !y_in_fp16(d) &&
+         small_forward_supported(d.T, d.D, d.E, d.k, d.I, d.shared);
 }
 
 int check_dims(const moe_dims* d) {
@@ -496,6 +519,24 @@ int forward_impl(const moe_dims* dims, const moe_prenorm* pre, const uint16_t* x
   auto* w_bound = static_cast<float*>(at(L.w_bound));
   const bool f16 = y_in_fp16(d);
 
+  // A batch of a few tokens on given logits: the whole layer in one
+  // cooperative launch (small_forward.cu), the same intermediates left in
+  // the workspace. Its grid barrier counts in the status region.
+  if (small_forward_applies(d, router_w != nullptr, pre != nullptr) && aligned16(s_gu) &&
+      aligned16(s_d)) {
+    auto* grid_counter = static_cast<unsigned*>(at(L.status + kGridCounterOffset));
+    if (cudaMemsetAsync(grid_counter, 0, sizeof(unsigned), stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    for (int i = 0; i <= 4; ++i) mark(i);
+    const int r = launch_small_forward(
+        d.T, d.D, d.E, d.k, d.I, d.shared, d.renormalize ? 1 : 0, x, router_logits, w_gu,
+        s_gu, w_d, s_d, shared_gate_w, out, ids, tw, counts, offsets, s2f, f2s, xq, sx,
+        gate, h, hq, sh, y, grid_counter, stream);
+    if (r != 0) return MOE_ERR_CUDA;
+    for (int i = 5; i <= 8; ++i) mark(i);
+    return MOE_OK;
+  }
+
   // Kernels after the first overlap their launch with the previous kernel's
   // tail (programmatic dependent launch); each orders itself with pdl_wait().
   // Event marks between the steps serialise them instead.
@@ -716,6 +757,14 @@ int moe_device_status(moe_stream_t stream, unsigned* detail) {
   unsigned* taken = global_word(1);
   if (word == nullptr || taken == nullptr) return MOE_ERR_CUDA;
   return take_status(word, taken, stream, detail);
+}
+
+int moe_forward_single_launch(const moe_dims* dims, int router_weights, int prenorm) {
+  const int st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  return dims->T > 0 && small_forward_applies(*dims, router_weights != 0, prenorm != 0)
+             ? 1
+             : 0;
 }
 
 int moe_workspace_status(void* ws, size_t ws_bytes, moe_stream_t stream,

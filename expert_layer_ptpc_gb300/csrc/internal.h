@@ -152,4 +152,21 @@ cudaError_t launch_combine_f16(const uint16_t* y16, const float* row_scale,
                                const float* shared_gate, uint16_t* out,
                                cudaStream_t stream, bool pdl);
 
+// The whole layer in one cooperative launch for batches of at most
+// kSfMaxTokens tokens on given router logits (small_forward.cu): routing,
+// permutation, x codes, gate/up + SwiGLU, one grid barrier, h codes, down +
+// combine, with every intermediate left where the multi-kernel path leaves
+// it. `grid_counter` must be zero. Returns a moe_status-like code (0 ok,
+// -1 unsupported shape, -3 launch failure).
+constexpr int kSfMaxTokens = 4;
+bool small_forward_supported(int T, int D, int E, int k, int I, int shared);
+int launch_small_forward(int T, int D, int E, int k, int I, int shared, int renormalize,
+                         const uint16_t* x, const float* logits, const uint8_t* w_gu,
+                         const float* s_gu, const uint8_t* w_d, const float* s_d,
+                         const uint16_t* gate_w, uint16_t* out, int32_t* ids, float* tw,
+                         int32_t* counts, int32_t* offsets, int32_t* s2f, int32_t* f2s,
+                         uint8_t* xq, float* sx, float* gate, float* h, uint8_t* hq,
+                         float* sh, float* y, unsigned* grid_counter,
+                         cudaStream_t stream);
+
 }  // namespace moe

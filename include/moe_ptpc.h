@@ -343,9 +343,30 @@ MOE_API int moe_combine_f16(const uint16_t* y16, const float* row_scale,
  *   (in stream order) before its first kernel, and its kernels record there
  *   the bounded waits that expire; moe_workspace_status() reads it. Two
  *   forwards in flight at once need two workspaces.
+ *   A batch of at most 4 tokens on router_logits (no router_w), with y in
+ *   fp32, a supported shape (moe_forward_single_launch) and 16-byte aligned
+ *   s_gu and s_d, runs as one
+ *   cooperative launch of one CTA per SM ("Ultimate Latency Optimization of
+ *   Qwen3 and Qwen3-VL on AMD MI300X Series", sections 2.1.4-2.1.5: the
+ *   small-batch MoE is bound by streaming the chosen experts' weights, and
+ *   the per-token steps are fused into their neighbours): the same steps and
+ *   roundings, products summed in another fp32 order, every intermediate
+ *   left in the workspace as the chained kernels leave it; a grid-wide
+ *   barrier whose wait expires sets error bit 5 (1 << 5). It runs only when
+ *   the environment variable MOE_SMALL_FORWARD=1 is set (off by default:
+ *   slower than the chained kernels on GB300).
  * Errors: those of the steps; MOE_ERR_WORKSPACE if ws_bytes is too small.
  */
 MOE_API size_t moe_forward_workspace_size(const moe_dims* dims);
+
+/*
+ * moe_forward_single_launch - 1 when moe_forward (router_weights = 0: given
+ *   logits, 1: router_w) or moe_forward_prenorm (prenorm = 1) with these dims
+ *   runs as the single cooperative launch described at moe_forward, 0 when
+ *   it chains its kernels, a negative status for invalid dims. Host only.
+ */
+MOE_API int moe_forward_single_launch(const moe_dims* dims, int router_weights,
+                                      int prenorm);
 MOE_API int moe_forward(const moe_dims* dims, const uint16_t* x,
                         const float* router_logits, const uint16_t* router_w,
                         const uint8_t* w_gu, const float* s_gu,

@@ -322,6 +322,50 @@ def test_forward_is_deterministic():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+# ---------------------------------------------------------------------------
+# a few tokens: the single-launch forward
+# ---------------------------------------------------------------------------
+SINGLE_LAUNCH = [
+    syn.LayerConfig("f1", 2, 512, 64, 8, 256, True, "normal"),
+    syn.LayerConfig("f2", 3, 256, 4, 3, 128, False, "normal"),     # experts shared by tokens
+    syn.LayerConfig("f3", 4, 1024, 128, 6, 512, True, "normal", False),
+    syn.LayerConfig("f4", 1, 4096, 512, 10, 1024, True, "normal"),  # the T=1 sweep shape
+    syn.LayerConfig("f5", 3, 2048, 1024, 32, 128, False, "normal"),   # k = 32, E = 1024
+    syn.LayerConfig("f6", 1, 128, 8, 1, 128, True, "normal"),      # one row per group
+]
+
+
+@pytest.mark.parametrize("cfg", SINGLE_LAUNCH, ids=lambda c: c.name)
+def test_single_launch_layer(cfg):
+    """Batches of at most four tokens on given logits: every token, stage by
+    stage against the oracle from the intermediates the forward leaves in
+    the workspace; chained kernels by default, one cooperative launch with
+    MOE_SMALL_FORWARD=1 (the next test)."""
+    import os
+    from expert_layer_ptpc_gb300 import binding
+    run = _Run(cfg)
+    expect = os.environ.get("MOE_SMALL_FORWARD", "0") == "1"
+    assert binding.moe_forward_single_launch(run.layer.dims(cfg.T)) == expect
+    run.check(cfg)
+
+
+def test_single_launch_variant():
+    """The same small layers, the T=1 sweep point and a guard-band case with
+    the single-launch forward turned on (MOE_SMALL_FORWARD=1), in a child
+    process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_SMALL_FORWARD="1")
+    cmd = [sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+           os.path.join(root, "tests", "test_gpu_layer.py"), "-k",
+           "test_single_launch_layer or test_sweep_layer[1] or g6"]
+    r = subprocess.run(cmd, env=env, cwd=root, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
+
+
 def test_empty_batch_is_noop():
     cfg = syn.LayerConfig("empty", 0, 256, 8, 2, 128, False, "normal")
     run = _Run(syn.LayerConfig("empty", 4, 256, 8, 2, 128, False, "normal"))
@@ -338,6 +382,7 @@ def test_empty_batch_is_noop():
     syn.LayerConfig("g3", 40, 256, 12, 2, 128, True, "weights"),      # exact router GEMM
     syn.LayerConfig("g4", 256, 1024, 16, 4, 256, False, "weights"),   # fused router
     syn.LayerConfig("g5", 9000, 256, 8, 2, 128, False, "normal"),     # multi-block permute
+    syn.LayerConfig("g6", 3, 1024, 64, 8, 512, True, "normal"),       # single launch
 ], ids=lambda c: c.name)
 def test_forward_leaves_guard_bands_intact(cfg):
     """Canaries in place of a memory checker: the forward workspace is filled
