@@ -100,8 +100,10 @@ def parity_tokens(ids, E, shared, n_min=256, seed=0):
     * the first and the last row of every expert that has rows;
     * both rows on either side of every tile boundary inside an expert's
       slice: every 64 rows (which covers the 64-, 128- and 256-row token
-      tiles and the 256-token CTA-pair tiles), or every 16 rows when the
-      experts average at most 32 rows (the 16- and 32-row tiles);
+      tiles), or every 16 rows when the experts average at most 32 rows (the
+      16- and 32-row tiles), and the boundaries of the CTA-pair kernels'
+      balanced tiles (an expert of r rows cut into t = ceil(r / bn) tiles of
+      32 * ceil(ceil(r / t) / 32) rows, bn = 192 or 256);
     * for the shared expert (one row per token, group E after the routed
       rows): the first and last token, and the tokens on either side of its
       first four and last four tile boundaries;
@@ -121,6 +123,12 @@ def parity_tokens(ids, E, shared, n_min=256, seed=0):
         rows.update((a, b - 1))
         for m in range(a + step, b, step):
             rows.update((m - 1, m))
+        r = b - a
+        for bn in (192, 256):
+            t = -(-r // bn)
+            w = (-(-r // t) + 31) // 32 * 32
+            for m in range(a + w, b, w):
+                rows.update((m - 1, m))
     toks = {int(s2f[s]) // k for s in rows}
     if shared and T > 0:
         toks.update((0, T - 1))
