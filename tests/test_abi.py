@@ -141,3 +141,38 @@ def test_checked_build_exports_the_same_symbols():
                          text=True, check=True).stdout
     names = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
     assert {n for n in names if n.startswith("moe_")} == set(binding.exported_names())
+
+
+_SINGLE_LAUNCH_PROBE = r"""
+import sys
+sys.path.insert(0, {root!r})
+from expert_layer_ptpc_gb300 import binding as B
+q = B.moe_forward_single_launch
+print(int(q(B.make_dims(1, 4096, 512, 10, 1024, 1, 1))),           # the T=1 sweep point
+      int(q(B.make_dims(4, 1024, 128, 6, 512, 1, 0))),             # four tokens
+      int(q(B.make_dims(5, 1024, 128, 6, 512, 1, 1))),             # five: chained
+      int(q(B.make_dims(1, 4096, 512, 10, 1024, 1, 1), router_weights=True)),
+      int(q(B.make_dims(1, 4096, 512, 10, 1024, 1, 1), prenorm=True)),
+      int(q(B.make_dims(4, 8192, 64, 4, 512, 0, 1))))              # x rows too long
+"""
+
+
+@pytest.mark.parametrize("mode,expect", [(None, "0 0 0 0 0 0"), ("1", "1 1 0 0 0 0")])
+def test_single_launch_rule_needs_no_gpu(lib, mode, expect):
+    """moe_forward_single_launch answers on the host: the one-launch forward
+    is off unless MOE_SMALL_FORWARD=1, and then applies to at most 4 tokens
+    on given logits without pre-norm, on shapes whose x and h rows fit its
+    buffers (child processes: the switch is read once)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    env.pop("MOE_SMALL_FORWARD", None)
+    if mode is not None:
+        env["MOE_SMALL_FORWARD"] = mode
+    r = subprocess.run([sys.executable, "-c", _SINGLE_LAUNCH_PROBE.format(root=root)],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.split() == expect.split()
+    bad = binding.make_dims(1, 100, 8, 2, 128, 0, 1)     # D not a multiple of 128
+    assert lib.moe_forward_single_launch(ctypes.byref(bad), 0, 0) < 0
