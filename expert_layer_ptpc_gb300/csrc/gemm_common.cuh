@@ -419,5 +419,9 @@ int wide_tiles_mode();
 // run; unset (0): from the rows per expert.
 int pair_bn_mode();
 
+// K atoms (128 bytes of K each) per stage of the gate/up CTA-pair kernel:
+// 2 (default) where K is a multiple of 256, MOE_GEMM_KATOMS=1 one.
+int pair_k_atoms();
+
 }  // namespace gemm
 }  // namespace moe

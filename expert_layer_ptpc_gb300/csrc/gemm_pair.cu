@@ -146,7 +146,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false>
+template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false, int KS = 1>
 struct PairCfg {
   static constexpr int kHalfB = BN / 2;                  // token rows per CTA
   // TMA boxes of one stage (per CTA): the weights in one 128-row box
@@ -156,16 +156,30 @@ struct PairCfg {
   static constexpr int kTBoxRows = kHalfB % 64 == 0 ? 64 : kHalfB;   // BN 192: one 96-row box
   static constexpr int kTBoxes = kHalfB / kTBoxRows;
   static constexpr int kBoxes = kWBoxes + kTBoxes;
-  static constexpr int kATile = 128 * kBK;               // this CTA's 128 MMA rows
-  static constexpr int kBTile = kHalfB * kBK;
+  // A stage holds KS atoms of K (128 bytes each): the K blocks x, x + 128,
+  // ... of the weights (A), then of the tokens (B), atom after atom. The
+  // MMA issuer pays a fixed cost per stage (one full-barrier wait, one
+  // commit) besides one per MMA, so two atoms (eight MMAs) per stage halve
+  // the first where the tiles are narrower than 256 tokens.
+  static constexpr int kAAtom = 128 * kBK;               // this CTA's 128 MMA rows
+  static constexpr int kBAtom = kHalfB * kBK;
+  static constexpr int kATile = KS * kAAtom;
+  static constexpr int kBTile = KS * kBAtom;
   static constexpr int kStage = kATile + kBTile;
   static constexpr int kStages = (kStageBudget / kStage) > 10 ? 10 : (kStageBudget / kStage);
   // Producer warps per box: one thread issues a TMA copy about every 0.35 us
-  // on GB300, so when the warps allow, two warps share each box and take
-  // alternate stages (warp 2b: even stages, 2b + 1: odd ones). An even
-  // stage count keeps each ring slot with one warp of a box.
-  static constexpr int kPar = (2 * kBoxes <= kMaxBoxes && kStages % 2 == 0) ? 2 : 1;
+  // on GB300, so where the warps allow, kPar warps share each box and take
+  // turns by stage (warp kPar*b + p: the stages q with q % kPar == p).
+  // One-atom stages keep two warps per box with an even stage count; the
+  // twice larger two-atom stages take up to three.
+  static constexpr int kPar =
+      KS == 1 ? ((2 * kBoxes <= kMaxBoxes && kStages % 2 == 0) ? 2 : 1)
+              : (kMaxBoxes / kBoxes >= 3 ? 3 : kMaxBoxes / kBoxes >= 2 ? 2 : 1);
   static_assert(kBoxes * kPar <= kMaxBoxes, "producer warps");
+  // a warp's next stage in a slot waits for the slot's previous stage, at
+  // most one phase back (no parity aliasing) when kPar <= kStages
+  static_assert(kPar <= kStages, "producer turns");
+  static_assert(KS == 1 || !WIDE, "two-atom stages: narrow tiles");
   static constexpr int kAccBufs = 2 * BN <= 512 ? 2 : 1;
   static constexpr int kTmemCols = pow2_at_least(kAccBufs * BN);
   static constexpr int kChunk = 32;                      // epilogue columns per pass
@@ -237,8 +251,8 @@ __device__ __forceinline__ bool token_box(int t, int n, int row0, int rank, int&
 
 // OUT16 (down projection only): y as fp16 codes plus one factor per row, the
 // encoding of the single-CTA kernel (gemm_tc.cu, fp16_rho).
-template <int BN, bool GATEUP, bool OUT16, bool WIDE>
-__global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1)
+template <int BN, bool GATEUP, bool OUT16, bool WIDE, int KS>
+__global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE, KS>::kThreadsT, 1)
     grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap tm_w,
     const __grid_constant__ CUtensorMap tm_a,
@@ -248,7 +262,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
     __half* __restrict__ out16, float* __restrict__ row_scale,
     const float* __restrict__ w_bound, int balanced, unsigned* __restrict__ err) {
   static_assert(!(OUT16 && GATEUP), "fp16 output is for the down projection");
-  using C = PairCfg<BN, GATEUP, OUT16, WIDE>;
+  using C = PairCfg<BN, GATEUP, OUT16, WIDE, KS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -267,7 +281,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
   const uint32_t rank = cluster_rank();        // 0: the leader issues the MMAs
   const int first_tile = (int)cluster_index();  // handed out first
   const int n_ctiles = N / C::kTileCh;
-  const int kblocks = K / kBK;
+  const int kblocks = K / (kBK * KS);   // stages of a tile
 
   // full (leader's is the one used): both halves of a stage landed;
   // empty: stage free in this CTA (the leader's multicast commit)
@@ -366,22 +380,27 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
     const bool weight_box = box < C::kWBoxes;
     if (lane == 0 && box < C::kBoxes) {
       const uint64_t pol = weight_box ? l2_policy_evict_normal() : l2_policy_evict_last();
-      // bytes of this box in one CTA; the leader expects both CTAs' bytes
+      // bytes of this box in one CTA (all atoms of the stage); the leader
+      // expects both CTAs' bytes
       const uint32_t bytes =
-          (uint32_t)((weight_box ? C::kWBoxRows : C::kTBoxRows) * kBK);
+          (uint32_t)(KS * (weight_box ? C::kWBoxRows : C::kTBoxRows) * kBK);
       auto issue = [&](int s, int kb, const TileInfo& ti) {
-        const int x = kb * kBK;
-        if (GATEUP && box == 0) {   // gate and up rows of this CTA's 64 channels
-          tma_load_5d(stage_a(s), &tm_w, x, (ti.ctile * 128 + (int)rank * 64) / 16,
-                      ti.group, rank == 0 ? full_bar(s) : map_to_rank(full_bar(s), 0),
-                      pol, rank != 0);
-        } else if (weight_box) {    // down: this CTA's 128 rows
-          load(stage_a(s), &tm_w, x, weight_row(ti), s, pol);
-        } else {                    // rows of this CTA's half of the token tile
-          int srow, trow;
-          if (token_box<WIDE, C::kTBoxRows>(box - C::kWBoxes, pair_width(ti), ti.row0, (int)rank, srow,
-                              trow))
-            load(stage_b(s) + srow * kBK, &tm_a, x, trow, s, pol);
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          const int x = (kb * KS + j) * kBK;
+          const uint32_t sa = stage_a(s) + j * C::kAAtom, sb = stage_b(s) + j * C::kBAtom;
+          if (GATEUP && box == 0) {   // gate and up rows of this CTA's 64 channels
+            tma_load_5d(sa, &tm_w, x, (ti.ctile * 128 + (int)rank * 64) / 16, ti.group,
+                        rank == 0 ? full_bar(s) : map_to_rank(full_bar(s), 0), pol,
+                        rank != 0);
+          } else if (weight_box) {    // down: this CTA's 128 rows
+            load(sa, &tm_w, x, weight_row(ti), s, pol);
+          } else {                    // rows of this CTA's half of the token tile
+            int srow, trow;
+            if (token_box<WIDE, C::kTBoxRows>(box - C::kWBoxes, pair_width(ti), ti.row0,
+                                              (int)rank, srow, trow))
+              load(sb + srow * kBK, &tm_a, x, trow, s, pol);
+          }
         }
       };
       // a token box past the tile's MMA width is not loaded by either CTA
@@ -392,9 +411,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
                                                         ti.row0, 0, srow, trow);
         mbar_arrive_expect_tx(full_bar(s), used ? 2 * bytes : 0u);
       };
-      int last_phase[C::kStages];
-#pragma unroll
-      for (int i = 0; i < C::kStages; ++i) last_phase[i] = -1;
+      int qlast = -1;   // the last stage this warp issued
       // q numbers this CTA's stages in order (tile by tile, K block by K
       // block); stage q fills slot q % kStages in phase (q / kStages) & 1,
       // and this warp issues the stages with q % kPar == par
@@ -409,9 +426,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
         for (int kb = par; kb < npre; kb += C::kPar) {   // fresh ring: phase 0
           expect(kb, t0);
           issue(kb, kb, t0);
-#pragma unroll
-          for (int i = 0; i < C::kStages; ++i)
-            if (i == kb) last_phase[i] = 0;
+          qlast = kb;
         }
         q = (uint32_t)npre;
       }
@@ -435,25 +450,20 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
           }
           expect(s, ti);
           issue(s, kb, ti);
-#pragma unroll
-          for (int i = 0; i < C::kStages; ++i)
-            if (i == s) last_phase[i] = (int)ph;
+          qlast = (int)q;
         }
       }
-      // drain: this CTA's copies have landed before its memory is released.
-      // The leader sees them (both halves) on its full barriers; the peer
-      // sees a stage consumed, hence landed, when the leader frees it.
-#pragma unroll
-      for (int i = 0; i < C::kStages; ++i) {
-        if (last_phase[i] >= 0) {
-          volatile int no_abort = 0;
-          if (rank == 0)
-            mbar_wait_bounded(full_bar(i), (uint32_t)last_phase[i], &no_abort, err,
-                              kErrTimeoutDrain);
-          else
-            wait_cluster_bounded(empty_bar(i), (uint32_t)last_phase[i], &no_abort,
-                                 err, kErrTimeoutDrain);
-        }
+      // drain: this warp's copies have landed before the CTA's memory is
+      // released. The MMA issuer consumes the stages in order, so once its
+      // commit has freed this warp's last stage (in both CTAs), every copy
+      // of the warp has landed. No later stage uses that slot (a warp's
+      // turns are kPar <= kStages stages apart), so the phase parity of the
+      // wait is unambiguous.
+      if (qlast >= 0) {
+        volatile int no_abort = 0;
+        wait_cluster_bounded(empty_bar(qlast % C::kStages),
+                             (uint32_t)(qlast / C::kStages) & 1u, &no_abort, err,
+                             kErrTimeoutDrain);
       }
     } else {
       pdl_wait();
@@ -490,13 +500,15 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a = stage_a(s), b = stage_b(s);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk) {
-            const uint64_t adesc = smem_desc_k_sw128(a + kk * 32);
-            mma_pair(d, adesc, smem_desc_k_sw128(b + kk * 32), idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < KS * kBK / 32; ++kk) {   // 32 K bytes per MMA
+            const int j = kk / (kBK / 32), k32 = (kk % (kBK / 32)) * 32;
+            const uint32_t a = stage_a(s) + j * C::kAAtom + k32;
+            const uint32_t b = stage_b(s) + j * C::kBAtom + k32;
+            const uint64_t adesc = smem_desc_k_sw128(a);
+            mma_pair(d, adesc, smem_desc_k_sw128(b), idesc, (kb | kk) != 0);
             if (WIDE && n2 > 0)   // columns 256.. from token rows 128.. of the stage
-              mma_pair(d + 256, adesc, smem_desc_k_sw128(b + 128 * kBK + kk * 32), idesc2,
+              mma_pair(d + 256, adesc, smem_desc_k_sw128(b + 128 * kBK), idesc2,
                        (kb | kk) != 0);
           }
           mma_commit_pair_mc(empty_bar(s), 0x3);   // stage free in both CTAs
@@ -578,6 +590,22 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
         const int nfirst = C::kChunk * eset;
         sx_next = nfirst + lane < nvalid ? a_scale[ti.row0 + nfirst + lane] : 0.f;
       }
+      // down: this thread's channel scale and, for fp16 output, the rows'
+      // factors a_scale / rho (written by the tile of the first channels)
+      const int ch_d = ti.ctile * 256 + (int)rank * 128 + m;
+      float sw_d = 0.f, swr_d = 0.f;
+      if constexpr (!GATEUP) {
+        sw_d = w_scale[(int64_t)ti.group * N + ch_d];
+        swr_d = sw_d;
+        if constexpr (OUT16) {
+          const float rho = fp16_rho(w_bound[ti.group], K);
+          swr_d = sw_d * rho;
+          if (ti.ctile == 0 && rank == 0) {   // one factor per row
+            for (int r = e_idx * 32 + lane; r < nvalid; r += 128 * C::kEpiSets)
+              row_scale[ti.row0 + r] = __fdiv_rn(a_scale[ti.row0 + r], rho);
+          }
+        }
+      }
       if (!warp_wait_cluster(accf_bar(ab), acc_ph, abort_flag, err,
                              kErrTimeoutEpilogue))
         break;
@@ -638,17 +666,8 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
           }
         }
       } else {
-        const int ch = ti.ctile * 256 + (int)rank * 128 + m;
-        const float sw = w_scale[(int64_t)ti.group * N + ch];
-        float swr = sw;
-        if constexpr (OUT16) {
-          const float rho = fp16_rho(w_bound[ti.group], K);
-          swr = sw * rho;
-          if (ti.ctile == 0 && rank == 0) {   // one factor per row
-            for (int r = e_idx * 32 + lane; r < nvalid; r += 128 * C::kEpiSets)
-              row_scale[ti.row0 + r] = __fdiv_rn(a_scale[ti.row0 + r], rho);
-          }
-        }
+        const int ch = ch_d;
+        const float sw = sw_d, swr = swr_d;
         for (int n0 = 32 * eset; n0 < nvalid; n0 += 32 * C::kEpiSets) {
           float acc[32];
           tmem_ld_x16(taddr + n0, *reinterpret_cast<float(*)[16]>(&acc[0]));
@@ -687,13 +706,14 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE>::kThreadsT, 1
   }
 }
 
-template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false>
+template <int BN, bool GATEUP, bool OUT16 = false, bool WIDE = false, int KS = 1>
 int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
              const uint8_t* W, const float* w_scale, const int32_t* offsets,
              int groups, int N, int K, float* out, cudaStream_t stream, bool pdl,
              int balanced, __half* out16 = nullptr, float* row_scale = nullptr,
              const float* w_bound = nullptr) {
-  using C = PairCfg<BN, GATEUP, OUT16, WIDE>;
+  using C = PairCfg<BN, GATEUP, OUT16, WIDE, KS>;
+  if (K % (kBK * KS) != 0) return -1;
   CUtensorMap tm_w, tm_a;
   if (GATEUP) {   // one box: 64 channels' gate and up rows, interleaved by 16
     if (!make_tmap_gateup_interleaved(&tm_w, W, groups, N, K)) return -3;
@@ -706,7 +726,7 @@ int run_pair(const uint8_t* A, const float* a_scale, int64_t a_rows,
                         ? make_tmap_out(&tm_out, out16, a_rows, N, C::kOutRows, 32, 2)
                         : make_tmap_out(&tm_out, out, a_rows, N, C::kOutRows, C::kOutCols, 4);
   if (!made) return -3;
-  auto kern = grouped_gemm_pair_kernel<BN, GATEUP, OUT16, WIDE>;
+  auto kern = grouped_gemm_pair_kernel<BN, GATEUP, OUT16, WIDE, KS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -3;
@@ -752,20 +772,38 @@ int launch_grouped_gemm_pair(int kind, const uint8_t* A, const float* a_scale,
     if (bn > 256)   // wide tiles are always balanced
       return run_pair<512, true, false, true>(A, a_scale, a_rows, W, w_scale, offsets,
                                               groups, N, K, out, stream, pdl, 1);
+    // two K atoms per stage where K allows
+    const bool ks2 = pair_k_atoms() == 2 && K % (2 * kBK) == 0;
     if (bn == 192)
-      return run_pair<192, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
-                                 out, stream, pdl, bal);
+      return ks2 ? run_pair<192, true, false, false, 2>(A, a_scale, a_rows, W, w_scale,
+                                                        offsets, groups, N, K, out, stream,
+                                                        pdl, bal)
+                 : run_pair<192, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
+                                       K, out, stream, pdl, bal);
     if (bn <= 128)
-      return run_pair<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                 K, out, stream, pdl, bal);
-    return run_pair<256, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
-                               out, stream, pdl, bal);
+      return ks2 ? run_pair<128, true, false, false, 2>(A, a_scale, a_rows, W, w_scale,
+                                                        offsets, groups, N, K, out, stream,
+                                                        pdl, bal)
+                 : run_pair<128, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
+                                       K, out, stream, pdl, bal);
+    return ks2 ? run_pair<256, true, false, false, 2>(A, a_scale, a_rows, W, w_scale,
+                                                      offsets, groups, N, K, out, stream,
+                                                      pdl, bal)
+               : run_pair<256, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
+                                     out, stream, pdl, bal);
   }
+  const bool ks2 = pair_k_atoms() == 2 && K % (2 * kBK) == 0;
   if (bn <= 128)
-    return run_pair<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                K, out, stream, pdl, bal);
-  return run_pair<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
-                              out, stream, pdl, bal);
+    return ks2 ? run_pair<128, false, false, false, 2>(A, a_scale, a_rows, W, w_scale,
+                                                       offsets, groups, N, K, out, stream,
+                                                       pdl, bal)
+               : run_pair<128, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
+                                      K, out, stream, pdl, bal);
+  return ks2 ? run_pair<256, false, false, false, 2>(A, a_scale, a_rows, W, w_scale,
+                                                     offsets, groups, N, K, out, stream, pdl,
+                                                     bal)
+             : run_pair<256, false>(A, a_scale, a_rows, W, w_scale, offsets, groups, N, K,
+                                    out, stream, pdl, bal);
 }
 
 int launch_grouped_gemm_pair_down_f16(const uint8_t* A, const float* a_scale,
@@ -776,12 +814,21 @@ int launch_grouped_gemm_pair_down_f16(const uint8_t* A, const float* a_scale,
                                       cudaStream_t stream, bool pdl) {
   __half* o = reinterpret_cast<__half*>(y16);
   const int bal = balanced_tiles();
+  const bool ks2 = pair_k_atoms() == 2 && K % (2 * kBK) == 0;
   if (bn <= 128)
-    return run_pair<128, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups,
-                                      N, K, nullptr, stream, pdl, bal, o, row_scale,
-                                      w_bound);
-  return run_pair<256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups, N,
-                                    K, nullptr, stream, pdl, bal, o, row_scale, w_bound);
+    return ks2 ? run_pair<128, false, true, false, 2>(A, a_scale, a_rows, W, w_scale,
+                                                      offsets, groups, N, K, nullptr,
+                                                      stream, pdl, bal, o, row_scale,
+                                                      w_bound)
+               : run_pair<128, false, true>(A, a_scale, a_rows, W, w_scale, offsets,
+                                            groups, N, K, nullptr, stream, pdl, bal, o,
+                                            row_scale, w_bound);
+  return ks2 ? run_pair<256, false, true, false, 2>(A, a_scale, a_rows, W, w_scale, offsets,
+                                                    groups, N, K, nullptr, stream, pdl, bal,
+                                                    o, row_scale, w_bound)
+             : run_pair<256, false, true>(A, a_scale, a_rows, W, w_scale, offsets, groups,
+                                          N, K, nullptr, stream, pdl, bal, o, row_scale,
+                                          w_bound);
 }
 
 }  // namespace moe

@@ -441,12 +441,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
       if (tile < 0) break;
       const int ab = it % C::kAccBufs;
       const uint32_t acc_ph = (uint32_t)(it / C::kAccBufs) & 1u;
-      if (!warp_wait(accf_bar(ab), acc_ph, abort_flag, err, kErrTimeoutEpilogue))
-        break;
-      tc_fence_after_sync();
       const int nvalid = min(BN, ti.row_end - ti.row0);
-      const uint32_t taddr =
-          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
+      // What does not depend on the accumulators is read (and the rows'
+      // factors written) while the MMAs finish, off the epilogue's path.
       // fp16 output: y16 = acc * s_d * rho with rho from the expert's scale
       // bound, so |y16| <= 60000 whatever the data; the row's factor
       // a_scale / rho (written once, by the tile of the first channels)
@@ -459,6 +456,19 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
             row_scale[ti.row0 + r] = __fdiv_rn(a_scale[ti.row0 + r], rho);
         }
       }
+      // down projection, staged output: each 128-channel half's channel scale
+      float sw_half[C::kNumA];
+#pragma unroll
+      for (int which = 0; which < C::kNumA; ++which)
+        sw_half[which] = !GATEUP && C::kStagedOut
+                             ? w_scale[(int64_t)ti.group * N + ti.ctile * BMW +
+                                       which * 128 + q * 32 + lane]
+                             : 0.f;
+      if (!warp_wait(accf_bar(ab), acc_ph, abort_flag, err, kErrTimeoutEpilogue))
+        break;
+      tc_fence_after_sync();
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
       if (GATEUP && C::kPacked) {
         // lanes 0-63: gate of channels ctile*64 + m; lanes 64-127: up of the
         // same channels. Up values pass to the gate threads through xbuf.
@@ -527,7 +537,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMW, GATEUP, OUT16, MINB>::kThreadsT, 
        for (int which = 0; which < C::kNumA; ++which) {   // 128-channel halves
         const int ch0 = ti.ctile * BMW + which * 128 + q * 32;
         const uint32_t ta = taddr + (uint32_t)(which * BN);
-        const float sw = w_scale[(int64_t)ti.group * N + ch0 + lane];
+        const float sw = sw_half[which];
         const float swr = sw * rho;
         for (int n0 = 32 * eset; n0 < nvalid; n0 += 32 * C::kEpiSets) {
           float acc[32], v[32];
@@ -762,6 +772,14 @@ int pair_bn_mode() {
     return b == 128 || b == 192 || b == 256 ? b : 0;
   }();
   return bn;
+}
+
+int pair_k_atoms() {
+  static const int ks = [] {
+    const char* v = std::getenv("MOE_GEMM_KATOMS");
+    return (v != nullptr && v[0] == '1') ? 1 : 2;
+  }();
+  return ks;
 }
 
 int balanced_tiles() {

@@ -497,7 +497,8 @@ def test_combine_f16(T, k, D, shared):
     {"MOE_GEMM_CTA_PAIR": "0"},
     {"MOE_GEMM_WIDE": "1"},
     {"MOE_GEMM_WIDE": "0"},
-], ids=["pair", "pair-unbalanced", "single", "wide", "no-wide"])
+    {"MOE_GEMM_CTA_PAIR": "1", "MOE_GEMM_KATOMS": "1"},
+], ids=["pair", "pair-unbalanced", "single", "wide", "no-wide", "pair-katoms1"])
 def test_grouped_gemm_cta_pair_variant(switches):
     """The wide-tile cases with the kernel choice forced, in a child process:
     MOE_GEMM_CTA_PAIR=1 runs the CTA-pair (cta_group::2) kernel for every
@@ -506,7 +507,9 @@ def test_grouped_gemm_cta_pair_variant(switches):
     take the pair). MOE_GEMM_BALANCED=0 cuts the pair kernel's token tiles
     into full ones and a partial tail instead of equal widths.
     MOE_GEMM_WIDE=1 / =0 turns the 512-token gate/up tiles (two MMAs per K
-    step) on / off above 256 rows per expert."""
+    step) on / off above 256 rows per expert. MOE_GEMM_KATOMS=1 gives the
+    gate/up pair kernel stages of one 128-byte K atom (the form that K not a
+    multiple of 256 takes) instead of two."""
     import os
     import subprocess
     import sys
