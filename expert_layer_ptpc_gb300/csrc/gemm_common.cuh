@@ -37,12 +37,15 @@ constexpr int pow2_at_least(int v) {
 // for an expert whose largest weight scale is `bound`: every product of two
 // e4m3 codes is at most 448^2 in magnitude, so |acc| <= 448^2 K and
 // |acc * s_d * rho| <= 60000 < 65504 (the largest finite fp16) for every
-// s_d <= bound. Computed in fp64, once per tile, so every CTA gets the same
-// value.
+// s_d <= bound. Computed in fp32 as ((60000 / 448^2) / K) / bound with IEEE
+// divisions, once per tile, so every CTA gets the same value; its three
+// roundings leave |acc * s_d * rho| below 60000.02, which fp16 rounds to at
+// most 60000. (The fp64 form cost each epilogue warp about 900 cycles per
+// tile on GB300's narrow fp64 pipe.)
 __device__ __forceinline__ float fp16_rho(float bound, int K) {
-  double r = 60000.0 / (200704.0 * (double)K * (double)bound);
-  if (!(r <= 3.0e38)) r = 3.0e38;   // a zero bound: any finite factor works
-  return (float)r;
+  float r = __fdiv_rn(__fdiv_rn(60000.0f / 200704.0f, (float)K), bound);
+  if (!(r <= 3.0e38f)) r = 3.0e38f;   // a zero bound: any finite factor works
+  return r;
 }
 
 struct TileInfo {
@@ -142,6 +145,16 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
+}
+// Relaxed arrive on another CTA's barrier, for a signal that publishes no
+// memory: an epilogue warp telling the MMA issuer that its tcgen05.ld of an
+// accumulator have completed (tcgen05.wait::ld, then
+// tcgen05.fence::before_thread_sync). The release form made the peer CTA's
+// epilogue warps wait about 2,800 cycles per tile on GB300.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                    cluster_addr)
                : "memory");
 }

@@ -690,7 +690,7 @@ __global__ void __launch_bounds__(PairCfg<BN, GATEUP, OUT16, WIDE, KS>::kThreads
       __syncwarp();
       if (lane == 0) {
         if (rank == 0) mbar_arrive(acce_bar(ab));
-        else mbar_arrive_cluster(map_to_rank(acce_bar(ab), 0));
+        else mbar_arrive_cluster_relaxed(map_to_rank(acce_bar(ab), 0));
       }
     }
     if (lane == 0) bulk_wait_all();   // this warp's TMA stores are complete

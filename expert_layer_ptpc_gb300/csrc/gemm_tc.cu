@@ -870,15 +870,16 @@ int launch_grouped_gemm_down_f16(const uint8_t* A, const float* a_scale,
                                  cudaStream_t stream, bool pdl) {
   if (a_rows == 0 || groups == 0) return 0;
   const int64_t avg = rows_hint > 0 ? rows_hint : std::max<int64_t>(1, a_rows / groups);
-  // From 512 rows per expert on, 256-token tiles run on a CTA pair: one
-  // M = 256 MMA of 256 channels per K step, each SM loading 128 weight rows
-  // and half of the token tile (prefill 0.399 -> 0.387 ms). With fewer rows
-  // per expert the pair's narrowed tail tiles cost more than the feed it
-  // saves (T=16384: 0.97 -> 1.08 ms, T=4096 at 128-token tiles: 0.38 ->
-  // 0.61 ms). MOE_GEMM_DOWN_PAIR=1 / =0 (or MOE_GEMM_CTA_PAIR=1 / =0) forces
-  // the pair (above 64 rows per expert) or the single CTA.
+  // From 256 rows per expert on, token tiles of up to 256 rows (balanced
+  // widths) run on a CTA pair: one M = 256 MMA of 256 channels per K step,
+  // each SM loading 128 weight rows and half of the token tile, so a weight
+  // tile is read once per 256 tokens instead of once per 128 (T=16384, 320
+  // rows per expert: 0.860 -> 0.773 ms; prefill 0.399 -> 0.334 ms). At 80
+  // rows per expert (T=4096) the single CTA's 128-token tiles stay ahead
+  // (0.386 vs 0.413 ms). MOE_GEMM_DOWN_PAIR=1 / =0 (or MOE_GEMM_CTA_PAIR=1 /
+  // =0) forces the pair (above 64 rows per expert) or the single CTA.
   const int dm = down_pair_mode() >= 0 ? down_pair_mode() : cta_pair_mode();
-  const bool pair = dm == 1 ? avg > 64 : dm == 0 ? false : avg >= 512;
+  const bool pair = dm == 1 ? avg > 64 : dm == 0 ? false : avg >= 256;
   if (pair && grouped_gemm_pair_supported(1, N))
     return launch_grouped_gemm_pair_down_f16(
         A, a_scale, a_rows, W, w_scale, w_bound, offsets, groups, N, K, y16, row_scale,

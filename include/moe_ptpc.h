@@ -279,7 +279,8 @@ MOE_API int moe_combine(const float* y, const int32_t* flat_to_sorted,
  * largest outputs; fp16 keeps 11 bits and halves y's HBM traffic against
  * fp32. Its range is guaranteed by construction:
  *   y16[r, n] = fp16_rne( acc[r, n] * w_scale[g, n] * rho_g ),
- *   rho_g = 60000 / (448^2 * K * w_bound[g])   (computed in fp64 -> fp32),
+ *   rho_g = 60000 / (448^2 * K * w_bound[g])   (in fp32: ((60000 / 448^2) / K)
+ *                                               / w_bound[g], IEEE divisions),
  *   row_scale[r] = a_scale[r] / rho_g           (IEEE fp32 division),
  * so that y[r, n] = row_scale[r] * y16[r, n] up to fp16 rounding, where acc
  * is the fp32 dot product of the codes. Every product of two e4m3 codes is
