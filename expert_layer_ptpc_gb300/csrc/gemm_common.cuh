@@ -40,7 +40,7 @@ constexpr int pow2_at_least(int v) {
 // s_d <= bound. Computed in fp32 as ((60000 / 448^2) / K) / bound with IEEE
 // divisions, once per tile, so every CTA gets the same value; its three
 // roundings leave |acc * s_d * rho| below 60000.02, which fp16 rounds to at
-// most 60000. (The fp64 form cost each epilogue warp about 900 cycles per
+// most 60000. (The fp64 form cost each epilogue warp 700-900 cycles per
 // tile on GB300's narrow fp64 pipe.)
 __device__ __forceinline__ float fp16_rho(float bound, int K) {
   float r = __fdiv_rn(__fdiv_rn(60000.0f / 200704.0f, (float)K), bound);
@@ -152,7 +152,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 // memory: an epilogue warp telling the MMA issuer that its tcgen05.ld of an
 // accumulator have completed (tcgen05.wait::ld, then
 // tcgen05.fence::before_thread_sync). The release form made the peer CTA's
-// epilogue warps wait about 2,800 cycles per tile on GB300.
+// epilogue warps wait 2,000-3,200 cycles per tile on GB300.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                    cluster_addr)
