@@ -18,16 +18,22 @@
 //            lane quarter, 16 lanes apart;
 //   down:    256 output channels, 128 per CTA.
 //
-// Roles per CTA (11 warps), both CTAs of the pair:
+// Roles per CTA (12 warps, 16 with the second epilogue set), both CTAs of
+// the pair:
 //   warp 0      TMEM allocation (both CTAs); the MMA issuer (leader)
-//   warps 1-4   epilogue on this CTA's TMEM rows
-//   warps 5-10  TMA producers, one box each: this CTA's weight box(es) and
-//               its token boxes, into its own ring of stages; both CTAs'
-//               copies complete on the leader's stage barrier, which expects
-//               both halves
+//   warps 1-4   epilogue on this CTA's TMEM rows (12-15: a second set taking
+//               every other 32-token chunk, for the down projection's fp16
+//               output and the wide tiles)
+//   warps 5-10  TMA producers: up to three per box (this CTA's weight box,
+//               its token boxes), taking turns by stage, into its own ring
+//               of stages of one or two 128-byte K atoms; both CTAs' copies
+//               complete on the leader's stage barrier, which expects both
+//               halves
+//   warp 11     tile scheduler (cluster launch control)
 // The leader's commits are multicast to both CTAs (stage free, accumulator
 // ready); both CTAs' epilogues release an accumulator buffer by arriving on
-// the leader's barrier. All waits are bounded (common.cuh).
+// the leader's barrier (the peer with a relaxed arrive: the signal publishes
+// no memory). All waits are bounded (common.cuh).
 #include <cuda_fp16.h>
 
 #include <algorithm>

@@ -819,10 +819,10 @@ int launch_grouped_gemm(int kind, const uint8_t* A, const float* a_scale,
                     : pair_mode == 0 ? false
                                      : kind == 0 && avg >= 256;
   // From 256 to 384 rows per expert an expert takes two balanced tiles of at
-  // most 192 tokens: a 28 KB stage leaves room for seven in the ring instead
-  // of six 32 KB ones, and the ring's copy latency bounds these tiles
-  // (uniform 320 rows per expert 1.156 -> 1.105 ms, T=16384 gate/up 1.289 ->
-  // 1.257 ms).
+  // most 192 tokens. With one-atom stages their 28 KB stage left room for
+  // seven in the ring instead of six 32 KB ones (uniform 320 rows per expert
+  // 1.156 -> 1.105 ms, T=16384 gate/up 1.289 -> 1.257 ms); with two-atom
+  // stages (K a multiple of 256) the ring holds three of 56 KB.
   // Tiles of up to 512 tokens (two MMAs per K step, one accumulator buffer)
   // move 25-30% fewer operand bytes per FLOP, but their epilogue cannot
   // overlap the next tile's MMAs: on GB300 they tie at 320 rows per expert
