@@ -1,5 +1,7 @@
-"""A host model of the CTA-pair GEMM's stage ring, checked under random
-interleavings (no GPU).
+"""Host models of the grouped GEMMs' mbarrier protocols, checked under
+random interleavings (no GPU): the CTA-pair stage ring, the accumulator
+buffers between the MMA issuer and the epilogue warps, and the scheduler's
+tile ring.
 
 The kernel's producer warps take turns by stage: warp p of a box issues the
 stages q with q % P == p into slot q % S, after waiting for the slot's
@@ -112,3 +114,148 @@ def test_more_turns_than_slots_aliases():
     """With P > S a warp can reach a slot two uses ahead of its barrier,
     where the parity wait passes wrongly: the model must catch it."""
     assert any(simulate(2, 3, 1, 30, seed)[0] for seed in range(300))
+
+
+def simulate_accumulators(A, warps, tiles, seed):
+    """The accumulator buffers between the MMA issuer and the epilogue warps:
+    tile i uses buffer i % A; the issuer waits until every epilogue warp has
+    released the buffer's previous tile (acce), then commits it full (accf);
+    each epilogue warp waits for accf, reads, and arrives on acce."""
+    rng = random.Random(seed)
+    accf = [0] * A           # completed phases: a tile's accumulators ready
+    acce = [0] * A           # completed phases: every warp released a tile
+    arrivals = [0] * A
+    bad = []
+    mma_next = 0
+    epi_next = [0] * warps
+
+    def check(hw, intended, what):
+        if hw != intended:
+            bad.append(what)
+        return hw
+
+    def mma():
+        nonlocal mma_next
+        i = mma_next
+        if i >= tiles:
+            return
+        b, j = i % A, i // A
+        if check(parity_wait(acce[b], (j & 1) ^ 1), acce[b] >= j, ("mma", i, acce[b])):
+            accf[b] += 1
+            mma_next += 1
+
+    def epi(w):
+        i = epi_next[w]
+        if i >= tiles:
+            return
+        b, j = i % A, i // A
+        if check(parity_wait(accf[b], j & 1), accf[b] >= j + 1, ("epi", w, i, accf[b])):
+            arrivals[b] += 1
+            if arrivals[b] == warps:
+                arrivals[b] = 0
+                acce[b] += 1
+            epi_next[w] += 1
+
+    for _ in range(tiles * (warps + 2) * 60):
+        if bad or (mma_next >= tiles and min(epi_next) >= tiles):
+            break
+        a = rng.randrange(warps + 1)
+        if a == warps:
+            mma()
+        else:
+            epi(a)
+    return bad, mma_next >= tiles and min(epi_next) >= tiles
+
+
+def simulate_tile_ring(R, consumers, tiles, seed):
+    """The scheduler's tile ring: the scheduler publishes tiles 0..tiles-1
+    and the end marker into slot n % R once every consumer has read the
+    slot's previous entry; each consumer reads every entry in order. One
+    consumer (the first producer) also marks each tile it takes, and the
+    scheduler waits for that mark before it asks for the next tile."""
+    rng = random.Random(seed)
+    full = [0] * R
+    empty = [0] * R
+    arrivals = [0] * R
+    taken = 0
+    bad = []
+    published = 0              # entries published (tiles, then the marker)
+    waits_taken = 0
+    pending_take = False
+    read = [0] * consumers
+    ring = [None] * R
+
+    def check(hw, intended, what):
+        if hw != intended:
+            bad.append(what)
+        return hw
+
+    def sched():
+        nonlocal published, waits_taken, pending_take
+        if published > tiles:
+            return
+        if pending_take:
+            m = waits_taken
+            if not check(parity_wait(taken, m & 1), taken >= m + 1, ("taken", m, taken)):
+                return
+            waits_taken += 1
+            pending_take = False
+            return
+        n = published
+        s, r = n % R, n // R
+        if not check(parity_wait(empty[s], (r & 1) ^ 1), empty[s] >= r,
+                     ("publish", n, empty[s])):
+            return
+        ring[s] = n if n < tiles else -1
+        full[s] += 1
+        published += 1
+        pending_take = n < tiles
+
+    def consume(c):
+        nonlocal taken
+        n = read[c]
+        if n > tiles:
+            return
+        s, r = n % R, n // R
+        if not check(parity_wait(full[s], r & 1), full[s] >= r + 1, ("read", c, n, full[s])):
+            return
+        t = ring[s]
+        if t != (n if n < tiles else -1):
+            bad.append(("value", c, n, t))
+        arrivals[s] += 1
+        if arrivals[s] == consumers:
+            arrivals[s] = 0
+            empty[s] += 1
+        if c == 0 and t >= 0:
+            taken += 1
+        read[c] += 1
+
+    for _ in range((tiles + 2) * (consumers + 2) * 80):
+        if bad or (published > tiles and min(read) > tiles):
+            break
+        a = rng.randrange(consumers + 1)
+        if a == consumers:
+            sched()
+        else:
+            consume(a)
+    return bad, published > tiles and min(read) > tiles
+
+
+@pytest.mark.parametrize("A,warps", [(1, 4), (2, 4), (2, 8), (2, 16), (1, 16)])
+def test_accumulator_buffers_never_alias(A, warps):
+    for seed in range(30):
+        for tiles in (1, 2, 3, 7, 33):
+            bad, done = simulate_accumulators(A, warps, tiles, seed * 100 + tiles)
+            assert not bad, (A, warps, tiles, seed, bad[:3])
+            assert done, (A, warps, tiles, seed)
+
+
+@pytest.mark.parametrize("consumers", [5, 11, 15, 19])
+def test_tile_ring_never_aliases(consumers):
+    """kRing = 4 slots; consumers as sched_init counts them (producer warps,
+    epilogue warps and, in the leader, the MMA issuer)."""
+    for seed in range(20):
+        for tiles in (0, 1, 3, 4, 5, 17):
+            bad, done = simulate_tile_ring(4, consumers, tiles, seed * 100 + tiles)
+            assert not bad, (consumers, tiles, seed, bad[:3])
+            assert done, (consumers, tiles, seed)
